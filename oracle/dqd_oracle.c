@@ -1,0 +1,403 @@
+/*
+ * CPU oracle for the memory-bound decode hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path (the CUDA library, its
+ * Python binding) may include, link, import or call this file. Only the tests,
+ * the package's smoke check and the benchmark's CPU-baseline leg use it.
+ * It shares no code, header, table or constant generator with the CUDA path.
+ *
+ * Every routine is the plain definition, evaluated in double precision with no
+ * blocking, fusion or reordering beyond what the definition states. Where a
+ * step decides an integer (an FP8 code), it is taken in the precision the
+ * method fixes for it (IEEE binary32, the kernel's precision) and says so.
+ *
+ * Sources (web pages; the section is named in each routine):
+ *   [MTC]  "降低每個 Token 的生成成本" (Making each token cheaper), optiverse-tech.com
+ *   [LIF]  "LLM 推理是怎么变快的" (How LLM inference gets fast), random.sdx88.com
+ *   [CS10] "第 10 讲：推理" (CS336 lecture 10 notes), semidirectx.com
+ *   [ATC]  "AcceptedTokens 阅读笔记" (reading notes on speculative-decoding energy), zhongzhuzhou.org
+ *
+ * Readings taken where the pages are silent (each is listed in the design doc):
+ *   - INT4 g128: unsigned codes 0..15 with a 4-bit zero point and a bf16 scale
+ *     per 128-weight group; deq = bf16_RNE((q - z) * s), one rounding.
+ *   - FP8 row-wise: scale = fp32(max|w|) / 448 (IEEE binary32 division),
+ *     code = e4m3_RNE_satfinite(fp32(w) / scale); a row of zeros takes scale 1.
+ *   - Paged KV layout [block][kv_head][16][d]; GQA groups are contiguous
+ *     (kv head = q head / (Hq/Hkv)); the W verify tokens are already in the
+ *     cache, query i sits at position ctx - W + i and sees keys 0..ctx-W+i.
+ *
+ * Builds with any C11 compiler (x86_64 and aarch64); OpenMP is optional.
+ * Do not build with -ffast-math: the FP8 quantiser relies on IEEE binary32.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_EXPORT __attribute__((visibility("default")))
+
+/* ------------------------------------------------------------------------ */
+/* bf16: the upper 16 bits of an IEEE binary32.                              */
+/* ------------------------------------------------------------------------ */
+
+static double bf16_to_double(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+ORC_EXPORT double orc_bf16_to_double(uint16_t h) { return bf16_to_double(h); }
+
+/* Round a real number to the nearest bf16 (8 significant bits, exponent range
+ * of binary32), ties to the even significand, overflow to infinity. Written
+ * from the format: the quantum of the binade holding |v| is 2^(e-7), with the
+ * subnormal quantum 2^-133 below 2^-126. */
+ORC_EXPORT uint16_t orc_bf16_round(double v) {
+  if (isnan(v)) return 0x7FC0;
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = fabs(v);
+  if (a == 0.0) return sign;
+  int e2;
+  (void)frexp(a, &e2);          /* a = f * 2^e2 with f in [0.5, 1) */
+  int lead = e2 - 1;            /* exponent of the leading bit      */
+  if (lead < -126) lead = -126; /* subnormal binade                 */
+  double quantum = ldexp(1.0, lead - 7);
+  double r = nearbyint(a / quantum) * quantum; /* default mode: ties to even */
+  if (r >= 0x1p128) return sign | 0x7F80;
+  float f = (float)r; /* exact: r has at most 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return sign | (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 E4M3 [MTC, "格式" (Formats)]: 4 exponent bits, 3 mantissa bits, largest */
+/* normal 448. Bias 7, subnormals, no infinities, S.1111.111 is NaN.          */
+/* ------------------------------------------------------------------------ */
+
+ORC_EXPORT double orc_e4m3_decode(uint8_t c) {
+  int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  double mag = (e == 0) ? ldexp((double)m, -9)          /* m/8 * 2^-6     */
+                        : ldexp((double)(8 + m), e - 10); /* (1+m/8) 2^(e-7) */
+  return s ? -mag : mag;
+}
+
+/* Round-to-nearest-even onto the finite E4M3 grid, saturating magnitudes at
+ * or above 448 to 448 ("satfinite"); NaN stays NaN. Brute force over the 127
+ * non-negative finite codes, so that nothing but the grid itself is assumed. */
+ORC_EXPORT uint8_t orc_e4m3_encode(float v) {
+  if (isnan(v)) return 0x7F;
+  uint8_t sign = signbit(v) ? 0x80 : 0;
+  double a = fabs((double)v);
+  if (a >= 448.0) return sign | 0x7E;
+  int best = 0;
+  double best_d = a; /* distance to code 0 (value 0) */
+  for (int c = 1; c <= 0x7E; ++c) {
+    double d = fabs(orc_e4m3_decode((uint8_t)c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return sign | (uint8_t)best;
+}
+
+/* FP8 row-wise weight quantiser [MTC, "格式" (Formats): values are multiplied
+ * by a scale before the cast so that they fit the narrow range]. The scale
+ * maps the row's largest magnitude onto 448. Decides integer codes, so it runs
+ * in IEEE binary32 like the kernel. W is bf16 [n][k] row-major. */
+ORC_EXPORT void orc_quant_fp8_rowwise(const uint16_t* w, int64_t n, int64_t k,
+                                      uint8_t* codes, float* scales) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < n; ++r) {
+    const uint16_t* row = w + r * k;
+    float amax = 0.0f;
+    for (int64_t j = 0; j < k; ++j) {
+      float a = fabsf((float)bf16_to_double(row[j]));
+      if (a > amax) amax = a;
+    }
+    float scale = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+    scales[r] = scale;
+    for (int64_t j = 0; j < k; ++j) {
+      float v = (float)bf16_to_double(row[j]) / scale;
+      codes[r * k + j] = orc_e4m3_encode(v);
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* INT4 g128 weight-only (W4A16) [MTC, "格式" (Formats): 4-bit integers, one    */
+/* scale per group of 128, dequantised to 16-bit before the arithmetic;        */
+/* CS10 §5.2 for the scale/zero-point form].                                  */
+/* ------------------------------------------------------------------------ */
+
+static uint16_t int4_deq(uint8_t q, uint8_t z, uint16_t s) {
+  /* (q - z) * s has at most 12 significant bits: exact in double. */
+  return orc_bf16_round((double)((int)q - (int)z) * bf16_to_double(s));
+}
+
+/* deq[n][k] (bf16) from codes u8 [n][k] (0..15), scales bf16 [n][k/128],
+ * zeros u8 [n][k/128] (0..15). */
+ORC_EXPORT void orc_int4_dequant(const uint8_t* codes, const uint16_t* scales,
+                                 const uint8_t* zeros, int64_t n, int64_t k,
+                                 uint16_t* deq) {
+  int64_t groups = k / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < n; ++r)
+    for (int64_t j = 0; j < k; ++j)
+      deq[r * k + j] = int4_deq(codes[r * k + j], zeros[r * groups + j / 128],
+                                scales[r * groups + j / 128]);
+}
+
+/* The packed INT4 g128 layout, as documented in include/dqd.h:
+ *   NT = ceil(n/16) row tiles, G = k/128 groups, block b = T*G + g.
+ *   Codes: 1024-byte blocks of 256 little-endian 32-bit words. Word
+ *   w = 128*h + 4*l + j (h in 0..1, l in 0..31, j in 0..3); i = 4h + j,
+ *   c = i/2, e = i%2, r0 = l/4, t = l%4. Nibble v (bits 4v..4v+3) holds the
+ *   code of row 16T + r0 + 8*(v&1), column 128g + 32c + 8t + 4e
+ *   + 2*((v>>1)&1) + (v>>2). Rows at or beyond n hold 0.
+ *   Scales: 32-byte blocks of 8 words; word r0 = bf16 scale of row 16T+r0
+ *   (bits 0..15) and of row 16T+r0+8 (bits 16..31).
+ *   Zeros: 8-byte blocks; byte r0 = zero of row 16T+r0 (bits 0..3) and of
+ *   row 16T+r0+8 (bits 4..7).
+ * The two routines below are each other's inverse and are written from that
+ * description alone. */
+static void int4_layout_position(int64_t T, int64_t g, int w, int v,
+                                 int64_t* row, int64_t* col) {
+  int h = w / 128, l = (w / 4) % 32, j = w % 4;
+  int i = 4 * h + j, c = i / 2, e = i % 2, r0 = l / 4, t = l % 4;
+  *row = 16 * T + r0 + 8 * (v & 1);
+  *col = 128 * g + 32 * c + 8 * t + 4 * e + 2 * ((v >> 1) & 1) + (v >> 2);
+}
+
+ORC_EXPORT void orc_int4_pack(const uint8_t* codes, const uint16_t* scales,
+                              const uint8_t* zeros, int64_t n, int64_t k,
+                              uint8_t* packed, uint8_t* packed_scales,
+                              uint8_t* packed_zeros) {
+  int64_t NT = (n + 15) / 16, G = k / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t T = 0; T < NT; ++T) {
+    for (int64_t g = 0; g < G; ++g) {
+      int64_t b = T * G + g;
+      for (int w = 0; w < 256; ++w) {
+        uint32_t word = 0;
+        for (int v = 0; v < 8; ++v) {
+          int64_t row, col;
+          int4_layout_position(T, g, w, v, &row, &col);
+          uint32_t q = (row < n) ? (codes[row * k + col] & 15u) : 0u;
+          word |= q << (4 * v);
+        }
+        for (int byte = 0; byte < 4; ++byte)
+          packed[b * 1024 + 4 * w + byte] = (uint8_t)(word >> (8 * byte));
+      }
+      for (int r0 = 0; r0 < 8; ++r0) {
+        int64_t lo = 16 * T + r0, hi = lo + 8;
+        uint16_t s_lo = (lo < n) ? scales[lo * G + g] : 0;
+        uint16_t s_hi = (hi < n) ? scales[hi * G + g] : 0;
+        uint8_t z_lo = (lo < n) ? (zeros[lo * G + g] & 15u) : 0;
+        uint8_t z_hi = (hi < n) ? (zeros[hi * G + g] & 15u) : 0;
+        uint8_t* sw = packed_scales + b * 32 + 4 * r0;
+        sw[0] = (uint8_t)(s_lo & 0xFF);
+        sw[1] = (uint8_t)(s_lo >> 8);
+        sw[2] = (uint8_t)(s_hi & 0xFF);
+        sw[3] = (uint8_t)(s_hi >> 8);
+        packed_zeros[b * 8 + r0] = (uint8_t)(z_lo | (z_hi << 4));
+      }
+    }
+  }
+}
+
+/* Decoder of the packed layout back to logical codes/scales/zeros. Rows at or
+ * beyond n are checked to be zero; returns the number of nonzero padding
+ * entries found (0 for a well-formed buffer). */
+ORC_EXPORT int64_t orc_int4_unpack(const uint8_t* packed,
+                                   const uint8_t* packed_scales,
+                                   const uint8_t* packed_zeros, int64_t n,
+                                   int64_t k, uint8_t* codes, uint16_t* scales,
+                                   uint8_t* zeros) {
+  int64_t NT = (n + 15) / 16, G = k / 128, bad = 0;
+  for (int64_t T = 0; T < NT; ++T) {
+    for (int64_t g = 0; g < G; ++g) {
+      int64_t b = T * G + g;
+      for (int w = 0; w < 256; ++w) {
+        const uint8_t* p = packed + b * 1024 + 4 * w;
+        uint32_t word = (uint32_t)p[0] | ((uint32_t)p[1] << 8) |
+                        ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+        for (int v = 0; v < 8; ++v) {
+          int64_t row, col;
+          int4_layout_position(T, g, w, v, &row, &col);
+          uint8_t q = (uint8_t)((word >> (4 * v)) & 15u);
+          if (row < n)
+            codes[row * k + col] = q;
+          else
+            bad += (q != 0);
+        }
+      }
+      for (int r0 = 0; r0 < 8; ++r0) {
+        const uint8_t* sw = packed_scales + b * 32 + 4 * r0;
+        uint16_t s_lo = (uint16_t)(sw[0] | (sw[1] << 8));
+        uint16_t s_hi = (uint16_t)(sw[2] | (sw[3] << 8));
+        uint8_t zb = packed_zeros[b * 8 + r0];
+        int64_t lo = 16 * T + r0, hi = lo + 8;
+        if (lo < n) {
+          scales[lo * G + g] = s_lo;
+          zeros[lo * G + g] = zb & 15u;
+        } else {
+          bad += (s_lo != 0) + ((zb & 15u) != 0);
+        }
+        if (hi < n) {
+          scales[hi * G + g] = s_hi;
+          zeros[hi * G + g] = zb >> 4;
+        } else {
+          bad += (s_hi != 0) + ((zb >> 4) != 0);
+        }
+      }
+    }
+  }
+  return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* dq_gemm: y = x * deq(W)^T [MTC, "量化省下什麼" (What quantisation saves):      */
+/* a quantised matrix times a full-precision vector, weights dequantised on   */
+/* the fly, activations not quantised]. x bf16 [m][k], W [n][k], y [m][n].    */
+/* ------------------------------------------------------------------------ */
+
+enum { ORC_W_BF16 = 0, ORC_W_FP8_E4M3 = 1, ORC_W_INT4_G128 = 2 };
+
+/* Dequantised weight value of W[r][j] as a real number.
+ *   BF16: the weight itself.
+ *   FP8:  the E4M3 value; the per-row scale multiplies the whole dot product.
+ *   INT4: bf16_RNE((q - z) * s). */
+static double weight_value(int wtype, const void* data, const void* scales,
+                           const uint8_t* zeros, int64_t k, int64_t r,
+                           int64_t j) {
+  switch (wtype) {
+    case ORC_W_BF16:
+      return bf16_to_double(((const uint16_t*)data)[r * k + j]);
+    case ORC_W_FP8_E4M3:
+      return orc_e4m3_decode(((const uint8_t*)data)[r * k + j]);
+    default: {
+      int64_t G = k / 128;
+      uint8_t q = ((const uint8_t*)data)[r * k + j];
+      return bf16_to_double(int4_deq(q, zeros[r * G + j / 128],
+                                     ((const uint16_t*)scales)[r * G + j / 128]));
+    }
+  }
+}
+
+/* Computes y[mi][ri] = sum_j x[mi][j] * value(W[rows[ri]][j]) (times the FP8
+ * row scale) for the listed rows (all n rows when rows == NULL; then
+ * nrows must equal n). y is [m][nrows] double. Returns 0, or -1 on bad
+ * arguments. */
+ORC_EXPORT int orc_dq_gemm(int wtype, const void* data, const void* scales,
+                           const uint8_t* zeros, int64_t n, int64_t k,
+                           const uint16_t* x, int64_t m, const int64_t* rows,
+                           int64_t nrows, double* y) {
+  if (wtype < 0 || wtype > 2 || n < 0 || k < 0 || m < 0 || nrows < 0) return -1;
+  if (wtype == ORC_W_INT4_G128 && k % 128 != 0) return -1;
+  if (rows == NULL && nrows != n) return -1;
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t ri = 0; ri < nrows; ++ri) {
+    int64_t r = rows ? rows[ri] : ri;
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+    for (int64_t j = 0; j < k; ++j)
+      wrow[j] = weight_value(wtype, data, scales, zeros, k, r, j);
+    double rs = (wtype == ORC_W_FP8_E4M3) ? (double)((const float*)scales)[r] : 1.0;
+    for (int64_t mi = 0; mi < m; ++mi) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < k; ++j) acc += bf16_to_double(x[mi * k + j]) * wrow[j];
+      y[mi * nrows + ri] = rs * acc;
+    }
+    free(wrow);
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* GQA decode / verify attention over a paged KV cache.                       */
+/*   softmax(q K^T * scale) V for the new tokens' queries against every       */
+/*   cached key/value [CS10 §2.2: append the new K,V, then attend; LIF §2.1]; */
+/*   K/V read through a block table of 16-token blocks [LIF §3.1, CS10 §7.3]; */
+/*   Hq query heads share Hkv KV heads [LIF §2.3]; causal inside the draft    */
+/*   block [ATC, Algorithm 1: later candidates cannot affect earlier ones].   */
+/* q: bf16 [B][W][Hq][D]; k_pool, v_pool: bf16 [blocks][Hkv][16][D];          */
+/* block_table: int32 [B][max_blocks]; ctx: int32 [B].                        */
+/* Output rows are r = (b*W + i)*Hq + h; out is [nrows][D] double.            */
+/* Returns 0, or -1 on bad arguments / a violated precondition.               */
+/* ------------------------------------------------------------------------ */
+
+ORC_EXPORT int orc_gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool,
+                                   const uint16_t* v_pool,
+                                   const int32_t* block_table, int64_t max_blocks,
+                                   const int32_t* ctx, int64_t num_blocks,
+                                   int64_t B, int64_t W, int64_t Hq, int64_t Hkv,
+                                   int64_t D, double scale, const int64_t* rows,
+                                   int64_t nrows, double* out) {
+  const int64_t BS = 16;
+  if (B < 0 || W < 1 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return -1;
+  if (rows == NULL && nrows != B * W * Hq) return -1;
+  for (int64_t b = 0; b < B; ++b)
+    if (ctx[b] < W || (ctx[b] + BS - 1) / BS > max_blocks) return -1;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+  for (int64_t ri = 0; ri < nrows; ++ri) {
+    int64_t r = rows ? rows[ri] : ri;
+    int64_t h = r % Hq, i = (r / Hq) % W, b = r / (Hq * W);
+    int64_t g = h / (Hq / Hkv);
+    int64_t pos = ctx[b] - W + i; /* keys 0..pos are visible */
+    int64_t nk = pos + 1;
+    double* s = (double*)malloc(sizeof(double) * (size_t)nk);
+    const uint16_t* qr = q + r * D;
+    double smax = -INFINITY;
+    for (int64_t j = 0; j < nk; ++j) {
+      int32_t phys = block_table[b * max_blocks + j / BS];
+      if (phys < 0 || phys >= num_blocks) { err |= 1; phys = 0; }
+      const uint16_t* kr = k_pool + ((phys * Hkv + g) * BS + j % BS) * D;
+      double dot = 0.0;
+      for (int64_t d = 0; d < D; ++d) dot += bf16_to_double(qr[d]) * bf16_to_double(kr[d]);
+      s[j] = scale * dot;
+      if (s[j] > smax) smax = s[j];
+    }
+    double denom = 0.0;
+    for (int64_t j = 0; j < nk; ++j) {
+      s[j] = exp(s[j] - smax);
+      denom += s[j];
+    }
+    for (int64_t d = 0; d < D; ++d) out[ri * D + d] = 0.0;
+    for (int64_t j = 0; j < nk; ++j) {
+      int32_t phys = block_table[b * max_blocks + j / BS];
+      if (phys < 0 || phys >= num_blocks) phys = 0;
+      const uint16_t* vr = v_pool + ((phys * Hkv + g) * BS + j % BS) * D;
+      double p = s[j] / denom;
+      for (int64_t d = 0; d < D; ++d) out[ri * D + d] += p * bf16_to_double(vr[d]);
+    }
+    free(s);
+  }
+  return err ? -1 : 0;
+}
+
+ORC_EXPORT int orc_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Array forms of the scalar codecs, for the Python wrapper. */
+ORC_EXPORT void orc_e4m3_decode_n(const uint8_t* c, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_decode(c[i]);
+}
+ORC_EXPORT void orc_e4m3_encode_n(const float* v, int64_t n, uint8_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(v[i]);
+}
+ORC_EXPORT void orc_bf16_round_n(const double* v, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_round(v[i]);
+}
