@@ -1,0 +1,530 @@
+"""Benchmark of the decode hot path (dq_gemm + gqa_decode_attn) on GB300.
+
+One step = every call of the workload once: for the default workload (a
+Llama-3-8B-shaped decode layer at batch 1) the QKV, O, gate+up and down
+projections in BF16 and in INT4 g128 plus paged GQA attention over 8192
+tokens. Weights and KV are resident in HBM; every step reads them once.
+
+Metric: effective HBM GB/s = algorithmic bytes of the step (weights with their
+scales/zeros, activations, outputs, K/V, q, block table) / step time.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME]
+Under torchrun (N > 1) every rank runs an independent replica (the path has
+no exchange step); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from memory_bound_decode_dq_gb300 import bounds, configs, synth  # noqa: E402
+
+WTYPE_NAMES = configs.WTYPE_NAMES
+DEFAULT_WORKLOAD = "llama3_8b_b1"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                   choices=[w.__name__ for w in configs.ALL])
+    p.add_argument("--graph-steps", type=int, default=50, help="steps unrolled per CUDA graph")
+    p.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps (capped at 2000)")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def workload(name):
+    return {w.__name__: w for w in configs.ALL}[name]()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "memory_bound_decode_dq_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(f.encode())
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "begin":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.06 <= r[0] <= (self.t1 or 1e30) + 0.06]
+        use = inside if inside else rows
+        sm = [float(p[2]) for _, p in use if p[2].replace(".", "").isdigit()]
+        smax = [float(p[3]) for _, p in use if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, p in use:
+            for name, val in zip(names, p[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------- device workload ----
+
+class Call:
+    def __init__(self, name, kind, nbytes, flops, fn, launches):
+        self.name, self.kind, self.nbytes, self.flops, self.fn, self.launches = name, kind, nbytes, flops, fn, launches
+
+
+def build_calls(wl, dev, dqd):
+    """Inputs drawn on the device, outputs and workspaces preallocated; returns
+    the calls of one step and the host-visible inputs/outputs for e2e."""
+    import torch
+    calls = []
+    io = []  # (name, device input tensors, device output tensors)
+    for c in wl.gemms:
+        seed = wl.seed
+        x = synth.normal_bf16(seed, c.name + ".x", (c.m, c.k), device=dev)
+        if c.wtype == configs.W_INT4_G128:
+            wq = synth.int4_weight(seed, c.name, c.n, c.k, device=dev)
+            weight = dqd.Weight.int4(dqd.pack_int4_g128(wq.codes, wq.scales, wq.zeros))
+            del wq
+        else:
+            if c.outliers:
+                w = synth.bf16_weight_outliers_device(seed, c.name, c.n, c.k, 0.02, c.outliers, 20.0, dev)
+            else:
+                w = synth.normal_bf16(seed, c.name, (c.n, c.k), 0.02, device=dev)
+            if c.wtype == configs.W_BF16:
+                weight = dqd.Weight.bf16(w)
+            else:
+                codes, scales = dqd.quant_fp8_rowwise(w)
+                weight = dqd.Weight.fp8(codes, scales)
+                del w
+        y = torch.empty((c.m, c.n), dtype=torch.bfloat16, device=dev)
+        need = dqd.dq_gemm_workspace_bytes(weight, c.m)
+        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev) if need else None
+
+        def fn(weight=weight, x=x, y=y, ws=ws):
+            dqd.dq_gemm(weight, x, y=y, ws=ws)
+        calls.append(Call(c.name, "dq_gemm", bounds.dq_gemm_bytes(c.wtype, c.m, c.n, c.k),
+                          bounds.dq_gemm_flops(c.m, c.n, c.k), fn, 1))
+        io.append((c.name, [x], [y]))
+    for a in wl.attns:
+        seed = wl.seed
+        ctx = list(a.context)
+        table, nblk = synth.block_table(seed, a.name + ".table", ctx, a.shuffle)
+        shape = (nblk, a.hkv, 16, a.d)
+        kp = synth.normal_bf16(seed, a.name + ".k", shape, 1.0, device=dev)
+        vp = synth.normal_bf16(seed, a.name + ".v", shape, 1.0, device=dev)
+        q = synth.normal_bf16(seed, a.name + ".q", (a.batch, a.width, a.hq, a.d), device=dev)
+        table_t = torch.from_numpy(table).to(dev)
+        ctx_t = torch.tensor(ctx, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        maxc = max(ctx)
+        need = dqd.gqa_decode_attn_workspace_bytes(a.batch, a.width, a.hq, a.hkv, a.d, maxc)
+        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev) if need else None
+
+        def fn(q=q, kp=kp, vp=vp, table_t=table_t, ctx_t=ctx_t, out=out, ws=ws, maxc=maxc):
+            dqd.gqa_decode_attn(q, kp, vp, table_t, ctx_t, maxc, out=out, ws=ws)
+        calls.append(Call(a.name, "gqa_decode_attn", bounds.attn_bytes(ctx, a.width, a.hq, a.hkv, a.d),
+                          bounds.attn_flops(ctx, a.width, a.hq, a.d), fn, 2 if need else 1))
+        io.append((a.name, [q, table_t, ctx_t], [out]))
+    return calls, io
+
+
+def working_set_bytes(calls):
+    return sum(c.nbytes for c in calls)
+
+
+def run_ours(args, rank, world, dev):
+    import torch
+    import torch.distributed as dist
+    from memory_bound_decode_dq_gb300 import dqd
+
+    wl = workload(args.workload)
+    calls, io = build_calls(wl, dev, dqd)
+    step_bytes = sum(c.nbytes for c in calls)
+    launches_per_step = sum(c.launches for c in calls)
+    torch.cuda.synchronize()
+
+    # warm-up: eager steps (also sets kernel attributes before capture)
+    for _ in range(max(args.warmup, 3)):
+        for c in calls:
+            c.fn()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    G = max(1, min(args.graph_steps, K))
+    reps, rem = divmod(K, G)
+
+    def make_graph(nsteps, with_events):
+        evs = []
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for c in calls:
+                c.fn()
+        torch.cuda.current_stream().wait_stream(s)
+        with torch.cuda.graph(g):
+            for _ in range(nsteps):
+                row = []
+                for c in calls:
+                    if with_events:
+                        e0 = torch.cuda.Event(enable_timing=True, external=True)
+                        e1 = torch.cuda.Event(enable_timing=True, external=True)
+                        e0.record()
+                        c.fn()
+                        e1.record()
+                        row.append((e0, e1))
+                    else:
+                        c.fn()
+                evs.append(row)
+        return g, evs
+
+    try:
+        graph, events = make_graph(G, True)
+        have_events = True
+    except Exception:
+        graph, events = make_graph(G, False)
+        have_events = False
+    graph_rem = make_graph(rem, False)[0] if rem else None
+    for _ in range(2):  # warm replays
+        graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index if world == 1 else int(os.environ.get("LOCAL_RANK", 0)))
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler.mark("begin")
+    t_start.record()
+    for _ in range(reps):
+        graph.replay()
+    if graph_rem is not None:
+        graph_rem.replay()
+    t_end.record()
+    torch.cuda.synchronize()
+    sampler.mark("end")
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+    clocks = sampler.stop() if rank == 0 else None
+
+    # per-call durations from the events of the last replay of the timed graph
+    per_call = {}
+    if have_events:
+        for i, c in enumerate(calls):
+            d = [events[s][i][0].elapsed_time(events[s][i][1]) for s in range(G)]
+            per_call[c.name] = sum(d) / len(d)
+
+    # end-to-end through the public API with pinned host buffers
+    e2e = run_e2e(args, calls, io, dev, dqd, step_bytes, world)
+    return dict(wl=wl, calls=calls, step_bytes=step_bytes, launches=launches_per_step, max_ms=max_ms,
+                per_call=per_call, clocks=clocks, e2e=e2e, K=K)
+
+
+def run_e2e(args, calls, io, dev, dqd, step_bytes, world):
+    """Each step: copy the step's inputs (activations, queries, block table,
+    context lengths) from pinned host memory, run every call through the
+    binding, copy every output back, synchronise. Weights and KV stay
+    resident (they are model and cache state, not per-step inputs)."""
+    import torch
+    import torch.distributed as dist
+    host_in, host_out = [], []
+    h2d = d2h = 0
+    for _, ins, outs in io:
+        hi = [t.detach().cpu().pin_memory() for t in ins]
+        ho = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        host_in.append(hi)
+        host_out.append(ho)
+        h2d += sum(t.numel() * t.element_size() for t in hi)
+        d2h += sum(t.numel() * t.element_size() for t in ho)
+    steps = args.e2e_steps or min(args.steps, 2000)
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        for (name, ins, outs), hi in zip(io, host_in):
+            for d, h in zip(ins, hi):
+                d.copy_(h, non_blocking=True)
+        for c in calls:
+            c.fn()
+        for (name, ins, outs), ho in zip(io, host_out):
+            for d, h in zip(outs, ho):
+                h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        one_step()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    t = torch.tensor([dt], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dt = float(t.item())
+    return {"value": round(step_bytes * steps * world / dt / 1e9, 3), "unit": "GB/s",
+            "ms_per_step": round(1e3 * dt / steps, 4), "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+class OracleSample:
+    """A bounded sample of the workload for the CPU oracle: every call is
+    evaluated on a random subset of its output rows (same shapes and
+    distributions), the subset sized so that one run costs about budget_s
+    seconds. Inputs are drawn once; run() times only the oracle calls."""
+
+    def __init__(self, wl, budget_s, seed=1234):
+        import numpy as np
+
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        rng = np.random.default_rng(seed)
+        costs = [c.m * c.n * c.k for c in wl.gemms] + \
+                [sum(a.context) * a.width * a.hq * a.d * 2 for a in wl.attns]
+        rate = 1.5e8 * max(1, oracle.num_threads())  # oracle multiply-adds per second, roughly
+        self.frac = frac = min(1.0, budget_s * rate / float(sum(costs)))
+        self.jobs, self.covered = [], 0.0
+        for c in wl.gemms:
+            rows = max(1, int(round(c.n * frac)))
+            x = synth.normal_bf16(wl.seed, c.name + ".x", (c.m, c.k))
+            if c.wtype == configs.W_INT4_G128:
+                args = (rng.integers(0, 16, (rows, c.k), dtype=np.uint8),
+                        synth.uniform_bf16(wl.seed, c.name + ".s", (rows, c.k // 128), 0.005, 0.02),
+                        rng.integers(0, 16, (rows, c.k // 128), dtype=np.uint8))
+            else:
+                w = synth.f32_to_bf16_bits(rng.standard_normal((rows, c.k), dtype=np.float32) * 0.02)
+                args = (w, None, None) if c.wtype == configs.W_BF16 else oracle.quant_fp8_rowwise(w) + (None,)
+            self.jobs.append(lambda c=c, args=args, x=x: oracle.dq_gemm(c.wtype, *args, x))
+            self.covered += bounds.dq_gemm_bytes(c.wtype, c.m, c.n, c.k) * rows / c.n
+        for a in wl.attns:
+            # one (sequence, kv head) group: its heads at every verify position
+            G = a.hq // a.hkv
+            b = int(rng.integers(0, a.batch))
+            ctx = [a.context[b]]
+            kv = synth.paged_kv(seed, a.name + ".cpu", ctx, 1, a.d, shuffle=a.shuffle)
+            q = synth.normal_bf16(seed, a.name + ".cpu.q", (1, a.width, G, a.d))
+            rows_all = a.batch * a.width * a.hq
+            want = max(1, int(round(rows_all * frac)))
+            # cost of a row in this group relative to an average row
+            rel = a.context[b] / (sum(a.context) / a.batch)
+            nrows = max(1, min(a.width * G, int(round(want / max(rel, 1e-9)))))
+            pick = np.sort(rng.choice(a.width * G, nrows, replace=False))
+            self.jobs.append(lambda kv=kv, q=q, pick=pick, d=a.d: oracle.gqa_decode_attn(
+                q, kv.k_pool, kv.v_pool, kv.block_table, kv.context_lens, 1, 1 / math.sqrt(d), rows=pick))
+            per_row = bounds.attn_bytes(a.context, a.width, a.hq, a.hkv, a.d) / rows_all
+            self.covered += per_row * rel * nrows
+        self.threads = oracle.num_threads()
+        self.desc = (f"oracle on a random {frac:.4g} of every projection's output rows and on "
+                     f"sampled query rows of one (sequence, kv head) per attention call; "
+                     f"{self.threads} OpenMP threads")
+
+    def run(self) -> float:
+        t0 = time.perf_counter()
+        for j in self.jobs:
+            j()
+        return time.perf_counter() - t0
+
+
+def run_reference(args, rank, world):
+    wl = workload(args.workload)
+    total_steps = args.steps + args.warmup
+    # the whole reference run ends within a few minutes
+    per_step_budget = max(0.002, min(2.0, 150.0 / max(1, total_steps)))
+    sample = OracleSample(wl, per_step_budget)
+    for _ in range(args.warmup):
+        sample.run()
+    secs = sum(sample.run() for _ in range(args.steps))
+    value = sample.covered * args.steps / secs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": sample.threads, "kind": "oracle",
+                         "sample": sample.desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+METRIC = "effective HBM GB/s (% of GB300 peak) and us/call for dq_gemm + gqa_decode_attn"
+
+
+def traffic_for(kernel_call_name, workload_name):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return None
+    ent = d.get(workload_name, {}).get(kernel_call_name)
+    if not ent or ent.get("csrc_hash") != csrc_hash():
+        return None
+    return ent.get("dram_bytes")
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    r = run_ours(args, rank, world, dev)
+    if rank == 0:
+        wl, calls = r["wl"], r["calls"]
+        hbm, tf, tf_sus, peak_src = peaks()
+        step_s = r["max_ms"] / 1e3 / r["K"]
+        value = r["step_bytes"] * world / step_s / 1e9
+        per_call = r["per_call"]
+        calls_info = {}
+        for c in calls:
+            us = per_call.get(c.name, 0.0) * 1e3
+            gbs = c.nbytes / (us * 1e-6) / 1e9 if us > 0 else None
+            calls_info[c.name] = {"us": round(us, 3), "GB/s": round(gbs, 1) if gbs else None,
+                                  "frac_hbm": round(gbs / hbm, 4) if gbs else None, "bytes": int(c.nbytes)}
+        dom = max(calls, key=lambda c: per_call.get(c.name, 0.0)) if per_call else None
+        roof = None
+        if dom is not None and per_call.get(dom.name, 0) > 0:
+            dur = per_call[dom.name] / 1e3
+            ach = dom.nbytes / dur / 1e9
+            roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(ach / hbm, 4), "traffic": traffic_for(dom.name, wl.name),
+                    "kernel": dom.kind, "call": dom.name, "peak_source": peak_src,
+                    "algorithmic_bytes": int(dom.nbytes), "us_per_launch": round(per_call[dom.name] * 1e3, 3)}
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            sample = OracleSample(wl, args.cpu_seconds / 3)
+            secs = sum(sample.run() for _ in range(3))
+            cpu = {"value": round(3 * sample.covered / secs / 1e9, 4), "unit": "GB/s", "cores": sample.threads,
+                   "kind": "oracle", "sample": sample.desc + f"; 3 runs, {secs:.1f} s"}
+        ws_mb = working_set_bytes(calls) / 1e6
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size / 1e6
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": r["K"],
+            "warmup": max(args.warmup, 3), "ms_per_step": round(r["max_ms"] / r["K"], 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "calls": [c.name for c in calls],
+                       "l2": f"inputs larger than L2: every step streams {ws_mb:.0f} MB once ({ws_mb / l2:.1f}x the {l2:.0f} MB L2)",
+                       "timing": f"CUDA graphs of {min(args.graph_steps, r['K'])} steps with per-call timing events",
+                       "parallelism": f"replicas x{world}"},
+            "frac_of_peak": round(value / world / hbm, 4),
+            "per_call": calls_info,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": r["e2e"],
+            "gpu_launches": r["launches"] * r["K"],
+            "clocks": r["clocks"],
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

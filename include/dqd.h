@@ -1,0 +1,231 @@
+/*
+ * dqd — memory-bound LLM decode kernels for GB300 (sm_103a), C ABI.
+ *
+ * Two operations make up the hot path of one decode (or speculative-verify)
+ * step, and two offline operations prepare weights for it:
+ *
+ *   dq_gemm          y = x * deq(W)^T, a weight-only quantised skinny GEMM.
+ *   gqa_decode_attn  GQA attention of the new tokens' queries over a paged
+ *                    BF16 KV cache, causal inside the verify block.
+ *   pack_int4_g128   re-lay INT4 g128 codes/scales/zeros for dq_gemm.
+ *   quant_fp8_rowwise  BF16 W -> FP8 E4M3 codes + per-output-row fp32 scales.
+ *
+ * Sources (web pages):
+ *   [MTC]  "降低每個 Token 的生成成本" (Making each token cheaper), optiverse-tech.com
+ *   [LIF]  "LLM 推理是怎么变快的" (How LLM inference gets fast), random.sdx88.com
+ *   [CS10] "第 10 讲：推理" (CS336 lecture 10 notes), semidirectx.com
+ *   [ATC]  "AcceptedTokens 阅读笔记" (speculative-decoding energy notes), zhongzhuzhou.org
+ *
+ * Conventions for every call:
+ *   - Buffers are owned by the caller. Pointers named in a signature are
+ *     DEVICE pointers (unless documented otherwise) and must be 16-byte
+ *     aligned. The library never allocates, frees or synchronises.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     A status is returned after all host-side checks and the launches;
+ *     argument errors are detected on the host and returned before anything
+ *     is enqueued. Device-side faults surface at the caller's next sync.
+ *   - bf16 values are passed as uint16_t bit patterns.
+ *   - Workspace: calls that need scratch take (workspace, ws_bytes); query the
+ *     size with the *_workspace_bytes function for the same arguments on the
+ *     same device. The first DQD_WS_COUNTER_BYTES bytes of a workspace hold
+ *     arrival counters: they must be zero before the first call that uses
+ *     the buffer, and every call leaves them zero again. Calls that share a
+ *     workspace must not overlap on the GPU.
+ *   - Thread safety: calls may be made from several host threads; the last
+ *     error message is kept per host thread (dqd_last_error()).
+ */
+#ifndef DQD_H_
+#define DQD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DQD_API __attribute__((visibility("default")))
+#else
+#define DQD_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* dqd_stream;
+
+typedef enum {
+  DQD_OK = 0,
+  DQD_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or shape      */
+  DQD_ERR_UNSUPPORTED = 2, /* shape or parameter outside what the kernels do  */
+  DQD_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required      */
+  DQD_ERR_CUDA = 4         /* a CUDA runtime call or a launch failed          */
+} dqd_status;
+
+typedef enum {
+  DQD_W_BF16 = 0,      /* data: bf16 [n][k] row-major; scales, zeros: NULL   */
+  DQD_W_FP8_E4M3 = 1,  /* data: E4M3 codes u8 [n][k]; scales: fp32 [n];
+                          zeros: NULL                                        */
+  DQD_W_INT4_G128 = 2  /* data/scales/zeros: the packed buffers written by
+                          pack_int4_g128 (layout below)                      */
+} dqd_wtype;
+
+/* A weight matrix W [n out][k in]. */
+typedef struct {
+  int32_t type;        /* dqd_wtype */
+  int64_t n, k;
+  const void* data;
+  const void* scales;
+  const void* zeros;
+} dqd_weight;
+
+/* Bytes of arrival counters at the start of every workspace. */
+#define DQD_WS_COUNTER_BYTES 65536
+
+/* Human-readable name of a status; never NULL. */
+DQD_API const char* dqd_status_string(dqd_status status);
+
+/* Detail of the error of the last library call made on the calling host
+ * thread (empty string if it succeeded). Valid until that thread's next call. */
+DQD_API const char* dqd_last_error(void);
+
+/* Library version, e.g. "dqd 0.1 sm_103a". */
+DQD_API const char* dqd_version(void);
+
+/* ------------------------------------------------------------------------
+ * pack_int4_g128 — re-lay W4A16 INT4 g128 weights for dq_gemm.
+ *
+ * Source: [MTC, section "格式" (Formats)]: weight-only INT4 stores 4-bit
+ * integers with one scale per group (group size 128) and dequantises to
+ * 16-bit before the arithmetic; [CS10 §5.2] scale and zero point.
+ * Reading: codes are unsigned 0..15, the zero point is a 4-bit value per
+ * group, deq = bf16_RNE((q - z) * s).
+ *
+ * Inputs (device):
+ *   codes        u8 [n][k], values 0..15 (only the low 4 bits are read)
+ *   scales_bf16  bf16 [n][k/128]
+ *   zeros        u8 [n][k/128], values 0..15 (low 4 bits read)
+ * Outputs (device), sizes from pack_int4_g128_bytes:
+ *   packed, packed_scales, packed_zeros
+ * Requirements: n >= 1, k >= 128, k % 128 == 0, all pointers 16-byte aligned.
+ *
+ * Packed layout (frozen). NT = ceil(n/16) row tiles, G = k/128 groups,
+ * block b = T*G + g for row tile T and group g.
+ *   packed:        NT*G blocks of 1024 bytes = 256 little-endian uint32 words.
+ *                  Word w = 128*h + 4*l + j (h in 0..1, l in 0..31, j in 0..3).
+ *                  With i = 4h + j, c = i/2, e = i%2, r0 = l/4, t = l%4,
+ *                  nibble v (bits 4v..4v+3) of word w is the code of
+ *                    row    16*T + r0 + 8*(v & 1)
+ *                    column 128*g + 32*c + 8*t + 4*e + 2*((v >> 1) & 1) + (v >> 2)
+ *                  (This puts, for lane l of a warp, the A-operand fragment
+ *                  of eight m16n8k16 MMAs in two 16-byte loads.)
+ *   packed_scales: NT*G blocks of 8 uint32 words; word r0 holds the bf16
+ *                  scale of row 16T+r0 in bits 0..15 and of row 16T+r0+8 in
+ *                  bits 16..31.
+ *   packed_zeros:  NT*G blocks of 8 bytes; byte r0 holds the zero point of
+ *                  row 16T+r0 in bits 0..3 and of row 16T+r0+8 in bits 4..7.
+ *   Rows at or beyond n (padding of the last tile) hold 0 everywhere.
+ * Storage: 4 + 16/128 + 4/128 = 4.15625 bits per weight.
+ * ---------------------------------------------------------------------- */
+
+/* which: 0 = packed codes, 1 = packed scales, 2 = packed zeros.
+ * Returns 0 for invalid arguments. Host-only arithmetic. */
+DQD_API size_t pack_int4_g128_bytes(int64_t n, int64_t k, int which);
+
+DQD_API dqd_status pack_int4_g128(const uint8_t* codes, const uint16_t* scales_bf16,
+                          const uint8_t* zeros, int64_t n, int64_t k,
+                          void* packed, void* packed_scales, void* packed_zeros,
+                          dqd_stream stream);
+
+/* ------------------------------------------------------------------------
+ * quant_fp8_rowwise — BF16 W [n][k] -> FP8 E4M3 codes [n][k] + fp32 scales [n].
+ *
+ * Source: [MTC, section "格式" (Formats)]: E4M3 has 4 exponent bits, 3
+ * mantissa bits and largest normal 448; values are multiplied by a scale
+ * before the cast to fit that range. Reading: per output row n,
+ *   scale[n] = fp32(max_k |W[n][k]|) / 448        (IEEE binary32 division)
+ *   code[n][k] = e4m3_RNE_satfinite(fp32(W[n][k]) / scale[n])
+ * and a row whose entries are all zero takes scale 1. W must be finite.
+ * Requirements: n >= 1, k >= 1, k % 16 == 0, pointers 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+DQD_API dqd_status quant_fp8_rowwise(const uint16_t* w_bf16, int64_t n, int64_t k,
+                             uint8_t* codes, float* scales, dqd_stream stream);
+
+/* ------------------------------------------------------------------------
+ * dq_gemm — y[m][n] = sum_k x[m][k] * deq(W)[n][k], bf16 in/out, fp32 accumulate.
+ *
+ * Source: [MTC, section "量化省下什麼" (What quantisation saves)]: the decode
+ * kernel multiplies a quantised matrix by a full-precision vector,
+ * dequantising the weights on the fly without quantising the activations;
+ * [LIF §4.1] weight-only quantisation dequantises back to 16-bit and wins at
+ * small batch because decode is bandwidth-bound.
+ * Per weight type:
+ *   BF16: y = x W^T.
+ *   FP8:  y[m][n] = scale[n] * sum_k x[m][k] * e4m3(code[n][k]); the E4M3
+ *         value is exact in bf16 and the scale multiplies the fp32 sum.
+ *   INT4: y = x deq^T with deq = (q - z) * s of each 128-group; (q - z) is
+ *         formed exactly in bf16 and s multiplies each group's fp32 sum.
+ * Rounding: fp32 accumulation (tensor-core MMA), one fp32 -> bf16 RNE at the
+ * output. Summation order is fixed for a given (shape, device), so results
+ * are reproducible run to run.
+ *
+ * x: bf16 [m][k] row-major (device); y: bf16 [m][n] row-major (device).
+ * Requirements: 1 <= m <= 65536, n >= 1, k >= 0; k % 8 == 0 (BF16),
+ * k % 16 == 0 (FP8), k % 128 == 0 (INT4); pointers 16-byte aligned.
+ * m == 0 or n == 0 is a no-op; k == 0 writes zeros.
+ * Workspace: may be NULL when dq_gemm_workspace_bytes reports 0.
+ * ---------------------------------------------------------------------- */
+DQD_API dqd_status dq_gemm_workspace_bytes(const dqd_weight* w, int64_t m, size_t* bytes);
+
+DQD_API dqd_status dq_gemm(const dqd_weight* w, const uint16_t* x_bf16, int64_t m,
+                   uint16_t* y_bf16, void* workspace, size_t ws_bytes,
+                   dqd_stream stream);
+
+/* ------------------------------------------------------------------------
+ * gqa_decode_attn — paged GQA decode / speculative-verify attention.
+ *
+ * Sources: [CS10 §2.2] the new tokens' K,V are appended to the cache, then
+ * each new token's query attends to all cached K,V; [LIF §2.1]
+ * softmax(q K^T / sqrt(d)) V; [LIF §2.3] Hq query heads share Hkv KV heads;
+ * [LIF §3.1, CS10 §7.3] KV stored in 16-token blocks addressed through a
+ * block table; [MTC, section "注意力 Kernel"] split K/V into chunks processed
+ * in parallel, then combine (Flash-Decoding), exact online softmax
+ * (FlashAttention); [ATC, Algorithm 1] verify positions form one causal
+ * forward: later draft tokens cannot affect earlier ones.
+ *
+ * For sequence b, verify position i (0 <= i < w) and query head h:
+ *   kv head  g   = h / (hq / hkv)
+ *   position p   = context_lens[b] - w + i
+ *   out[b][i][h] = sum_{j<=p} softmax_j(softmax_scale * q[b][i][h] . K_j) V_j
+ * where K_j, V_j are row (j % 16) of physical block block_table[b][j / 16],
+ * kv head g.
+ *
+ * q:            bf16 [b][w][hq][d]              (device)
+ * k_pool,v_pool:bf16 [num_blocks][hkv][16][d]   (device)
+ * block_table:  int32 [b][max_blocks_per_seq]   (device)
+ * context_lens: int32 [b]                        (device); includes the w new
+ *               tokens, so context_lens[b] >= w is required
+ * max_context:  host upper bound of context_lens (plans the split)
+ * out:          bf16 [b][w][hq][d]              (device)
+ * Requirements: d == 128, 1 <= w <= 16, hq % hkv == 0, 1 <= b,
+ * max_context <= 16 * max_blocks_per_seq, num_blocks >= 1.
+ * Block-table entries outside [0, num_blocks) are clamped into range (the
+ * output is then meaningless, but no memory outside the pool is read).
+ * A query row that sees no key (context_lens[b] < w) is written as zeros.
+ * ---------------------------------------------------------------------- */
+DQD_API dqd_status gqa_decode_attn_workspace_bytes(int32_t b, int32_t w, int32_t hq,
+                                           int32_t hkv, int32_t d,
+                                           int32_t max_context, size_t* bytes);
+
+DQD_API dqd_status gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool,
+                           const uint16_t* v_pool, int64_t num_blocks,
+                           const int32_t* block_table, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, int32_t max_context,
+                           int32_t b, int32_t w, int32_t hq, int32_t hkv, int32_t d,
+                           float softmax_scale, uint16_t* out, void* workspace,
+                           size_t ws_bytes, dqd_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DQD_H_ */

@@ -1,0 +1,478 @@
+// gqa_decode_attn: paged GQA decode / speculative-verify attention.
+//
+// Sources: "第 10 讲：推理" (CS336 lecture 10 notes) §2.2 — append the new
+// tokens' K,V, then each new query attends to all cached K,V; "LLM 推理是怎么
+// 变快的" §2.1 softmax(q K^T / sqrt(d)) V, §2.3 GQA (query heads share KV heads),
+// §3.1 PagedAttention (16-token blocks + block table), §6.1 online softmax is
+// exact; "降低每個 Token 的生成成本" (Making each token cheaper), section
+// "注意力 Kernel": Flash-Decoding splits K/V into chunks processed in parallel
+// and combines them; "AcceptedTokens 阅读笔记", Algorithm 1: the verify
+// positions go through one causal forward.
+//
+// Work item = (sequence b, kv head g, chunk of the context, group of up to
+// four 16-row query tiles). The query rows of one kv head are the G = Hq/Hkv
+// heads at each of the W verify positions (row r -> position r / G, head
+// g*G + r % G). A CTA has 4 warps: warp = (query tile, key slot); the KS = 4/QT
+// key slots split each pipeline stage's blocks between them.
+//
+//  * K/V blocks (4 KB each per kv head) are gathered through the block table
+//    with cp.async into a 3-stage shared-memory ring. 16-byte unit u of key row
+//    r is stored at u ^ sigma(r), sigma(r) = ((r>>1)&3)<<1 ^ (r&1)<<2, which
+//    makes both the K loads (lanes differ in key and d) and the V loads (lanes
+//    differ in key pair and d) conflict-free.
+//  * S = Q K^T and O += P V run on mma.m16n8k16 (bf16 in, fp32 accumulate).
+//    For QK^T the head dimension is permuted inside each 32-wide chunk exactly
+//    like dq_gemm's k (lane t owns d = 32c + 8t .. +7) for both Q and K. For
+//    PV the B operand needs V[key 2t][d], V[key 2t+1][d] in one register: the
+//    lane loads 8 consecutive d of four keys and pairs them with prmt; the
+//    output column of n8 tile (h, jj), slot s is d = 64h + 8s + jj.
+//  * Online softmax in the log2 domain (ex2), masked keys -> -inf by select:
+//    key j is visible to row r iff j <= ctx - W + r / G. V rows past the
+//    context are zeroed before the MMA so stale pool contents cannot leak.
+//  * Warps sharing a query tile merge through shared memory; the CTA then
+//    either writes the normalised bf16 output (one chunk) or an fp32 partial
+//    (o, m, l) that attn_merge_kernel combines per output row.
+#include "dqd_device.cuh"
+#include "dqd_internal.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+
+namespace dqd {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBlk = 16;
+constexpr int kThreads = 128;
+constexpr int kStages = 3;
+constexpr int kBlockBytes = kBlk * kD * 2;  // one block, one kv head, K or V
+constexpr float kNegInf = -INFINITY;
+
+struct Args {
+  const uint16_t* q;
+  const uint16_t* kp;
+  const uint16_t* vp;
+  const int32_t* table;
+  const int32_t* ctx;
+  uint16_t* out;
+  float* part_o;   // [rows][nchunks][128]
+  float* part_ml;  // [rows][nchunks][2]
+  int64_t num_blocks;
+  int max_blocks, B, W, Hq, Hkv, G, QR;
+  int chunk_blocks, nchunks, qgroups;
+  float scale_log2;
+};
+
+__device__ __forceinline__ int sigma(int r) { return (((r >> 1) & 3) << 1) ^ ((r & 1) << 2); }
+
+__device__ __forceinline__ int seq_ctx(const Args& a, int b) {
+  int c = a.ctx[b];
+  return max(0, min(c, a.max_blocks * kBlk));
+}
+
+template <int QT>
+struct Smem {
+  static constexpr int KS = 4 / QT;
+  static constexpr int STAGE = KS * 2 * kBlockBytes;  // K and V of KS blocks
+  static constexpr int RING = kStages * STAGE;
+  static constexpr int MERGE = 4 * 16 * (kD + 2) * 4;  // (o, m, l) per warp-row
+  static constexpr int BYTES = RING > MERGE ? RING : MERGE;
+};
+
+// Gather the KS blocks of stage s (block indices blk0 + s*KS + i) into ring slot.
+template <int QT>
+__device__ __forceinline__ void stage_kv(uint32_t slot, const Args& a, int b, int g, int blk_first,
+                                         int blk_end) {
+  constexpr int KS = Smem<QT>::KS;
+  constexpr int UNITS = kBlockBytes / 16;  // 256 per K (or V) block
+#pragma unroll
+  for (int i = 0; i < KS * 2 * UNITS / kThreads; ++i) {
+    const int u = threadIdx.x + i * kThreads;
+    const int blk_local = u / (2 * UNITS);
+    const int kv = (u / UNITS) & 1;
+    const int unit = u % UNITS;
+    const int blk = blk_first + blk_local;
+    const bool ok = blk < blk_end;
+    int64_t phys = 0;
+    if (ok) {
+      phys = a.table[(int64_t)b * a.max_blocks + blk];
+      phys = phys < 0 ? 0 : (phys >= a.num_blocks ? a.num_blocks - 1 : phys);
+    }
+    const uint16_t* base = kv ? a.vp : a.kp;
+    const uint16_t* src = base + ((phys * a.Hkv + g) * kBlk) * kD + unit * 8;
+    const int r = unit >> 4, cu = unit & 15;
+    const uint32_t dst = slot + blk_local * 2 * kBlockBytes + kv * kBlockBytes +
+                         (r * 16 + (cu ^ sigma(r))) * 16;
+    cp_async16(dst, ok ? src : a.kp, ok);
+  }
+  cp_async_commit();
+}
+
+template <int QT>
+__global__ void __launch_bounds__(kThreads) attn_split_kernel(const Args a) {
+  using S = Smem<QT>;
+  constexpr int KS = S::KS;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, t = lane & 3;
+  const int chunk = blockIdx.x, g = blockIdx.y;
+  const int b = blockIdx.z / a.qgroups, qg = blockIdx.z % a.qgroups;
+  const int ctx = seq_ctx(a, b);
+  const int nblk_seq = (ctx + kBlk - 1) / kBlk;
+  const int blk0 = chunk * a.chunk_blocks;
+  if (blk0 >= nblk_seq) {  // whole CTA: nothing of this sequence here
+    if (a.nchunks == 1 && nblk_seq == 0) {
+      // empty context: the rows see no key and are written as zeros
+      for (int i = threadIdx.x; i < QT * 16 * kD / 2; i += kThreads) {
+        const int r = (qg * QT) * 16 + i / (kD / 2);
+        if (r < a.QR) {
+          const int64_t orow = ((int64_t)b * a.W + r / a.G) * a.Hq + g * a.G + r % a.G;
+          reinterpret_cast<uint32_t*>(a.out + orow * kD)[i % (kD / 2)] = 0u;
+        }
+      }
+    }
+    return;
+  }
+  const int blk_end = min(blk0 + a.chunk_blocks, nblk_seq);
+  const int nstages = (blk_end - blk0 + KS - 1) / KS;
+  const int qt = warp % QT, ks = warp / QT;
+  const int row_base = (qg * QT + qt) * 16;  // first query row of this warp's tile
+  const uint32_t sring = smem_addr(smem);
+
+  // Prologue: start two stages.
+  stage_kv<QT>(sring, a, b, g, blk0, blk_end);
+  if (nstages > 1) stage_kv<QT>(sring + S::STAGE, a, b, g, blk0 + KS, blk_end);
+
+  // Q fragments for this warp's 16 query rows, head dim permuted per 32-chunk.
+  uint32_t qf[4][2][4];
+  int pos_lo, pos_hi;  // last visible key index of rows gq and gq+8 (-1: none)
+  {
+    const int rl = row_base + gq, rh = rl + 8;
+    const bool okl = rl < a.QR, okh = rh < a.QR;
+    const int64_t ql = okl ? (((int64_t)b * a.W + rl / a.G) * a.Hq + g * a.G + rl % a.G) * kD : 0;
+    const int64_t qh = okh ? (((int64_t)b * a.W + rh / a.G) * a.Hq + g * a.G + rh % a.G) * kD : 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      uint4 vl = okl ? *reinterpret_cast<const uint4*>(a.q + ql + 32 * c + 8 * t) : z;
+      uint4 vh = okh ? *reinterpret_cast<const uint4*>(a.q + qh + 32 * c + 8 * t) : z;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        qf[c][e][0] = word(vl, 2 * e);
+        qf[c][e][1] = word(vh, 2 * e);
+        qf[c][e][2] = word(vl, 2 * e + 1);
+        qf[c][e][3] = word(vh, 2 * e + 1);
+      }
+    }
+    pos_lo = okl ? ctx - a.W + rl / a.G : -1;
+    pos_hi = okh ? ctx - a.W + rh / a.G : -1;
+  }
+
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m_lo = kNegInf, m_hi = kNegInf, l_lo = 0.f, l_hi = 0.f;
+
+  for (int s = 0; s < nstages; ++s) {
+    if (s + 1 < nstages) cp_async_wait<1>(); else cp_async_wait<0>();
+    __syncthreads();
+    if (s + 2 < nstages)
+      stage_kv<QT>(sring + ((s + 2) % kStages) * S::STAGE, a, b, g, blk0 + (s + 2) * KS, blk_end);
+    const int blk = blk0 + s * KS + ks;
+    if (blk >= blk_end) continue;
+    const uint32_t ks_addr = sring + (s % kStages) * S::STAGE + ks * 2 * kBlockBytes;
+    const uint32_t vs_addr = ks_addr + kBlockBytes;
+    const int key0 = blk * kBlk;
+    const int ntok = min(kBlk, ctx - key0);
+
+    // ---- S = Q K^T for 16 keys (two n8 halves) ----
+    float sc[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      sc[h][0] = sc[h][1] = sc[h][2] = sc[h][3] = 0.f;
+      const int r = 8 * h + gq;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 kv = lds128(ks_addr + (r * 16 + ((4 * c + t) ^ sigma(r))) * 16);
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          mma_bf16(sc[h], qf[c][e][0], qf[c][e][1], qf[c][e][2], qf[c][e][3], word(kv, 2 * e),
+                   word(kv, 2 * e + 1));
+      }
+    }
+    // ---- mask, scale, online softmax ----
+    float mx_lo = kNegInf, mx_hi = kNegInf;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int key = key0 + 8 * h + 2 * t + (q & 1);
+        const int pos = (q & 2) ? pos_hi : pos_lo;
+        const float v = key <= pos ? sc[h][q] * a.scale_log2 : kNegInf;
+        sc[h][q] = v;
+        if (q & 2) mx_hi = fmaxf(mx_hi, v); else mx_lo = fmaxf(mx_lo, v);
+      }
+    }
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, off));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, off));
+    }
+    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+    const float base_lo = mn_lo == kNegInf ? 0.f : mn_lo;
+    const float base_hi = mn_hi == kNegInf ? 0.f : mn_hi;
+    const float al_lo = ex2(m_lo - base_lo), al_hi = ex2(m_hi - base_hi);  // exp2(-inf) = 0
+    m_lo = mn_lo;
+    m_hi = mn_hi;
+    float p[2][4];
+    float rs_lo = 0.f, rs_hi = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      p[h][0] = ex2(sc[h][0] - base_lo);
+      p[h][1] = ex2(sc[h][1] - base_lo);
+      p[h][2] = ex2(sc[h][2] - base_hi);
+      p[h][3] = ex2(sc[h][3] - base_hi);
+      rs_lo += p[h][0] + p[h][1];
+      rs_hi += p[h][2] + p[h][3];
+    }
+    l_lo = l_lo * al_lo + rs_lo;
+    l_hi = l_hi * al_hi + rs_hi;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      o[i][0] *= al_lo;
+      o[i][1] *= al_lo;
+      o[i][2] *= al_hi;
+      o[i][3] *= al_hi;
+    }
+    const uint32_t pa0 = pack_bf16x2(p[0][0], p[0][1]), pa1 = pack_bf16x2(p[0][2], p[0][3]);
+    const uint32_t pa2 = pack_bf16x2(p[1][0], p[1][1]), pa3 = pack_bf16x2(p[1][2], p[1][3]);
+
+    // ---- O += P V ----
+    const int k0 = 2 * t, k1 = 2 * t + 1, k2 = 2 * t + 8, k3 = 2 * t + 9;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int u = 8 * h + gq;
+      uint4 va = lds128(vs_addr + (k0 * 16 + (u ^ sigma(k0))) * 16);
+      uint4 vb = lds128(vs_addr + (k1 * 16 + (u ^ sigma(k1))) * 16);
+      uint4 vc = lds128(vs_addr + (k2 * 16 + (u ^ sigma(k2))) * 16);
+      uint4 vd = lds128(vs_addr + (k3 * 16 + (u ^ sigma(k3))) * 16);
+      if (ntok < kBlk) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        if (k0 >= ntok) va = z;
+        if (k1 >= ntok) vb = z;
+        if (k2 >= ntok) vc = z;
+        if (k3 >= ntok) vd = z;
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const uint32_t sel = (jj & 1) ? 0x7632u : 0x5410u;
+        const uint32_t b0 = prmt(word(va, jj >> 1), word(vb, jj >> 1), sel);
+        const uint32_t b1 = prmt(word(vc, jj >> 1), word(vd, jj >> 1), sel);
+        mma_bf16(o[8 * h + jj], pa0, pa1, pa2, pa3, b0, b1);
+      }
+    }
+  }
+
+  // ---- merge the KS warps of each query tile through shared memory ----
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+  __syncthreads();  // ring no longer needed
+  float* mo = reinterpret_cast<float*>(smem);  // [warp][16 rows][130]
+  {
+    float* wbase = mo + warp * 16 * (kD + 2);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int d0 = 64 * h + 8 * (2 * t) + jj, d1 = d0 + 8;
+        wbase[gq * (kD + 2) + d0] = o[8 * h + jj][0];
+        wbase[gq * (kD + 2) + d1] = o[8 * h + jj][1];
+        wbase[(gq + 8) * (kD + 2) + d0] = o[8 * h + jj][2];
+        wbase[(gq + 8) * (kD + 2) + d1] = o[8 * h + jj][3];
+      }
+    if (t == 0) {
+      wbase[gq * (kD + 2) + kD] = m_lo;
+      wbase[gq * (kD + 2) + kD + 1] = l_lo;
+      wbase[(gq + 8) * (kD + 2) + kD] = m_hi;
+      wbase[(gq + 8) * (kD + 2) + kD + 1] = l_hi;
+    }
+  }
+  __syncthreads();
+  // thread -> (query tile, row, 128/ (kThreads/(QT*16)) columns)
+  constexpr int TPR = kThreads / (QT * 16);  // threads per row
+  constexpr int CPT = kD / TPR;              // columns per thread
+  const int row_id = threadIdx.x / TPR;      // 0 .. QT*16-1
+  const int col0 = (threadIdx.x % TPR) * CPT;
+  const int mqt = row_id / 16, mrow = row_id % 16;
+  const int r = (qg * QT + mqt) * 16 + mrow;
+  if (r >= a.QR) return;
+  float mstar = kNegInf;
+#pragma unroll
+  for (int j = 0; j < KS; ++j) {
+    const float* wb = mo + (j * QT + mqt) * 16 * (kD + 2) + mrow * (kD + 2);
+    mstar = fmaxf(mstar, wb[kD]);
+  }
+  const float mbase = mstar == kNegInf ? 0.f : mstar;
+  float wgt[KS];
+  float L = 0.f;
+#pragma unroll
+  for (int j = 0; j < KS; ++j) {
+    const float* wb = mo + (j * QT + mqt) * 16 * (kD + 2) + mrow * (kD + 2);
+    wgt[j] = ex2(wb[kD] - mbase);
+    L += wgt[j] * wb[kD + 1];
+  }
+  const int64_t orow = ((int64_t)b * a.W + r / a.G) * a.Hq + g * a.G + r % a.G;
+  if (a.nchunks == 1) {
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int c = 0; c < CPT; c += 2) {
+      float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        const float* wb = mo + (j * QT + mqt) * 16 * (kD + 2) + mrow * (kD + 2);
+        v0 += wgt[j] * wb[col0 + c];
+        v1 += wgt[j] * wb[col0 + c + 1];
+      }
+      *reinterpret_cast<uint32_t*>(a.out + orow * kD + col0 + c) = pack_bf16x2(v0 * inv, v1 * inv);
+    }
+  } else {
+    float* po = a.part_o + (orow * a.nchunks + chunk) * kD;
+    for (int c = 0; c < CPT; ++c) {
+      float v = 0.f;
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        const float* wb = mo + (j * QT + mqt) * 16 * (kD + 2) + mrow * (kD + 2);
+        v += wgt[j] * wb[col0 + c];
+      }
+      po[col0 + c] = v;
+    }
+    if (threadIdx.x % TPR == 0) {
+      a.part_ml[(orow * a.nchunks + chunk) * 2] = mstar;
+      a.part_ml[(orow * a.nchunks + chunk) * 2 + 1] = L;
+    }
+  }
+}
+
+// One warp per output row: combine the chunk partials of that row.
+__global__ void __launch_bounds__(128) attn_merge_kernel(const Args a) {
+  const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)a.B * a.W * a.Hq;
+  if (row >= rows) return;
+  const int b = (int)(row / ((int64_t)a.W * a.Hq));
+  const int ctx = seq_ctx(a, b);
+  const int nblk = (ctx + kBlk - 1) / kBlk;
+  const int nch = min(a.nchunks, (nblk + a.chunk_blocks - 1) / a.chunk_blocks);
+  const float* ml = a.part_ml + row * a.nchunks * 2;
+  float mstar = kNegInf;
+  for (int c = 0; c < nch; ++c) mstar = fmaxf(mstar, ml[2 * c]);
+  const float mbase = mstar == kNegInf ? 0.f : mstar;
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = 0; c < nch; ++c) {
+    const float w = ex2(ml[2 * c] - mbase);
+    L += w * ml[2 * c + 1];
+    const float4 v = *reinterpret_cast<const float4*>(a.part_o + (row * a.nchunks + c) * kD + lane * 4);
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint2 o;
+  o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  o.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(a.out + row * kD + lane * 4) = o;
+}
+
+template <int QT>
+cudaError_t launch_split(const Args& a, const AttnPlan& p, cudaStream_t s) {
+  using S = Smem<QT>;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<QT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  dim3 grid(p.nchunks, a.Hkv, a.B * p.qgroups);
+  attn_split_kernel<QT><<<grid, kThreads, S::BYTES, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms) {
+  AttnPlan p{};
+  const int G = hq / hkv;
+  const int qr = G * w;
+  const int tiles = (qr + 15) / 16;
+  p.qt = tiles <= 1 ? 1 : (tiles <= 2 ? 2 : 4);
+  p.qgroups = (tiles + p.qt - 1) / p.qt;
+  const int ks = 4 / p.qt;
+  const int maxblk = std::max(1, (max_context + kBlk - 1) / kBlk);
+  const int64_t items = (int64_t)b * hkv * p.qgroups;
+  const int ctas_per_sm = p.qt == 1 ? 2 : (p.qt == 2 ? 3 : 6);
+  const int64_t target = (int64_t)std::max(num_sms, 1) * ctas_per_sm;
+  int64_t nch = std::max<int64_t>(1, (target + items - 1) / items);
+  nch = std::min<int64_t>(nch, (maxblk + ks - 1) / ks);
+  int cb = (int)((maxblk + nch - 1) / nch);
+  // Test hook: DQD_ATTN_CHUNK_BLOCKS forces the split-KV chunk size.
+  if (const char* env = std::getenv("DQD_ATTN_CHUNK_BLOCKS")) {
+    const long v = std::strtol(env, nullptr, 10);
+    if (v >= 1) cb = (int)std::min<long>(v, maxblk);
+  }
+  cb = (cb + ks - 1) / ks * ks;
+  p.chunk_blocks = cb;
+  p.nchunks = (maxblk + cb - 1) / cb;
+  p.smem_bytes = p.qt == 1 ? Smem<1>::BYTES : (p.qt == 2 ? Smem<2>::BYTES : Smem<4>::BYTES);
+  const size_t rows = (size_t)b * w * hq;
+  p.ws_bytes = p.nchunks > 1 ? kCounterBytes + rows * p.nchunks * (kD + 2) * sizeof(float) : 0;
+  return p;
+}
+
+cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) {
+  Args a;
+  a.q = l.q;
+  a.kp = l.k_pool;
+  a.vp = l.v_pool;
+  a.table = l.block_table;
+  a.ctx = l.context_lens;
+  a.out = l.out;
+  const size_t rows = (size_t)l.b * l.w * l.hq;
+  if (p.nchunks > 1) {
+    a.part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(l.workspace) + kCounterBytes);
+    a.part_ml = a.part_o + rows * p.nchunks * kD;
+  } else {
+    a.part_o = nullptr;
+    a.part_ml = nullptr;
+  }
+  a.num_blocks = l.num_blocks;
+  a.max_blocks = l.max_blocks;
+  a.B = l.b;
+  a.W = l.w;
+  a.Hq = l.hq;
+  a.Hkv = l.hkv;
+  a.G = l.hq / l.hkv;
+  a.QR = a.G * l.w;
+  a.chunk_blocks = p.chunk_blocks;
+  a.nchunks = p.nchunks;
+  a.qgroups = p.qgroups;
+  a.scale_log2 = l.softmax_scale * 1.4426950408889634f;
+  cudaError_t e;
+  switch (p.qt) {
+    case 1: e = launch_split<1>(a, p, s); break;
+    case 2: e = launch_split<2>(a, p, s); break;
+    default: e = launch_split<4>(a, p, s); break;
+  }
+  if (e != cudaSuccess || p.nchunks == 1) return e;
+  const int64_t blocks = ((int64_t)rows + 3) / 4;
+  attn_merge_kernel<<<(unsigned)blocks, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dqd

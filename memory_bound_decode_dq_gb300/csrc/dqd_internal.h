@@ -1,0 +1,82 @@
+// Internal interface between the C-ABI layer (dqd_api.cu) and the kernel
+// launchers. Host-only declarations.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace dqd {
+
+enum WType { kBF16 = 0, kFP8 = 1, kINT4 = 2 };
+
+constexpr size_t kCounterBytes = 65536;  // = DQD_WS_COUNTER_BYTES
+
+// ---------------------------------------------------------------- dq_gemm --
+
+struct GemmPlan {
+  int mt;            // m8 tiles per CTA pass (1, 2, 4, 8)
+  int m_chunks;      // ceil(m / (8*mt))
+  int grid_x;        // CTAs along n (4 row tiles of 16 each)
+  int splits;        // CTAs along k
+  int64_t k_per_split;
+  int kc;            // k per pipeline stage
+  int smem_bytes;    // dynamic shared memory per CTA
+  size_t ws_bytes;   // workspace needed (0 if splits == 1)
+};
+
+GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms);
+
+struct GemmLaunch {
+  int wtype;
+  const void* data;
+  const void* scales;
+  const void* zeros;
+  const uint16_t* x;
+  uint16_t* y;
+  int64_t m, n, k;
+  void* workspace;
+};
+
+cudaError_t launch_dq_gemm(const GemmLaunch& a, const GemmPlan& p, cudaStream_t s);
+
+// ------------------------------------------------------------ attention --
+
+struct AttnPlan {
+  int qt;            // 16-row query tiles per CTA (1, 2, 4)
+  int qgroups;       // CTAs needed to cover all query rows of one kv head
+  int chunk_blocks;  // 16-token blocks per split-KV chunk
+  int nchunks;
+  int smem_bytes;
+  size_t ws_bytes;   // 0 if nchunks == 1
+};
+
+AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms);
+
+struct AttnLaunch {
+  const uint16_t* q;
+  const uint16_t* k_pool;
+  const uint16_t* v_pool;
+  int64_t num_blocks;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* context_lens;
+  int b, w, hq, hkv;
+  float softmax_scale;
+  uint16_t* out;
+  void* workspace;
+};
+
+cudaError_t launch_attn(const AttnLaunch& a, const AttnPlan& p, cudaStream_t s);
+
+// -------------------------------------------------------------- formats --
+
+cudaError_t launch_pack_int4(const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
+                             int64_t n, int64_t k, void* packed, void* pscales, void* pzeros,
+                             cudaStream_t s);
+
+cudaError_t launch_quant_fp8(const uint16_t* w, int64_t n, int64_t k, uint8_t* codes,
+                             float* scales, cudaStream_t s);
+
+}  // namespace dqd

@@ -1,0 +1,293 @@
+"""Thin ctypes binding of libdqd over torch tensors.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libdqd.so (built by ``memory_bound_decode_dq_gb300.build``). The
+names are the C names declared in ``include/dqd.h``. There is no fallback: if
+the library is missing, importing this module raises ImportError.
+
+torch provides device memory and streams: tensors' ``data_ptr()`` and the
+current stream's handle are passed to the C calls unchanged.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdqd.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"` "
+        "or `python memory_bound_decode_dq_gb300/build.py` (needs nvcc)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+DQD_OK, DQD_ERR_INVALID_ARG, DQD_ERR_UNSUPPORTED, DQD_ERR_WORKSPACE, DQD_ERR_CUDA = range(5)
+DQD_W_BF16, DQD_W_FP8_E4M3, DQD_W_INT4_G128 = 0, 1, 2
+DQD_WS_COUNTER_BYTES = 65536
+
+
+class _WeightDesc(ctypes.Structure):
+    _fields_ = [("type", ctypes.c_int32), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("data", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("zeros", ctypes.c_void_p)]
+
+
+_P = ctypes.c_void_p
+_I32, _I64, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+_SIGS = {
+    "dqd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "dqd_last_error": (ctypes.c_char_p, []),
+    "dqd_version": (ctypes.c_char_p, []),
+    "pack_int4_g128_bytes": (_SZ, [_I64, _I64, ctypes.c_int]),
+    "pack_int4_g128": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _P, _P, _P]),
+    "quant_fp8_rowwise": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
+    "dq_gemm_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(_WeightDesc), _I64, ctypes.POINTER(_SZ)]),
+    "dq_gemm": (ctypes.c_int, [ctypes.POINTER(_WeightDesc), _P, _I64, _P, _P, _SZ, _P]),
+    "gqa_decode_attn_workspace_bytes": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32,
+                                                       ctypes.POINTER(_SZ)]),
+    "gqa_decode_attn": (ctypes.c_int, [_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
+                                       _I32, ctypes.c_float, _P, _P, _SZ, _P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class DqdError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        name = _lib.dqd_status_string(status).decode()
+        detail = _lib.dqd_last_error().decode()
+        super().__init__(f"{where}: {name}: {detail}")
+
+
+def _check(status: int, where: str) -> None:
+    if status != DQD_OK:
+        raise DqdError(status, where)
+
+
+def version() -> str:
+    return _lib.dqd_version().decode()
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libdqd handle (for callers that want the raw C ABI)."""
+    return _lib
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtypes, device=None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_U8 = (torch.uint8,)
+_B16 = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
+_F32 = (torch.float32,)
+_I32T = (torch.int32,)
+
+
+# ------------------------------------------------------------ workspace ----
+
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+def workspace(nbytes: int, device, stream=None) -> torch.Tensor | None:
+    """A zero-initialised workspace of at least ``nbytes`` for ``device``,
+    cached per (device, stream). Every library call leaves the counter region
+    zero, so a cached buffer can be reused by later calls on the same stream."""
+    if nbytes == 0:
+        return None
+    dev = torch.device(device)
+    sid = (stream or torch.cuda.current_stream(dev)).cuda_stream
+    key = (dev.index, sid)
+    with _ws_lock:
+        buf = _ws_cache.get(key)
+        if buf is None or buf.numel() < nbytes:
+            size = max(nbytes, 2 * (buf.numel() if buf is not None else 0))
+            buf = torch.zeros(size, dtype=torch.uint8, device=dev)
+            _ws_cache[key] = buf
+        return buf
+
+
+# --------------------------------------------------------------- weights ----
+
+@dataclass
+class Int4Packed:
+    """INT4 g128 weight in the packed layout of include/dqd.h."""
+    packed: torch.Tensor
+    scales: torch.Tensor
+    zeros: torch.Tensor
+    n: int
+    k: int
+
+
+@dataclass
+class Weight:
+    """W [n out, k in] for dq_gemm. ``type`` is DQD_W_BF16, DQD_W_FP8_E4M3 or
+    DQD_W_INT4_G128; the tensors stay referenced for the call's lifetime."""
+    type: int
+    n: int
+    k: int
+    data: torch.Tensor
+    scales: torch.Tensor | None = None
+    zeros: torch.Tensor | None = None
+
+    @staticmethod
+    def bf16(w: torch.Tensor) -> "Weight":
+        _need(w, "w", _B16)
+        return Weight(DQD_W_BF16, w.shape[0], w.shape[1], w)
+
+    @staticmethod
+    def fp8(codes: torch.Tensor, scales: torch.Tensor) -> "Weight":
+        _need(codes, "codes", _U8 + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ()))
+        _need(scales, "scales", _F32)
+        return Weight(DQD_W_FP8_E4M3, codes.shape[0], codes.shape[1], codes, scales)
+
+    @staticmethod
+    def int4(p: Int4Packed) -> "Weight":
+        return Weight(DQD_W_INT4_G128, p.n, p.k, p.packed, p.scales, p.zeros)
+
+    def desc(self) -> _WeightDesc:
+        return _WeightDesc(int(self.type), int(self.n), int(self.k), _ptr(self.data),
+                           _ptr(self.scales), _ptr(self.zeros))
+
+
+# ------------------------------------------------------------ functions ----
+
+def pack_int4_g128_bytes(n: int, k: int, which: int) -> int:
+    return int(_lib.pack_int4_g128_bytes(n, k, which))
+
+
+def pack_int4_g128(codes: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+                   stream=None) -> Int4Packed:
+    """Logical INT4 g128 (codes u8 [n,k], bf16 scales [n,k/128], u8 zeros
+    [n,k/128]) -> packed layout, on the GPU."""
+    _need(codes, "codes", _U8)
+    dev = codes.device
+    _need(scales, "scales", _B16, dev)
+    _need(zeros, "zeros", _U8, dev)
+    n, k = codes.shape
+    sizes = [pack_int4_g128_bytes(n, k, i) for i in range(3)]
+    if 0 in sizes:
+        raise ValueError(f"pack_int4_g128: unsupported shape n={n} k={k} (k must be a multiple of 128)")
+    if scales.shape != (n, k // 128) or zeros.shape != (n, k // 128):
+        raise ValueError("pack_int4_g128: scales and zeros must be [n, k/128]")
+    out = [torch.empty(s, dtype=torch.uint8, device=dev) for s in sizes]
+    _check(_lib.pack_int4_g128(_ptr(codes), _ptr(scales), _ptr(zeros), n, k, _ptr(out[0]),
+                               _ptr(out[1]), _ptr(out[2]), _stream(stream)), "pack_int4_g128")
+    return Int4Packed(out[0], out[1], out[2], n, k)
+
+
+def quant_fp8_rowwise(w: torch.Tensor, stream=None):
+    """bf16 W [n, k] -> (E4M3 codes u8 [n, k], fp32 scales [n])."""
+    _need(w, "w", _B16)
+    n, k = w.shape
+    codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((n,), dtype=torch.float32, device=w.device)
+    _check(_lib.quant_fp8_rowwise(_ptr(w), n, k, _ptr(codes), _ptr(scales), _stream(stream)),
+           "quant_fp8_rowwise")
+    return codes, scales
+
+
+def dq_gemm_workspace_bytes(weight: Weight, m: int) -> int:
+    out = _SZ(0)
+    d = weight.desc()
+    _check(_lib.dq_gemm_workspace_bytes(ctypes.byref(d), int(m), ctypes.byref(out)),
+           "dq_gemm_workspace_bytes")
+    return int(out.value)
+
+
+def dq_gemm(weight: Weight, x: torch.Tensor, y: torch.Tensor | None = None,
+            ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = x * deq(W)^T. x bf16 [m, k] (or [k]); returns bf16 [m, n]."""
+    _need(x, "x", _B16)
+    squeeze = x.dim() == 1
+    x2 = x.view(1, -1) if squeeze else x
+    m, k = x2.shape
+    if k != weight.k:
+        raise ValueError(f"dq_gemm: x has k={k}, weight has k={weight.k}")
+    if y is None:
+        y = torch.empty((m, weight.n), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(y, "y", _B16, x.device)
+        if tuple(y.shape) not in ((m, weight.n),) + (((weight.n,),) if squeeze else ()):
+            raise ValueError("dq_gemm: y must be [m, n]")
+    d = weight.desc()
+    need = dq_gemm_workspace_bytes(weight, m)
+    if ws is None:
+        ws = workspace(need, x.device, stream)
+    _check(_lib.dq_gemm(ctypes.byref(d), _ptr(x2), m, _ptr(y), _ptr(ws),
+                        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "dq_gemm")
+    return y.view(-1) if squeeze and y.dim() == 2 else y
+
+
+def gqa_decode_attn_workspace_bytes(b: int, w: int, hq: int, hkv: int, d: int, max_context: int) -> int:
+    out = _SZ(0)
+    _check(_lib.gqa_decode_attn_workspace_bytes(b, w, hq, hkv, d, max_context, ctypes.byref(out)),
+           "gqa_decode_attn_workspace_bytes")
+    return int(out.value)
+
+
+def gqa_decode_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                    block_table: torch.Tensor, context_lens: torch.Tensor, max_context: int,
+                    softmax_scale: float | None = None, out: torch.Tensor | None = None,
+                    ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Paged GQA decode/verify attention. q bf16 [B, W, Hq, D]; pools bf16
+    [num_blocks, Hkv, 16, D]; block_table int32 [B, max_blocks]; context_lens
+    int32 [B] (device, includes the W new tokens); max_context: host bound."""
+    _need(q, "q", _B16)
+    dev = q.device
+    _need(k_pool, "k_pool", _B16, dev)
+    _need(v_pool, "v_pool", _B16, dev)
+    _need(block_table, "block_table", _I32T, dev)
+    _need(context_lens, "context_lens", _I32T, dev)
+    B, W, Hq, D = q.shape
+    nblk, Hkv, bs, D2 = k_pool.shape
+    if bs != 16 or D2 != D or v_pool.shape != k_pool.shape:
+        raise ValueError("gqa_decode_attn: pools must be [num_blocks, Hkv, 16, D] and equal shapes")
+    if block_table.dim() != 2 or block_table.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("gqa_decode_attn: block_table must be [B, max_blocks], context_lens [B]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q, dtype=torch.bfloat16)
+    else:
+        _need(out, "out", _B16, dev)
+        if out.shape != q.shape:
+            raise ValueError("gqa_decode_attn: out must have q's shape")
+    need = gqa_decode_attn_workspace_bytes(B, W, Hq, Hkv, D, int(max_context))
+    if ws is None:
+        ws = workspace(need, dev, stream)
+    _check(_lib.gqa_decode_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), nblk, _ptr(block_table),
+                                block_table.shape[1], _ptr(context_lens), int(max_context), B, W, Hq,
+                                Hkv, D, float(softmax_scale), _ptr(out), _ptr(ws),
+                                0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "gqa_decode_attn")
+    return out

@@ -90,7 +90,17 @@ ORC_EXPORT double orc_e4m3_decode(uint8_t c) {
 /* Round-to-nearest-even onto the finite E4M3 grid, saturating magnitudes at
  * or above 448 to 448 ("satfinite"); NaN stays NaN. Brute force over the 127
  * non-negative finite codes, so that nothing but the grid itself is assumed. */
+static double e4m3_grid[0x7F]; /* values of codes 0x00..0x7E */
+
+static void e4m3_grid_init(void) {
+  static volatile int done = 0;
+  if (done) return;
+  for (int c = 0; c <= 0x7E; ++c) e4m3_grid[c] = orc_e4m3_decode((uint8_t)c);
+  done = 1;
+}
+
 ORC_EXPORT uint8_t orc_e4m3_encode(float v) {
+  e4m3_grid_init();
   if (isnan(v)) return 0x7F;
   uint8_t sign = signbit(v) ? 0x80 : 0;
   double a = fabs((double)v);
@@ -98,7 +108,7 @@ ORC_EXPORT uint8_t orc_e4m3_encode(float v) {
   int best = 0;
   double best_d = a; /* distance to code 0 (value 0) */
   for (int c = 1; c <= 0x7E; ++c) {
-    double d = fabs(orc_e4m3_decode((uint8_t)c) - a);
+    double d = fabs(e4m3_grid[c] - a);
     if (d < best_d || (d == best_d && (c & 1) == 0)) {
       best = c;
       best_d = d;
@@ -113,6 +123,7 @@ ORC_EXPORT uint8_t orc_e4m3_encode(float v) {
  * in IEEE binary32 like the kernel. W is bf16 [n][k] row-major. */
 ORC_EXPORT void orc_quant_fp8_rowwise(const uint16_t* w, int64_t n, int64_t k,
                                       uint8_t* codes, float* scales) {
+  e4m3_grid_init();
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < n; ++r) {
     const uint16_t* row = w + r * k;
@@ -395,6 +406,7 @@ ORC_EXPORT void orc_e4m3_decode_n(const uint8_t* c, int64_t n, double* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_decode(c[i]);
 }
 ORC_EXPORT void orc_e4m3_encode_n(const float* v, int64_t n, uint8_t* out) {
+  e4m3_grid_init();
 #pragma omp parallel for schedule(static)
   for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(v[i]);
 }

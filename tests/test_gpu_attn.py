@@ -1,0 +1,177 @@
+"""GPU parity of gqa_decode_attn against the float64 oracle, plus the
+properties that fix attention independently of its evaluation order."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from memory_bound_decode_dq_gb300 import synth
+from gpu_util import assert_close, bf, bits, f64, i32, require_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_cuda()
+
+
+@pytest.fixture(scope="module")
+def dqd():
+    from memory_bound_decode_dq_gb300 import dqd as m
+    return m
+
+
+@pytest.fixture
+def chunk(monkeypatch):
+    def set_chunk(v):
+        if v is None:
+            monkeypatch.delenv("DQD_ATTN_CHUNK_BLOCKS", raising=False)
+        else:
+            monkeypatch.setenv("DQD_ATTN_CHUNK_BLOCKS", str(v))
+    yield set_chunk
+    monkeypatch.delenv("DQD_ATTN_CHUNK_BLOCKS", raising=False)
+
+
+def run(dqd, dev, q, kv, hkv, ctx=None, scale=None, max_context=None, table=None):
+    ctx = kv.context_lens if ctx is None else np.asarray(ctx, np.int32)
+    table = kv.block_table if table is None else table
+    out = dqd.gqa_decode_attn(bf(q, dev), bf(kv.k_pool, dev), bf(kv.v_pool, dev), i32(table, dev),
+                              i32(ctx, dev), int(max_context or max(int(ctx.max()), 1)),
+                              softmax_scale=scale)
+    return out
+
+
+def ref(q, kv, hkv, ctx=None, scale=None, table=None):
+    d = q.shape[-1]
+    return oracle.gqa_decode_attn(q, kv.k_pool, kv.v_pool, kv.block_table if table is None else table,
+                                  kv.context_lens if ctx is None else ctx, hkv,
+                                  1 / math.sqrt(d) if scale is None else scale)
+
+
+CASES = [
+    # B, W, Hq, Hkv, contexts
+    (1, 1, 8, 2, (256,)),
+    (1, 1, 32, 8, (1000,)),
+    (3, 1, 8, 2, (1, 17, 300)),
+    (2, 1, 4, 4, (33, 64)),          # MHA
+    (2, 1, 64, 8, (129, 2048)),      # 8 heads per group
+    (2, 6, 32, 8, (6, 700)),         # verify, 24 rows per kv head
+    (2, 16, 32, 8, (16, 513)),       # verify, 64 rows per kv head
+    (1, 16, 64, 8, (900,)),          # 128 rows per kv head: two query groups
+    (4, 3, 12, 4, (5, 16, 31, 47)),
+]
+
+
+@pytest.mark.parametrize("B,W,hq,hkv,ctx", CASES)
+def test_against_oracle(dev, dqd, B, W, hq, hkv, ctx):
+    kv = synth.paged_kv(B * 100 + W, "kv", ctx, hkv, spare_blocks=3)
+    q = synth.normal_bf16(B + W, "q", (B, W, hq, 128))
+    out = run(dqd, dev, q, kv, hkv)
+    assert_close(f64(out), ref(q, kv, hkv), what=f"attn B={B} W={W} {hq}/{hkv} ctx={ctx}")
+
+
+@pytest.mark.parametrize("cb", [1, 2, 3, 4, 7, 16, 1000])
+@pytest.mark.parametrize("W", [1, 16])
+def test_every_chunk_size(dev, dqd, chunk, cb, W):
+    chunk(cb)
+    kv = synth.paged_kv(cb, "kv", (W + 40, 333), 2)
+    q = synth.normal_bf16(cb, "q", (2, W, 8, 128))
+    assert_close(f64(run(dqd, dev, q, kv, 2)), ref(q, kv, 2), what=f"chunk_blocks={cb} W={W}")
+
+
+def test_uniform_v_returns_v(dev, dqd):
+    kv = synth.paged_kv(1, "kv", (77, 500), 2)
+    v = synth.normal_bf16(1, "v", (2, 128))
+    kv.v_pool[:] = v[None, :, None, :]
+    q = synth.normal_bf16(1, "q", (2, 4, 8, 128))
+    out = bits(run(dqd, dev, q, kv, 2))
+    want = np.broadcast_to(v[None, None, [0, 0, 0, 0, 1, 1, 1, 1], :], out.shape)
+    # normalised sum of identical rows: exact up to the final rounding
+    diff = np.abs(((out.astype(np.uint32) << 16).view(np.float32)) - ((want.astype(np.uint32) << 16).view(np.float32)))
+    assert np.all(diff <= np.abs((want.astype(np.uint32) << 16).view(np.float32)) * 2 ** -7)
+    assert np.mean(out == want) > 0.99
+
+
+def test_single_key_returns_its_value(dev, dqd):
+    kv = synth.paged_kv(2, "kv", (1, 1), 4)
+    q = synth.normal_bf16(2, "q", (2, 1, 4, 128))
+    out = bits(run(dqd, dev, q, kv, 4))
+    for b in range(2):
+        blk = kv.block_table[b, 0]
+        assert np.array_equal(out[b, 0], kv.v_pool[blk, :, 0, :])
+
+
+def test_dominant_logit(dev, dqd):
+    kv = synth.paged_kv(3, "kv", (50,), 1, shuffle=False)
+    kv.k_pool[:] = 0
+    q = np.zeros((1, 1, 2, 128), np.uint16)
+    q[0, 0, :, 0] = 0x3F80
+    kv.k_pool[2, 0, 3, 0] = 0x41F0  # logit 30 at key 35
+    out = f64(run(dqd, dev, q, kv, 1, scale=1.0))
+    target = (kv.v_pool[2, 0, 3].astype(np.uint32) << 16).view(np.float32)
+    assert np.abs(out[0, 0, 0] - target).max() <= np.abs(target).max() * 2 ** -7
+    assert np.abs(out[0, 0, 1] - target).max() <= np.abs(target).max() * 2 ** -7
+
+
+def test_block_permutation_is_bit_identical(dev, dqd):
+    ctx = (100, 37, 16, 200)
+    kv = synth.paged_kv(5, "kv", ctx, 2)
+    q = synth.normal_bf16(5, "q", (4, 2, 8, 128))
+    a = bits(run(dqd, dev, q, kv, 2))
+    perm = np.random.default_rng(9).permutation(kv.num_blocks)
+    kp = np.empty_like(kv.k_pool)
+    vp = np.empty_like(kv.v_pool)
+    kp[perm] = kv.k_pool
+    vp[perm] = kv.v_pool
+    moved = synth.PagedKV(kp, vp, perm[kv.block_table].astype(np.int32), kv.context_lens, kv.num_blocks)
+    assert np.array_equal(bits(run(dqd, dev, q, moved, 2)), a)
+
+
+def test_verify_rows_match_plain_decode(dev, dqd):
+    W, ctx = 6, (61, 250)
+    kv = synth.paged_kv(6, "kv", ctx, 2)
+    q = synth.normal_bf16(6, "q", (2, W, 8, 128))
+    out = f64(run(dqd, dev, q, kv, 2))
+    for i in range(W):
+        short = np.asarray(ctx, np.int32) - W + i + 1
+        one = f64(run(dqd, dev, q[:, i:i + 1].copy(), kv, 2, ctx=short, max_context=max(ctx)))
+        assert_close(out[:, i], one[:, 0], what=f"verify row {i}")
+
+
+def test_stale_pool_contents_do_not_leak(dev, dqd):
+    """Slots past the context inside the last block hold NaN; the output must
+    not see them."""
+    ctx = (21, 5)
+    kv = synth.paged_kv(7, "kv", ctx, 2)
+    for b, c in enumerate(ctx):
+        last = kv.block_table[b, (c - 1) // 16]
+        kv.k_pool[last, :, c % 16:, :] = 0x7FC0
+        kv.v_pool[last, :, c % 16:, :] = 0x7FC0
+    q = synth.normal_bf16(7, "q", (2, 1, 8, 128))
+    out = f64(run(dqd, dev, q, kv, 2))
+    assert np.all(np.isfinite(out))
+    assert_close(out, ref(q, kv, 2), what="NaN padding")
+
+
+def test_context_shorter_than_width_gives_zero_rows(dev, dqd):
+    kv = synth.paged_kv(8, "kv", (10,), 1)
+    q = synth.normal_bf16(8, "q", (1, 4, 2, 128))
+    out = f64(run(dqd, dev, q, kv, 1, ctx=np.array([2], np.int32), max_context=10))
+    # rows 0 and 1 sit at positions -2 and -1: they see no key
+    assert np.all(out[0, :2] == 0)
+    ref_rows = oracle.gqa_decode_attn(q[:, 2:], kv.k_pool, kv.v_pool, kv.block_table, np.array([2], np.int32),
+                                      1, 1 / math.sqrt(128))
+    assert_close(out[:, 2:], ref_rows, what="rows with keys")
+
+
+def test_rejects_bad_arguments(dev, dqd):
+    kv = synth.paged_kv(9, "kv", (16,), 2)
+    q = synth.normal_bf16(9, "q", (1, 17, 4, 128))
+    with pytest.raises(dqd.DqdError):
+        run(dqd, dev, q, kv, 2)          # width 17 > 16
+    q = synth.normal_bf16(9, "q", (1, 1, 3, 128))
+    with pytest.raises(dqd.DqdError):
+        run(dqd, dev, q, kv, 2)          # 3 heads over 2 kv heads

@@ -1,0 +1,143 @@
+"""Parity at the full workload sizes, in the launch configuration the
+benchmark times. The oracle evaluates sampled output rows (every row where it
+finishes in seconds); inputs are drawn once per case on the device and the
+sampled slices are copied back for the oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from memory_bound_decode_dq_gb300 import configs, synth
+from gpu_util import assert_close, bits, f64, require_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_cuda()
+
+
+@pytest.fixture(scope="module")
+def dqd():
+    from memory_bound_decode_dq_gb300 import dqd as m
+    return m
+
+
+def sample_rows(n: int, count: int, seed: int) -> np.ndarray:
+    if count >= n:
+        return np.arange(n)
+    r = np.random.default_rng(seed).choice(n, count - 2, replace=False)
+    return np.unique(np.concatenate([[0, n - 1], r]))
+
+
+def check_gemm(dqd, dev, case, seed, max_oracle_macs=4e8):
+    n, k, m = case.n, case.k, case.m
+    x = synth.normal_bf16(seed, case.name + ".x", (m, k), device=dev)
+    rows = sample_rows(n, max(16, int(max_oracle_macs // (m * k))), seed)
+    ridx = torch.as_tensor(rows, device=dev)
+    if case.wtype == oracle.W_INT4_G128:
+        wq = synth.int4_weight(seed, case.name, n, k, device=dev)
+        weight = dqd.Weight.int4(dqd.pack_int4_g128(wq.codes, wq.scales, wq.zeros))
+        host = (wq.codes[ridx].cpu().numpy(), bits(wq.scales[ridx]), wq.zeros[ridx].cpu().numpy())
+    else:
+        if case.outliers:
+            w = synth.bf16_weight_outliers_device(seed, case.name, n, k, 0.02, case.outliers, 20.0, dev)
+        else:
+            w = synth.normal_bf16(seed, case.name, (n, k), 0.02, device=dev)
+        if case.wtype == oracle.W_BF16:
+            weight = dqd.Weight.bf16(w)
+            host = (bits(w[ridx]), None, None)
+        else:
+            codes, scales = dqd.quant_fp8_rowwise(w)
+            weight = dqd.Weight.fp8(codes, scales)
+            rc, rs = oracle.quant_fp8_rowwise(bits(w[ridx]))
+            assert np.array_equal(codes[ridx].cpu().numpy(), rc), "GPU FP8 codes differ from the oracle's"
+            assert np.array_equal(scales[ridx].cpu().numpy(), rs)
+            host = (rc, rs, None)
+    y = dqd.dq_gemm(weight, x)
+    ref = oracle.dq_gemm(case.wtype, *host, bits(x))
+    assert_close(f64(y[:, ridx]), ref, what=case.name)
+
+
+def check_attn(dqd, dev, case, seed, max_groups=None):
+    B, W, hq, hkv = case.batch, case.width, case.hq, case.hkv
+    G = hq // hkv
+    ctx = np.asarray(case.context, np.int32)
+    table, nblk = synth.block_table(seed, case.name + ".table", ctx, case.shuffle)
+    shape = (nblk, hkv, 16, 128)
+    kp = synth.normal_bf16(seed, case.name + ".k", shape, 1.0, device=dev)
+    vp = synth.normal_bf16(seed, case.name + ".v", shape, 1.0, device=dev)
+    q = synth.normal_bf16(seed, case.name + ".q", (B, W, hq, 128), device=dev)
+    out = dqd.gqa_decode_attn(q, kp, vp, torch.from_numpy(table).to(dev), torch.from_numpy(ctx).to(dev),
+                              int(ctx.max()))
+    groups = [(b, g) for b in range(B) for g in range(hkv)]
+    if max_groups is not None and len(groups) > max_groups:
+        pick = np.random.default_rng(seed).choice(len(groups), max_groups, replace=False)
+        groups = [groups[i] for i in sorted(pick)]
+    tab_dev = torch.from_numpy(table).to(dev)
+    for b, g in groups:
+        nb = (int(ctx[b]) + 15) // 16
+        blocks = tab_dev[b, :nb].long()
+        ksub = bits(kp[blocks, g].unsqueeze(1).contiguous())     # [nb, 1, 16, 128]
+        vsub = bits(vp[blocks, g].unsqueeze(1).contiguous())
+        qsub = bits(q[b:b + 1, :, g * G:(g + 1) * G].contiguous())  # [1, W, G, 128]
+        ref = oracle.gqa_decode_attn(qsub, ksub, vsub, np.arange(nb, dtype=np.int32)[None, :],
+                                     ctx[b:b + 1], 1, 1 / math.sqrt(128))
+        got = f64(out[b:b + 1, :, g * G:(g + 1) * G])
+        assert_close(got, ref, what=f"{case.name} b={b} g={g}")
+
+
+WORKLOADS = {w.__name__: w() for w in configs.ALL}
+
+
+@pytest.mark.parametrize("case", WORKLOADS["tiny"].gemms, ids=lambda c: c.name)
+def test_tiny_gemm(dev, dqd, case):
+    check_gemm(dqd, dev, case, WORKLOADS["tiny"].seed)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["tiny"].attns, ids=lambda c: c.name)
+def test_tiny_attn(dev, dqd, case):
+    check_attn(dqd, dev, case, WORKLOADS["tiny"].seed)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["llama3_8b_b1"].gemms, ids=lambda c: c.name)
+def test_llama3_8b_gemm(dev, dqd, case):
+    check_gemm(dqd, dev, case, WORKLOADS["llama3_8b_b1"].seed, max_oracle_macs=2e8)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["llama3_8b_b1"].attns, ids=lambda c: c.name)
+def test_llama3_8b_attn(dev, dqd, case):
+    check_attn(dqd, dev, case, WORKLOADS["llama3_8b_b1"].seed)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["dense70b_b32"].gemms, ids=lambda c: c.name)
+def test_dense70b_gemm(dev, dqd, case):
+    check_gemm(dqd, dev, case, WORKLOADS["dense70b_b32"].seed)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["dense70b_b32"].attns, ids=lambda c: c.name)
+def test_dense70b_attn(dev, dqd, case):
+    check_attn(dqd, dev, case, WORKLOADS["dense70b_b32"].seed, max_groups=24)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["verify_8b"].gemms, ids=lambda c: c.name)
+def test_verify_gemm(dev, dqd, case):
+    check_gemm(dqd, dev, case, WORKLOADS["verify_8b"].seed)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["verify_8b"].attns, ids=lambda c: c.name)
+def test_verify_attn(dev, dqd, case):
+    check_attn(dqd, dev, case, WORKLOADS["verify_8b"].seed, max_groups=24)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["longctx_70b_b8"].gemms, ids=lambda c: c.name)
+def test_longctx_gemm(dev, dqd, case):
+    check_gemm(dqd, dev, case, WORKLOADS["longctx_70b_b8"].seed)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["longctx_70b_b8"].attns, ids=lambda c: c.name)
+def test_longctx_attn(dev, dqd, case):
+    check_attn(dqd, dev, case, WORKLOADS["longctx_70b_b8"].seed, max_groups=3)
