@@ -224,6 +224,41 @@ DQD_API dqd_status gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool,
                            float softmax_scale, uint16_t* out, void* workspace,
                            size_t ws_bytes, dqd_stream stream);
 
+/* ------------------------------------------------------------------------
+ * gqa_decode_attn_static_ws — gqa_decode_attn without a caller workspace.
+ *
+ * The pages have no counterpart to this entry point: it is an interface for
+ * callers that cannot allocate device memory. Examples are a runtime that
+ * forbids cudaMalloc once serving has started (an allocation can stall the
+ * device or fail under memory pressure) and a plug-in running inside a host
+ * process whose memory allocator it does not own. Such callers still own q,
+ * the pools, the tables and out; only the split-KV scratch changes hands.
+ *
+ * Arguments, layouts and results are those of gqa_decode_attn. The scratch
+ * is a fixed 32 MiB array inside the library (a static device variable that
+ * every GPU loading the library holds until the process exits). A call that
+ * needs more than that (b * w * hq * chunks * 520 bytes, plus 64 KiB) returns
+ * DQD_ERR_WORKSPACE with a message and launches nothing; use gqa_decode_attn
+ * with a caller workspace instead.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it: make that first call before any CUDA
+ * stream capture. The function itself allocates nothing and calls no
+ * allocating routine.
+ *
+ * All calls on a device share the one scratch array, which keeps whatever the
+ * previous call left in it; each call writes the partial results it reads,
+ * so nothing has to start at zero. Calls whose executions overlap on the GPU
+ * (different streams, or different host threads) race on the scratch and
+ * give wrong results: serialise them, e.g. on a single stream.
+ * ---------------------------------------------------------------------- */
+DQD_API dqd_status gqa_decode_attn_static_ws(const uint16_t* q, const uint16_t* k_pool,
+                                     const uint16_t* v_pool, int64_t num_blocks,
+                                     const int32_t* block_table, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, int32_t max_context,
+                                     int32_t b, int32_t w, int32_t hq, int32_t hkv, int32_t d,
+                                     float softmax_scale, uint16_t* out, dqd_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

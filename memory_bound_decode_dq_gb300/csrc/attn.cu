@@ -36,6 +36,7 @@
 #include "dqd_internal.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 
@@ -404,7 +405,39 @@ cudaError_t launch_split(const Args& a, const AttnPlan& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Fixed scratch for gqa_decode_attn_static_ws, for callers that cannot
+// allocate device memory. Every GPU that loads this module holds it until the
+// process exits. It is zero at load; the attention path never uses its
+// counter region and writes every split-KV partial before reading it.
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) uint8_t g_attn_static_scratch[kStaticScratchBytes];
+
 }  // namespace
+
+size_t attn_static_scratch_bytes() { return kStaticScratchBytes; }
+
+// Device address of the static scratch on the current device. In host code the
+// array's name is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress once per device (with that device current) and cached.
+cudaError_t attn_static_scratch(void** ptr) {
+  static std::atomic<void*> cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) {
+    void* p = cache[dev].load(std::memory_order_acquire);
+    if (p) {
+      *ptr = p;
+      return cudaSuccess;
+    }
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cache[dev].store(p, std::memory_order_release);
+  *ptr = p;
+  return cudaSuccess;
+}
 
 AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms) {
   AttnPlan p{};

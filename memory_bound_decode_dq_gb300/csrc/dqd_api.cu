@@ -270,4 +270,61 @@ dqd_status gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool, const uint
                       "gqa_decode_attn launch");
 }
 
+dqd_status gqa_decode_attn_static_ws(const uint16_t* q, const uint16_t* k_pool,
+                                     const uint16_t* v_pool, int64_t num_blocks,
+                                     const int32_t* block_table, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, int32_t max_context, int32_t b,
+                                     int32_t w, int32_t hq, int32_t hkv, int32_t d,
+                                     float softmax_scale, uint16_t* out, dqd_stream stream) {
+  g_last_error.clear();
+  dqd_status st = check_attn_shape(b, w, hq, hkv, d, max_context);
+  if (st != DQD_OK) return st;
+  if (num_blocks < 1) return fail(DQD_ERR_INVALID_ARG, "num_blocks must be >= 1");
+  if (max_blocks_per_seq < 1 || (int64_t)max_context > 16 * (int64_t)max_blocks_per_seq)
+    return fail(DQD_ERR_INVALID_ARG, "max_context (%d) exceeds 16 * max_blocks_per_seq (%d)", max_context,
+                max_blocks_per_seq);
+  if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
+    return fail(DQD_ERR_INVALID_ARG, "softmax_scale must be finite");
+  const void* ptrs[] = {q, k_pool, v_pool, out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return fail(DQD_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned device pointers");
+  if (!block_table || !context_lens || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(DQD_ERR_INVALID_ARG, "block_table and context_lens must be 4-byte aligned device pointers");
+  int sms = 0;
+  if ((st = sm_count(&sms)) != DQD_OK) return st;
+  const dqd::AttnPlan plan = dqd::plan_attn(b, w, hq, hkv, max_context, sms);
+  if ((int64_t)b * plan.qgroups > 65535)
+    return fail(DQD_ERR_UNSUPPORTED, "b * query groups exceeds the grid limit (b=%d)", b);
+  const size_t cap = dqd::attn_static_scratch_bytes();
+  if (plan.ws_bytes > cap)
+    return fail(DQD_ERR_WORKSPACE,
+                "gqa_decode_attn_static_ws: this call needs %zu bytes of scratch but the library's "
+                "static scratch holds %zu; use gqa_decode_attn with a caller workspace",
+                plan.ws_bytes, cap);
+  void* scratch = nullptr;
+  if (plan.ws_bytes > 0) {
+    cudaError_t e = dqd::attn_static_scratch(&scratch);
+    if (e != cudaSuccess)
+      return fail(DQD_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(e));
+  }
+  dqd::AttnLaunch l;
+  l.q = q;
+  l.k_pool = k_pool;
+  l.v_pool = v_pool;
+  l.num_blocks = num_blocks;
+  l.block_table = block_table;
+  l.max_blocks = max_blocks_per_seq;
+  l.context_lens = context_lens;
+  l.b = b;
+  l.w = w;
+  l.hq = hq;
+  l.hkv = hkv;
+  l.softmax_scale = softmax_scale;
+  l.out = out;
+  l.workspace = scratch;
+  return check_launch(dqd::launch_attn(l, plan, reinterpret_cast<cudaStream_t>(stream)),
+                      "gqa_decode_attn_static_ws launch");
+}
+
 }  // extern "C"

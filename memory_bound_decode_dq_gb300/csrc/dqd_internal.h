@@ -70,6 +70,11 @@ struct AttnLaunch {
 
 cudaError_t launch_attn(const AttnLaunch& a, const AttnPlan& p, cudaStream_t s);
 
+// Library-owned attention scratch (a static __device__ array in attn.cu):
+// its size, and its device address on the current device.
+size_t attn_static_scratch_bytes();
+cudaError_t attn_static_scratch(void** ptr);
+
 // -------------------------------------------------------------- formats --
 
 cudaError_t launch_pack_int4(const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,
