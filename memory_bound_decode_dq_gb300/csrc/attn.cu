@@ -356,7 +356,9 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const Args a) {
   }
 }
 
-// One warp per output row: combine the chunk partials of that row.
+// One warp per output row: combine the chunk partials of that row. Lane c
+// reads (m, l) of chunk c (32 chunks per pass); the o partials are then summed
+// in chunk order with their loads issued ahead of the adds.
 __global__ void __launch_bounds__(128) attn_merge_kernel(const Args a) {
   const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -367,21 +369,48 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const Args a) {
   const int nblk = (ctx + kBlk - 1) / kBlk;
   const int nch = min(a.nchunks, (nblk + a.chunk_blocks - 1) / a.chunk_blocks);
   const float* ml = a.part_ml + row * a.nchunks * 2;
+  const float* po = a.part_o + row * a.nchunks * kD + lane * 4;
   float mstar = kNegInf;
-  for (int c = 0; c < nch; ++c) mstar = fmaxf(mstar, ml[2 * c]);
+  for (int c = lane; c < nch; c += 32) mstar = fmaxf(mstar, ml[2 * c]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
   const float mbase = mstar == kNegInf ? 0.f : mstar;
-  float L = 0.f;
+  float lpart = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c = 0; c < nch; ++c) {
-    const float w = ex2(ml[2 * c] - mbase);
-    L += w * ml[2 * c + 1];
-    const float4 v = *reinterpret_cast<const float4*>(a.part_o + (row * a.nchunks + c) * kD + lane * 4);
-    acc.x += w * v.x;
-    acc.y += w * v.y;
-    acc.z += w * v.z;
-    acc.w += w * v.w;
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    const int c = c0 + lane;
+    float wl = 0.f;
+    if (c < nch) {
+      wl = ex2(ml[2 * c] - mbase);
+      lpart += wl * ml[2 * c + 1];
+    }
+    const int cnt = min(32, nch - c0);
+    int j = 0;
+    for (; j + 4 <= cnt; j += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcg(reinterpret_cast<const float4*>(po + (int64_t)(c0 + j + u) * kD));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float w = __shfl_sync(0xffffffffu, wl, j + u);
+        acc.x += w * v[u].x;
+        acc.y += w * v[u].y;
+        acc.z += w * v[u].z;
+        acc.w += w * v[u].w;
+      }
+    }
+    for (; j < cnt; ++j) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(po + (int64_t)(c0 + j) * kD));
+      const float w = __shfl_sync(0xffffffffu, wl, j);
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, off);
+  const float inv = lpart > 0.f ? 1.f / lpart : 0.f;
   uint2 o;
   o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
   o.y = pack_bf16x2(acc.z * inv, acc.w * inv);

@@ -305,19 +305,29 @@ __global__ void __launch_bounds__(kThreads) dq_gemm_kernel(const Args a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  float sum[MT][4];
-#pragma unroll
-  for (int j = 0; j < MT; ++j)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int64_t mm = m0 + 8 * j + 2 * t + (q & 1);
-      const int64_t nn = (q & 2) ? r1 : r0;
-      float sacc = 0.f;
-      if (tile_ok && mm < a.m && nn < a.n)
-        for (int sp = 0; sp < a.splits; ++sp) sacc += __ldcg(a.part + ((int64_t)sp * a.m + mm) * a.n + nn);
-      sum[j][q] = sacc;
+  // Cooperative reduction of the CTA's 64 x ROWS outputs: each thread owns
+  // whole outputs and sums their split partials in split order (loads issued
+  // ahead of the adds, so they overlap).
+  const int64_t n0 = (int64_t)blockIdx.x * kWarps * 16;
+  const int64_t S = a.splits, plane = a.m * a.n;
+  for (int e = threadIdx.x; e < kWarps * 16 * C::ROWS; e += kThreads) {
+    const int64_t nn = n0 + e / C::ROWS, mm = m0 + e % C::ROWS;
+    if (nn >= a.n || mm >= a.m) continue;
+    const float* p = a.part + mm * a.n + nn;
+    float sacc = 0.f;
+    int64_t sp = 0;
+    for (; sp + 4 <= S; sp += 4) {
+      const float v0 = __ldcg(p + sp * plane), v1 = __ldcg(p + (sp + 1) * plane);
+      const float v2 = __ldcg(p + (sp + 2) * plane), v3 = __ldcg(p + (sp + 3) * plane);
+      sacc += v0;
+      sacc += v1;
+      sacc += v2;
+      sacc += v3;
     }
-  store(sum);
+    for (; sp < S; ++sp) sacc += __ldcg(p + sp * plane);
+    if constexpr (WT == kFP8) sacc *= reinterpret_cast<const float*>(a.ws)[nn];
+    a.y[mm * a.n + nn] = f32_to_bf16(sacc);
+  }
   if (threadIdx.x == 0) *cnt = 0u;  // leave the counter at zero for the next call
 }
 
