@@ -91,6 +91,14 @@ DQD_API const char* dqd_last_error(void);
 /* Library version, e.g. "dqd 0.1 sm_103a". */
 DQD_API const char* dqd_version(void);
 
+/* Kernels never spin without bound: every wait on an asynchronous copy gives
+ * up after a fixed number of polls (seconds), records a flag in a device error
+ * word and ends the kernel (its output is then meaningless). This call
+ * synchronises with the current device, returns the OR of those flags in
+ * *flags (0: none; bit 0: a bounded wait gave up) and clears them. */
+#define DQD_DEVICE_ERR_WAIT_TIMEOUT 1u
+DQD_API dqd_status dqd_device_errors(uint32_t* flags);
+
 /* ------------------------------------------------------------------------
  * pack_int4_g128 — re-lay W4A16 INT4 g128 weights for dq_gemm.
  *

@@ -111,4 +111,11 @@ def longctx_70b_b8() -> Workload:
                     attns=(AttnCase("attn_64_8_b8_ctx131072", 8, 1, 64, 8, (131072,) * 8),))
 
 
-ALL = (tiny, llama3_8b_b1, dense70b_b32, verify_8b, longctx_70b_b8)
+def longctx_70b_b1() -> Workload:
+    """The long-context attention at one sequence (512 MiB of KV): the size
+    used for Nsight Compute captures of the long-context kernel."""
+    return Workload("longctx_70b_b1_ctx131072", 5,
+                    attns=(AttnCase("attn_64_8_b1_ctx131072", 1, 1, 64, 8, (131072,)),))
+
+
+ALL = (tiny, llama3_8b_b1, dense70b_b32, verify_8b, longctx_70b_b8, longctx_70b_b1)

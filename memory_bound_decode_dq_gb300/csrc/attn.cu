@@ -39,6 +39,8 @@
 #include <atomic>
 #include <cmath>
 #include <cstdlib>
+#include <cstring>
+#include <mutex>
 
 namespace dqd {
 namespace {
@@ -46,7 +48,6 @@ namespace {
 constexpr int kD = 128;
 constexpr int kBlk = 16;
 constexpr int kThreads = 128;
-constexpr int kStages = 3;
 constexpr int kBlockBytes = kBlk * kD * 2;  // one block, one kv head, K or V
 constexpr float kNegInf = -INFINITY;
 
@@ -65,56 +66,40 @@ struct Args {
   float scale_log2;
 };
 
-__device__ __forceinline__ int sigma(int r) { return (((r >> 1) & 3) << 1) ^ ((r & 1) << 2); }
-
 __device__ __forceinline__ int seq_ctx(const Args& a, int b) {
   int c = a.ctx[b];
   return max(0, min(c, a.max_blocks * kBlk));
 }
 
+// Per-module device error word (kErrWaitTimeout when a bounded wait gave up).
+__device__ unsigned int g_attn_error;
+
 template <int QT>
-struct Smem {
-  static constexpr int KS = 4 / QT;
-  static constexpr int STAGE = KS * 2 * kBlockBytes;  // K and V of KS blocks
-  static constexpr int RING = kStages * STAGE;
-  static constexpr int MERGE = 4 * 16 * (kD + 2) * 4;  // (o, m, l) per warp-row
-  static constexpr int BYTES = RING > MERGE ? RING : MERGE;
+struct Cfg {
+  static constexpr int KS = 4 / QT;                        // key-slot groups per CTA
+  static constexpr int NS = QT == 1 ? 3 : (QT == 2 ? 4 : 6);  // ring slots per group
+  static constexpr int SLOT = 2 * kBlockBytes;            // K (2 x 2 KB) + V (2 x 2 KB)
+  static constexpr int RING = KS * NS * SLOT;
+  static constexpr int MERGE = 4 * 16 * (kD + 2) * 4;     // (o, m, l) per warp-row
+  static constexpr int BODY = RING > MERGE ? RING : MERGE;
+  static constexpr int BARS = 2 * KS * NS * 8;            // full + empty mbarriers
+  static constexpr int BYTES = 1024 + BODY + BARS;        // + alignment slack
 };
 
-// Gather the KS blocks of stage s (block indices blk0 + s*KS + i) into ring slot.
-template <int QT>
-__device__ __forceinline__ void stage_kv(uint32_t slot, const Args& a, int b, int g, int blk_first,
-                                         int blk_end) {
-  constexpr int KS = Smem<QT>::KS;
-  constexpr int UNITS = kBlockBytes / 16;  // 256 per K (or V) block
-#pragma unroll
-  for (int i = 0; i < KS * 2 * UNITS / kThreads; ++i) {
-    const int u = threadIdx.x + i * kThreads;
-    const int blk_local = u / (2 * UNITS);
-    const int kv = (u / UNITS) & 1;
-    const int unit = u % UNITS;
-    const int blk = blk_first + blk_local;
-    const bool ok = blk < blk_end;
-    int64_t phys = 0;
-    if (ok) {
-      phys = a.table[(int64_t)b * a.max_blocks + blk];
-      phys = phys < 0 ? 0 : (phys >= a.num_blocks ? a.num_blocks - 1 : phys);
-    }
-    const uint16_t* base = kv ? a.vp : a.kp;
-    const uint16_t* src = base + ((phys * a.Hkv + g) * kBlk) * kD + unit * 8;
-    const int r = unit >> 4, cu = unit & 15;
-    const uint32_t dst = slot + blk_local * 2 * kBlockBytes + kv * kBlockBytes +
-                         (r * 16 + (cu ^ sigma(r))) * 16;
-    cp_async16(dst, ok ? src : a.kp, ok);
-  }
-  cp_async_commit();
+// K and V of one (block, kv head) arrive as four 2 KB TMA boxes of 16 rows x
+// 64 head dims, 128-byte swizzled: 16-byte unit u of row r sits at unit
+// u ^ (r & 7) of that row. Offsets inside a slot: K d<64, K d>=64, V d<64, V d>=64.
+__device__ __forceinline__ uint32_t kv_unit(uint32_t half_base, int row, int unit) {
+  return half_base + row * 128 + ((unit ^ (row & 7)) << 4);
 }
 
 template <int QT>
-__global__ void __launch_bounds__(kThreads) attn_split_kernel(const Args a) {
-  using S = Smem<QT>;
-  constexpr int KS = S::KS;
-  extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                              const __grid_constant__ CUtensorMap tmv,
+                                                              const Args a) {
+  using C = Cfg<QT>;
+  constexpr int KS = C::KS, NS = C::NS;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, t = lane & 3;
   const int chunk = blockIdx.x, g = blockIdx.y;
@@ -136,36 +121,86 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const Args a) {
     return;
   }
   const int blk_end = min(blk0 + a.chunk_blocks, nblk_seq);
-  const int nstages = (blk_end - blk0 + KS - 1) / KS;
-  const int qt = warp % QT, ks = warp / QT;
+  const int qt = warp % QT, grp = warp / QT;
+  const bool leader = qt == 0;
   const int row_base = (qg * QT + qt) * 16;  // first query row of this warp's tile
-  const uint32_t sring = smem_addr(smem);
 
-  // Prologue: start two stages.
-  stage_kv<QT>(sring, a, b, g, blk0, blk_end);
-  if (nstages > 1) stage_kv<QT>(sring + S::STAGE, a, b, g, blk0 + KS, blk_end);
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;
+  const uint32_t bars = ring + C::BODY;
+  auto full_bar = [&](int s) { return bars + (grp * NS + s) * 8; };
+  auto empty_bar = [&](int s) { return bars + (KS * NS + grp * NS + s) * 8; };
+  auto slot_addr = [&](int s) { return ring + (grp * NS + s) * C::SLOT; };
 
-  // Q fragments for this warp's 16 query rows, head dim permuted per 32-chunk.
-  uint32_t qf[4][2][4];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < KS * NS; ++i) {
+      mbar_init(bars + i * 8, 1);
+      mbar_init(bars + (KS * NS + i) * 8, QT);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // This group's blocks: blk0 + grp + KS * i for i in [0, nb).
+  const int span = blk_end - blk0;
+  const int nb = span > grp ? (span - grp + KS - 1) / KS : 0;
+  const int64_t tab_row = (int64_t)b * a.max_blocks;
+
+  // Leader warp: lane l caches the physical id of group block tab_base + l.
+  int tab_base = -1;
+  int32_t tab = 0;
+  auto phys_of = [&](int i) -> int {
+    if (tab_base < 0 || i - tab_base >= 32) {
+      tab_base = i;
+      const int blk = blk0 + grp + KS * (i + lane);
+      const int32_t v = (i + lane < nb) ? a.table[tab_row + blk] : 0;
+      tab = v < 0 ? 0 : (v >= a.num_blocks ? (int32_t)(a.num_blocks - 1) : v);
+    }
+    return __shfl_sync(0xffffffffu, tab, i - tab_base);
+  };
+  auto issue = [&](int i) {  // the whole leader warp calls; lane 0 issues
+    const int phys = phys_of(i);
+    if (lane == 0) {
+      const int s = i % NS;
+      const uint32_t dst = slot_addr(s), fb = full_bar(s);
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(fb, C::SLOT);
+      tma_load_4d(dst, &tmk, fb, 0, 0, g, phys);
+      tma_load_4d(dst + 2048, &tmk, fb, 64, 0, g, phys);
+      tma_load_4d(dst + 4096, &tmv, fb, 0, 0, g, phys);
+      tma_load_4d(dst + 6144, &tmv, fb, 64, 0, g, phys);
+    }
+  };
+  if (leader)
+    for (int i = 0; i < min(NS, nb); ++i) issue(i);
+
+  // Q fragments for this warp's 16 query rows. The head dimension is permuted
+  // inside each 64-wide half: lane t owns d = 16t .. 16t+15 (16-byte units 2t
+  // and 2t+1), MMA i of the half reads d = 16t + 4i .. +3. K is read the same way.
+  uint32_t qf[2][4][4];
   int pos_lo, pos_hi;  // last visible key index of rows gq and gq+8 (-1: none)
   {
     const int rl = row_base + gq, rh = rl + 8;
     const bool okl = rl < a.QR, okh = rh < a.QR;
     const int64_t ql = okl ? (((int64_t)b * a.W + rl / a.G) * a.Hq + g * a.G + rl % a.G) * kD : 0;
     const int64_t qh = okh ? (((int64_t)b * a.W + rh / a.G) * a.Hq + g * a.G + rh % a.G) * kD : 0;
+    const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      uint4 vl = okl ? *reinterpret_cast<const uint4*>(a.q + ql + 32 * c + 8 * t) : z;
-      uint4 vh = okh ? *reinterpret_cast<const uint4*>(a.q + qh + 32 * c + 8 * t) : z;
+    for (int dh = 0; dh < 2; ++dh)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        qf[c][e][0] = word(vl, 2 * e);
-        qf[c][e][1] = word(vh, 2 * e);
-        qf[c][e][2] = word(vl, 2 * e + 1);
-        qf[c][e][3] = word(vh, 2 * e + 1);
+      for (int u = 0; u < 2; ++u) {
+        const int d = 64 * dh + 16 * t + 8 * u;
+        const uint4 vl = okl ? *reinterpret_cast<const uint4*>(a.q + ql + d) : z;
+        const uint4 vh = okh ? *reinterpret_cast<const uint4*>(a.q + qh + d) : z;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = 2 * u + e;
+          qf[dh][i][0] = word(vl, 2 * e);
+          qf[dh][i][1] = word(vh, 2 * e);
+          qf[dh][i][2] = word(vl, 2 * e + 1);
+          qf[dh][i][3] = word(vh, 2 * e + 1);
+        }
       }
-    }
     pos_lo = okl ? ctx - a.W + rl / a.G : -1;
     pos_hi = okh ? ctx - a.W + rh / a.G : -1;
   }
@@ -174,33 +209,37 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const Args a) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m_lo = kNegInf, m_hi = kNegInf, l_lo = 0.f, l_hi = 0.f;
+  bool ok = true;
 
-  for (int s = 0; s < nstages; ++s) {
-    if (s + 1 < nstages) cp_async_wait<1>(); else cp_async_wait<0>();
-    __syncthreads();
-    if (s + 2 < nstages)
-      stage_kv<QT>(sring + ((s + 2) % kStages) * S::STAGE, a, b, g, blk0 + (s + 2) * KS, blk_end);
-    const int blk = blk0 + s * KS + ks;
-    if (blk >= blk_end) continue;
-    const uint32_t ks_addr = sring + (s % kStages) * S::STAGE + ks * 2 * kBlockBytes;
-    const uint32_t vs_addr = ks_addr + kBlockBytes;
-    const int key0 = blk * kBlk;
+  for (int i = 0; i < nb; ++i) {
+    const int s = i % NS;
+    if (!mbar_wait(full_bar(s), (i / NS) & 1)) {
+      if (lane == 0) atomicOr(&g_attn_error, kErrWaitTimeout);
+      ok = false;
+      break;
+    }
+    const uint32_t kb = slot_addr(s), vb = kb + 4096;
+    const int key0 = (blk0 + grp + KS * i) * kBlk;
     const int ntok = min(kBlk, ctx - key0);
 
-    // ---- S = Q K^T for 16 keys (two n8 halves) ----
+    // ---- S = Q K^T for 16 keys: two n8 halves, two accumulators each ----
     float sc[2][4];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      sc[h][0] = sc[h][1] = sc[h][2] = sc[h][3] = 0.f;
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
       const int r = 8 * h + gq;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 kv = lds128(ks_addr + (r * 16 + ((4 * c + t) ^ sigma(r))) * 16);
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          mma_bf16(sc[h], qf[c][e][0], qf[c][e][1], qf[c][e][2], qf[c][e][3], word(kv, 2 * e),
-                   word(kv, 2 * e + 1));
+      for (int dh = 0; dh < 2; ++dh) {
+        const uint4 k0 = lds128(kv_unit(kb + 2048 * dh, r, 2 * t));
+        const uint4 k1 = lds128(kv_unit(kb + 2048 * dh, r, 2 * t + 1));
+        float(&acc)[4] = dh ? sb : sa;
+        mma_bf16(acc, qf[dh][0][0], qf[dh][0][1], qf[dh][0][2], qf[dh][0][3], k0.x, k0.y);
+        mma_bf16(acc, qf[dh][1][0], qf[dh][1][1], qf[dh][1][2], qf[dh][1][3], k0.z, k0.w);
+        mma_bf16(acc, qf[dh][2][0], qf[dh][2][1], qf[dh][2][2], qf[dh][2][3], k1.x, k1.y);
+        mma_bf16(acc, qf[dh][3][0], qf[dh][3][1], qf[dh][3][2], qf[dh][3][3], k1.z, k1.w);
       }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sc[h][q] = sa[q] + sb[q];
     }
     // ---- mask, scale, online softmax ----
     float mx_lo = kNegInf, mx_hi = kNegInf;
@@ -240,39 +279,61 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const Args a) {
     l_lo = l_lo * al_lo + rs_lo;
     l_hi = l_hi * al_hi + rs_hi;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= al_lo;
-      o[i][1] *= al_lo;
-      o[i][2] *= al_hi;
-      o[i][3] *= al_hi;
+    for (int j = 0; j < 16; ++j) {
+      o[j][0] *= al_lo;
+      o[j][1] *= al_lo;
+      o[j][2] *= al_hi;
+      o[j][3] *= al_hi;
     }
     const uint32_t pa0 = pack_bf16x2(p[0][0], p[0][1]), pa1 = pack_bf16x2(p[0][2], p[0][3]);
     const uint32_t pa2 = pack_bf16x2(p[1][0], p[1][1]), pa3 = pack_bf16x2(p[1][2], p[1][3]);
 
-    // ---- O += P V ----
+    // ---- O += P V: n8 tile (h, jj), slot s <-> d = 64h + 8s + jj ----
     const int k0 = 2 * t, k1 = 2 * t + 1, k2 = 2 * t + 8, k3 = 2 * t + 9;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int u = 8 * h + gq;
-      uint4 va = lds128(vs_addr + (k0 * 16 + (u ^ sigma(k0))) * 16);
-      uint4 vb = lds128(vs_addr + (k1 * 16 + (u ^ sigma(k1))) * 16);
-      uint4 vc = lds128(vs_addr + (k2 * 16 + (u ^ sigma(k2))) * 16);
-      uint4 vd = lds128(vs_addr + (k3 * 16 + (u ^ sigma(k3))) * 16);
+      const uint32_t hb = vb + 2048 * h;
+      uint4 va = lds128(kv_unit(hb, k0, gq));
+      uint4 vv = lds128(kv_unit(hb, k1, gq));
+      uint4 vc = lds128(kv_unit(hb, k2, gq));
+      uint4 vd = lds128(kv_unit(hb, k3, gq));
       if (ntok < kBlk) {
         const uint4 z = make_uint4(0, 0, 0, 0);
         if (k0 >= ntok) va = z;
-        if (k1 >= ntok) vb = z;
+        if (k1 >= ntok) vv = z;
         if (k2 >= ntok) vc = z;
         if (k3 >= ntok) vd = z;
       }
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const uint32_t sel = (jj & 1) ? 0x7632u : 0x5410u;
-        const uint32_t b0 = prmt(word(va, jj >> 1), word(vb, jj >> 1), sel);
+        const uint32_t b0 = prmt(word(va, jj >> 1), word(vv, jj >> 1), sel);
         const uint32_t b1 = prmt(word(vc, jj >> 1), word(vd, jj >> 1), sel);
         mma_bf16(o[8 * h + jj], pa0, pa1, pa2, pa3, b0, b1);
       }
     }
+
+    // ---- release the slot and refill it ----
+    __syncwarp();
+    if constexpr (QT > 1) {
+      if (lane == 0) mbar_arrive(empty_bar(s));
+    }
+    if (leader && i + NS < nb) {
+      if constexpr (QT > 1) {
+        if (!mbar_wait(empty_bar(s), (i / NS) & 1)) {
+          if (lane == 0) atomicOr(&g_attn_error, kErrWaitTimeout);
+          ok = false;
+          break;
+        }
+      }
+      issue(i + NS);
+    }
+  }
+  if (!ok) {
+    // Drain the copies this group may still have in flight (bounded) before
+    // the shared memory is reused or released.
+    if (leader)
+      for (int i = 0; i < min(NS, nb); ++i) (void)mbar_wait(full_bar(i), 0);
   }
 
   // ---- merge the KS warps of each query tile through shared memory ----
@@ -280,8 +341,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const Args a) {
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  __syncthreads();  // ring no longer needed
-  float* mo = reinterpret_cast<float*>(smem);  // [warp][16 rows][130]
+  __syncthreads();  // every warp is done with the ring
+  float* mo = reinterpret_cast<float*>(smem_raw + (ring - raw));  // [warp][16 rows][130]
   {
     float* wbase = mo + warp * 16 * (kD + 2);
 #pragma unroll
@@ -417,21 +478,95 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const Args a) {
   *reinterpret_cast<uint2*>(a.out + row * kD + lane * 4) = o;
 }
 
+// ------------------------------------------------------------ tensor maps --
+// A 4-D tensor map over a KV pool [num_blocks][hkv][16][128] bf16 whose box is
+// 64 head dims x 16 tokens of one (block, kv head), 128-byte swizzled. The
+// encoder is reached through the runtime's driver entry point (no -lcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void* pool;
+  int64_t num_blocks;
+  int hkv;
+  bool operator==(const MapKey& o) const { return pool == o.pool && num_blocks == o.num_blocks && hkv == o.hkv; }
+};
+
+// Small cache: the same pools are used by every decode step.
+cudaError_t kv_tensor_map(const void* pool, int hkv, int64_t num_blocks, CUtensorMap* out) {
+  static std::mutex mu;
+  static MapKey keys[16];
+  static CUtensorMap maps[16];
+  static int used = 0, next = 0;
+  const MapKey key{pool, num_blocks, hkv};
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+      if (keys[i] == key) {
+        *out = maps[i];
+        return cudaSuccess;
+      }
+  }
+  EncodeTiledFn fn = encoder();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kBlk, (cuuint64_t)hkv, (cuuint64_t)num_blocks};
+  const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)kBlk * kD * 2,
+                                 (cuuint64_t)hkv * kBlk * kD * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)kBlk, 1, 1};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof m);
+  const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lk(mu);
+  keys[next] = key;
+  maps[next] = m;
+  next = (next + 1) % 16;
+  used = std::min(used + 1, 16);
+  *out = m;
+  return cudaSuccess;
+}
+
 template <int QT>
-cudaError_t launch_split(const Args& a, const AttnPlan& p, cudaStream_t s) {
-  using S = Smem<QT>;
-  static int configured[64] = {0};
+cudaError_t launch_split(const Args& a, const AttnPlan& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                         cudaStream_t s) {
+  using C = Cfg<QT>;
+  static std::atomic<int> configured[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<QT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
+    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::BYTES);
     if (e != cudaSuccess) return e;
-    configured[dev] = 1;
+    if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_relaxed);
   }
   dim3 grid(p.nchunks, a.Hkv, a.B * p.qgroups);
-  attn_split_kernel<QT><<<grid, kThreads, S::BYTES, s>>>(a);
+  attn_split_kernel<QT><<<grid, kThreads, C::BYTES, s>>>(tmk, tmv, a);
   return cudaGetLastError();
+}
+
+template <int QT>
+constexpr int ctas_per_sm() {
+  // shared memory (227 KB per SM usable) and registers (~165 per thread -> 3 CTAs)
+  return std::min(227 * 1024 / Cfg<QT>::BYTES, 3);
 }
 
 // Fixed scratch for gqa_decode_attn_static_ws, for callers that cannot
@@ -478,23 +613,36 @@ AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms) 
   const int ks = 4 / p.qt;
   const int maxblk = std::max(1, (max_context + kBlk - 1) / kBlk);
   const int64_t items = (int64_t)b * hkv * p.qgroups;
-  const int ctas_per_sm = p.qt == 1 ? 2 : (p.qt == 2 ? 3 : 6);
-  const int64_t target = (int64_t)std::max(num_sms, 1) * ctas_per_sm;
-  int64_t nch = std::max<int64_t>(1, (target + items - 1) / items);
-  nch = std::min<int64_t>(nch, (maxblk + ks - 1) / ks);
-  int cb = (int)((maxblk + nch - 1) / nch);
+  const int cps = p.qt == 1 ? ctas_per_sm<1>() : (p.qt == 2 ? ctas_per_sm<2>() : ctas_per_sm<4>());
+  const int64_t slots = (int64_t)std::max(num_sms, 1) * cps;
+  // About four waves of CTAs so that waves balance; each key-slot group gets
+  // at least four blocks, and a chunk's partial (o, m, l) per query row stays
+  // small next to the chunk's K/V bytes (cb >= 1.3 * rows).
+  const int cb_min = std::max(4 * ks, (13 * qr + 9) / 10);
+  int64_t nch = std::max<int64_t>(1, (4 * slots + items - 1) / items);
+  int cb = std::max<int>((int)((maxblk + nch - 1) / nch), cb_min);
   // Test hook: DQD_ATTN_CHUNK_BLOCKS forces the split-KV chunk size.
   if (const char* env = std::getenv("DQD_ATTN_CHUNK_BLOCKS")) {
     const long v = std::strtol(env, nullptr, 10);
-    if (v >= 1) cb = (int)std::min<long>(v, maxblk);
+    if (v >= 1) cb = (int)v;
   }
+  cb = std::min(cb, maxblk);
   cb = (cb + ks - 1) / ks * ks;
   p.chunk_blocks = cb;
   p.nchunks = (maxblk + cb - 1) / cb;
-  p.smem_bytes = p.qt == 1 ? Smem<1>::BYTES : (p.qt == 2 ? Smem<2>::BYTES : Smem<4>::BYTES);
+  p.smem_bytes = p.qt == 1 ? Cfg<1>::BYTES : (p.qt == 2 ? Cfg<2>::BYTES : Cfg<4>::BYTES);
   const size_t rows = (size_t)b * w * hq;
   p.ws_bytes = p.nchunks > 1 ? kCounterBytes + rows * p.nchunks * (kD + 2) * sizeof(float) : 0;
   return p;
+}
+
+cudaError_t attn_take_device_error(uint32_t* flags) {
+  uint32_t v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_attn_error, sizeof v);
+  if (e != cudaSuccess) return e;
+  if (v) e = cudaMemcpyToSymbol(g_attn_error, &zero, sizeof zero);
+  *flags |= v;
+  return e;
 }
 
 cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) {
@@ -525,11 +673,14 @@ cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) 
   a.nchunks = p.nchunks;
   a.qgroups = p.qgroups;
   a.scale_log2 = l.softmax_scale * 1.4426950408889634f;
-  cudaError_t e;
+  CUtensorMap tmk, tmv;
+  cudaError_t e = kv_tensor_map(l.k_pool, l.hkv, l.num_blocks, &tmk);
+  if (e == cudaSuccess) e = kv_tensor_map(l.v_pool, l.hkv, l.num_blocks, &tmv);
+  if (e != cudaSuccess) return e;
   switch (p.qt) {
-    case 1: e = launch_split<1>(a, p, s); break;
-    case 2: e = launch_split<2>(a, p, s); break;
-    default: e = launch_split<4>(a, p, s); break;
+    case 1: e = launch_split<1>(a, p, tmk, tmv, s); break;
+    case 2: e = launch_split<2>(a, p, tmk, tmv, s); break;
+    default: e = launch_split<4>(a, p, tmk, tmv, s); break;
   }
   if (e != cudaSuccess || p.nchunks == 1) return e;
   const int64_t blocks = ((int64_t)rows + 3) / 4;

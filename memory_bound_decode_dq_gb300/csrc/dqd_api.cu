@@ -103,6 +103,15 @@ const char* dqd_last_error(void) { return g_last_error.c_str(); }
 
 const char* dqd_version(void) { return "dqd 0.1 sm_103a"; }
 
+dqd_status dqd_device_errors(uint32_t* flags) {
+  g_last_error.clear();
+  if (!flags) return fail(DQD_ERR_INVALID_ARG, "flags is NULL");
+  *flags = 0;
+  cudaError_t e = dqd::attn_take_device_error(flags);
+  if (e != cudaSuccess) return fail(DQD_ERR_CUDA, "reading the device error words: %s", cudaGetErrorString(e));
+  return DQD_OK;
+}
+
 size_t pack_int4_g128_bytes(int64_t n, int64_t k, int which) {
   if (n < 1 || k < 128 || k % 128) return 0;
   const size_t blocks = (size_t)((n + 15) / 16) * (size_t)(k / 128);

@@ -75,6 +75,9 @@ cudaError_t launch_attn(const AttnLaunch& a, const AttnPlan& p, cudaStream_t s);
 size_t attn_static_scratch_bytes();
 cudaError_t attn_static_scratch(void** ptr);
 
+// ORs the attention module's device error word into *flags and clears it.
+cudaError_t attn_take_device_error(uint32_t* flags);
+
 // -------------------------------------------------------------- formats --
 
 cudaError_t launch_pack_int4(const uint8_t* codes, const uint16_t* scales, const uint8_t* zeros,

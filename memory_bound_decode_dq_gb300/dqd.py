@@ -44,6 +44,7 @@ _SIGS = {
     "dqd_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dqd_last_error": (ctypes.c_char_p, []),
     "dqd_version": (ctypes.c_char_p, []),
+    "dqd_device_errors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "pack_int4_g128_bytes": (_SZ, [_I64, _I64, ctypes.c_int]),
     "pack_int4_g128": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _P, _P, _P]),
     "quant_fp8_rowwise": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
@@ -75,6 +76,14 @@ def _check(status: int, where: str) -> None:
 
 def version() -> str:
     return _lib.dqd_version().decode()
+
+
+def device_errors() -> int:
+    """OR of the kernels' device error flags since the last call (0: none;
+    bit 0: a bounded wait on an asynchronous copy gave up). Synchronises."""
+    v = ctypes.c_uint32(0)
+    _check(_lib.dqd_device_errors(ctypes.byref(v)), "dqd_device_errors")
+    return int(v.value)
 
 
 def library() -> ctypes.CDLL:

@@ -175,3 +175,8 @@ def test_rejects_bad_arguments(dev, dqd):
     q = synth.normal_bf16(9, "q", (1, 1, 3, 128))
     with pytest.raises(dqd.DqdError):
         run(dqd, dev, q, kv, 2)          # 3 heads over 2 kv heads
+
+
+def test_no_device_error_flags_after_the_suite(dev, dqd):
+    """No bounded wait on an asynchronous copy gave up during this module."""
+    assert dqd.device_errors() == 0
