@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
   const int gq = lane >> 2, t = lane & 3;
   const int chunk = blockIdx.x, g = blockIdx.y;
   const int b = blockIdx.z / a.qgroups, qg = blockIdx.z % a.qgroups;
+  grid_dependency_wait();  // q, the tables and the cache may come from the previous kernel
+  allow_dependent_launch();
   const int ctx = seq_ctx(a, b);
   const int nblk_seq = (ctx + kBlk - 1) / kBlk;
   const int blk0 = chunk * a.chunk_blocks;
@@ -421,6 +423,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
 // reads (m, l) of chunk c (32 chunks per pass); the o partials are then summed
 // in chunk order with their loads issued ahead of the adds.
 __global__ void __launch_bounds__(128) attn_merge_kernel(const Args a) {
+  grid_dependency_wait();  // the partials come from the split kernel
+  allow_dependent_launch();
   const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)a.B * a.W * a.Hq;
@@ -559,8 +563,7 @@ cudaError_t launch_split(const Args& a, const AttnPlan& p, const CUtensorMap& tm
     if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_relaxed);
   }
   dim3 grid(p.nchunks, a.Hkv, a.B * p.qgroups);
-  attn_split_kernel<QT><<<grid, kThreads, C::BYTES, s>>>(tmk, tmv, a);
-  return cudaGetLastError();
+  return launch_pdl(attn_split_kernel<QT>, grid, dim3(kThreads), C::BYTES, s, tmk, tmv, a);
 }
 
 template <int QT>
@@ -684,8 +687,7 @@ cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) 
   }
   if (e != cudaSuccess || p.nchunks == 1) return e;
   const int64_t blocks = ((int64_t)rows + 3) / 4;
-  attn_merge_kernel<<<(unsigned)blocks, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(attn_merge_kernel, dim3((unsigned)blocks), dim3(128), 0, s, a);
 }
 
 }  // namespace dqd

@@ -7,20 +7,26 @@
 // 16-bit, and decode time is weight bytes over bandwidth.
 //
 // Design (HBM-bound at decode m):
-//  * A CTA is 4 warps; each warp owns one 16-row tile of W (the A operand of
-//    mma.m16n8k16, "swap-AB": weights fill the 16-row side, the m tokens the
-//    8-column side) and walks a k range. W is streamed straight from HBM into
-//    registers with 128-bit loads, double-buffered one pipeline stage ahead.
+//  * Each warp owns one 16-row tile of W: the weights are the A operand of
+//    mma.m16n8k16 ("swap-AB"), the m tokens its 8-column side. A CTA has 8
+//    warps for m <= 16 (4 for wider m) that share the activation stage.
+//  * W and x stream through a 3-stage cp.async ring in shared memory (one
+//    barrier per stage), so the bytes in flight per SM are set by the ring,
+//    not by registers. Rows past n, tokens past m and k past the end are
+//    zero-filled by the copies themselves.
 //  * Inside each 32-k (BF16/INT4) or 64-k (FP8) chunk, lane t owns a run of
-//    8 (16) consecutive k for rows g and g+8, so one 16-byte load feeds 2 (4)
-//    MMAs. The reduction index k is thereby permuted within the chunk; the
-//    activations are read with the same permutation, so the sum is unchanged.
-//  * x for the CTA's k stage sits in shared memory (cp.async, two stages),
-//    shared by the 4 warps; row strides are padded so the B-fragment loads
-//    are free of bank conflicts.
-//  * INT4: per 128-group, (q - z) is formed exactly in bf16 and the group's
-//    fp32 MMA sum is multiplied by the group scale. FP8: the E4M3 value is
-//    built exactly in bf16 and the per-row scale multiplies the fp32 total.
+//    8 (16) consecutive k for rows g and g+8, so one 16-byte shared load
+//    feeds 2 (4) MMAs. The reduction index is thereby permuted inside the
+//    chunk; x is read with the same permutation, so the sum is unchanged.
+//    The 16-byte units of odd rows are XOR-swizzled so both operands' loads
+//    are free of bank conflicts without padding.
+//  * INT4: OR-ing a code into the mantissa of bf16 128.0 gives 128 + q
+//    exactly and subtracting 128 + z in bf16 leaves q - z exactly, so the
+//    group's fp32 MMA sum is sum x (q - z); the group scale multiplies it.
+//    (A second MMA carrying the zero point would save three ALU operations
+//    per eight weights, but mma.sync throughput on this part is the tighter
+//    limit.) FP8: the E4M3 value is
+//    built exactly in bf16; the row scale multiplies the fp32 total.
 //  * Split-K when the n tiles alone cannot fill the GPU: each split writes
 //    fp32 partials; the last CTA to arrive (atomic ticket, no waiting) sums
 //    them in split order, so the result does not depend on arrival order.
@@ -28,29 +34,35 @@
 #include "dqd_internal.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 
 namespace dqd {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kCtasPerSmTarget = 3;
+constexpr int kStages = 3;
 
 __host__ __device__ constexpr int kc_base(int wt) { return wt == kBF16 ? 128 : (wt == kFP8 ? 256 : 512); }
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
 template <int WT, int MT>
 struct Cfg {
+  static constexpr int WARPS = MT <= 2 ? 8 : 4;
+  static constexpr int THREADS = WARPS * 32;
   static constexpr int ROWS = 8 * MT;                        // activation rows per CTA pass
   static constexpr int KC = cmin(kc_base(WT), 8192 / ROWS);  // k per pipeline stage
-  static constexpr int NLD = WT == kBF16 ? KC / 16 : (WT == kFP8 ? KC / 32 : KC / 64);  // 16B loads/lane/stage
-  static constexpr int PADB = WT == kFP8 ? 16 : 64;          // bank-conflict-free B loads
-  static constexpr int SROW = KC * 2 + PADB;                 // bytes per x row in smem
-  static constexpr int STAGE = ROWS * SROW;
-  static constexpr int SMEM = 2 * STAGE;
-  static constexpr int NGRP = KC / 128;                      // INT4 groups per stage
+  static constexpr int NG = KC / 128;                        // INT4 groups per stage
+  static constexpr int ESZ = WT == kBF16 ? 2 : 1;            // bytes per BF16/FP8 weight
+  static constexpr int WROWB = KC * ESZ;                     // bytes of one W row per stage
+  static constexpr int WSTAGE = WT == kINT4 ? WARPS * NG * 1024 : WARPS * 16 * WROWB;
+  static constexpr int MSTAGE = WT == kINT4 ? WARPS * NG * 48 : 0;  // INT4 scales + zeros
+  static constexpr int XROWB = KC * 2;                       // bytes of one x row per stage
 };
+
+// XOR on the 16-byte unit index of row r (see the header comment).
+template <int WT>
+__device__ __forceinline__ int xswz(int r) { return WT == kFP8 ? (r & 1) : ((r & 1) << 2); }
+__device__ __forceinline__ int wswz(int r) { return (r & 1) << 2; }
 
 struct Args {
   const uint8_t* w;        // BF16 rows / FP8 rows / packed INT4 codes
@@ -63,227 +75,262 @@ struct Args {
   int64_t m, n, k;
   int64_t k_per_split;
   int splits;
+  int ra;                  // activation rows held per stage (<= ROWS)
+  int slot;                // bytes per ring slot
 };
 
+__device__ __forceinline__ void cp_async8(uint32_t saddr, const void* gptr, bool pred) {
+  int n = pred ? 8 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(saddr), "l"(gptr), "r"(n) : "memory");
+}
+
+// Issue the weight copies of one k stage into one ring slot (no commit).
 template <int WT, int MT>
-__device__ __forceinline__ void stage_x(uint32_t sbase, const Args& a, int64_t m0, int64_t kst,
+__device__ __forceinline__ void issue_w(uint32_t slot, const Args& a, int64_t tile0, int64_t kst,
                                         int64_t kend) {
   using C = Cfg<WT, MT>;
-  constexpr int UPR = C::KC / 8;  // 16-byte units per row
+  const int tid = threadIdx.x;
+  if constexpr (WT != kINT4) {
+    constexpr int UPR = C::WROWB / 16;
+    constexpr int UNITS = C::WARPS * 16 * UPR;
+    constexpr int EPU = 16 / C::ESZ;  // weights per 16-byte unit
 #pragma unroll
-  for (int i = 0; i < (C::ROWS * UPR + kThreads - 1) / kThreads; ++i) {
-    int u = threadIdx.x + i * kThreads;
-    if (u < C::ROWS * UPR) {
-      int r = u / UPR, cu = u % UPR;
-      int64_t mm = m0 + r, kk = kst + (int64_t)cu * 8;
-      bool ok = mm < a.m && kk < kend;
-      const uint16_t* src = ok ? a.x + mm * a.k + kk : a.x;
-      cp_async16(sbase + r * C::SROW + cu * 16, src, ok);
+    for (int i = 0; i < (UNITS + C::THREADS - 1) / C::THREADS; ++i) {
+      const int u = tid + i * C::THREADS;
+      if (UNITS % C::THREADS == 0 || u < UNITS) {
+        const int r = u / UPR, cu = u % UPR;
+        const int64_t row = tile0 * 16 + r, kk = kst + (int64_t)cu * EPU;
+        const bool ok = row < a.n && kk < kend;
+        const uint8_t* src = ok ? a.w + (row * a.k + kk) * C::ESZ : a.w;
+        cp_async16(slot + r * C::WROWB + ((cu ^ wswz(r)) << 4), src, ok);
+      }
+    }
+  } else {
+    const int64_t G = a.k / 128, g0 = kst / 128, gend = kend / 128, NT = (a.n + 15) / 16;
+    constexpr int UNITS = C::WARPS * C::NG * 64;
+#pragma unroll
+    for (int i = 0; i < UNITS / C::THREADS; ++i) {
+      const int u = tid + i * C::THREADS;
+      const int wi = u / (C::NG * 64), rem = u % (C::NG * 64), j = rem / 64, cu = rem % 64;
+      const int64_t tile = tile0 + wi;
+      const bool ok = tile < NT && g0 + j < gend;
+      const uint8_t* src = ok ? a.w + (tile * G + g0 + j) * 1024 + cu * 16 : a.w;
+      cp_async16(slot + (wi * C::NG + j) * 1024 + cu * 16, src, ok);
+    }
+    const uint32_t meta = slot + C::WSTAGE;
+    for (int u = tid; u < C::WARPS * C::NG * 3; u += C::THREADS) {
+      const int wi = u / (C::NG * 3), rem = u % (C::NG * 3), j = rem / 3, part = rem % 3;
+      const int64_t tile = tile0 + wi;
+      const bool ok = tile < NT && g0 + j < gend;
+      const int64_t blk = tile * G + g0 + j;
+      const uint32_t dst = meta + (wi * C::NG + j) * 48;
+      if (part < 2)
+        cp_async16(dst + part * 16, ok ? a.ws + blk * 32 + part * 16 : a.ws, ok);
+      else
+        cp_async8(dst + 32, ok ? a.wz + blk * 8 : a.wz, ok);
     }
   }
-  cp_async_commit();
+}
+
+// Issue the activation copies of one k stage into one ring slot (no commit).
+template <int WT, int MT>
+__device__ __forceinline__ void issue_x(uint32_t slot, const Args& a, int64_t m0, int64_t kst, int64_t kend) {
+  using C = Cfg<WT, MT>;
+  const int tid = threadIdx.x;
+  const uint32_t xbase = slot + C::WSTAGE + C::MSTAGE;
+  constexpr int XUPR = C::XROWB / 16;
+  for (int u = tid; u < a.ra * XUPR; u += C::THREADS) {
+    const int r = u / XUPR, cu = u % XUPR;
+    const int64_t mm = m0 + r, kk = kst + (int64_t)cu * 8;
+    const bool ok = mm < a.m && kk < kend;
+    cp_async16(xbase + r * C::XROWB + ((cu ^ xswz<WT>(r)) << 4), ok ? a.x + mm * a.k + kk : a.x, ok);
+  }
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(saddr));
+  return r;
+}
+__device__ __forceinline__ uint32_t lds8(uint32_t saddr) {
+  uint16_t r;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(r) : "r"(saddr));
+  return r;
+}
+
+// One warp's MMAs for one stage. acc[j][*]: rows (g, g+8) x token columns
+// (8j + 2t, 8j + 2t + 1). ngroups bounds the INT4 groups inside [kbeg, kend).
+template <int WT, int MT>
+__device__ __forceinline__ void compute_stage(float (&acc)[MT][4], uint32_t slot, int warp, int lane,
+                                              int ra, int ngroups) {
+  using C = Cfg<WT, MT>;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t xbase = slot + C::WSTAGE + C::MSTAGE;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  if constexpr (WT == kBF16) {
+    const uint32_t wb = slot + warp * 16 * C::WROWB;
+#pragma unroll
+    for (int c = 0; c < C::KC / 32; ++c) {
+      const int unit = 4 * c + t;
+      const uint4 wa = lds128(wb + g * C::WROWB + ((unit ^ wswz(g)) << 4));
+      const uint4 wc = lds128(wb + (g + 8) * C::WROWB + ((unit ^ wswz(g)) << 4));
+      uint4 xv[MT];
+#pragma unroll
+      for (int j = 0; j < MT; ++j) {
+        const int r = 8 * j + g;
+        xv[j] = r < ra ? lds128(xbase + r * C::XROWB + ((unit ^ xswz<WT>(r)) << 4)) : zero;
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+#pragma unroll
+        for (int j = 0; j < MT; ++j)
+          mma_bf16(acc[j], word(wa, 2 * e), word(wc, 2 * e), word(wa, 2 * e + 1), word(wc, 2 * e + 1),
+                   word(xv[j], 2 * e), word(xv[j], 2 * e + 1));
+      }
+    }
+  } else if constexpr (WT == kFP8) {
+    const uint32_t wb = slot + warp * 16 * C::WROWB;
+#pragma unroll
+    for (int d = 0; d < C::KC / 64; ++d) {
+      const int unit = 4 * d + t;
+      const uint4 wa = lds128(wb + g * C::WROWB + ((unit ^ wswz(g)) << 4));
+      const uint4 wc = lds128(wb + (g + 8) * C::WROWB + ((unit ^ wswz(g)) << 4));
+      uint4 xa[MT], xb[MT];
+#pragma unroll
+      for (int j = 0; j < MT; ++j) {
+        const int r = 8 * j + g;
+        const int u0 = 8 * d + 2 * t;
+        xa[j] = r < ra ? lds128(xbase + r * C::XROWB + ((u0 ^ xswz<WT>(r)) << 4)) : zero;
+        xb[j] = r < ra ? lds128(xbase + r * C::XROWB + (((u0 + 1) ^ xswz<WT>(r)) << 4)) : zero;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t ug = word(wa, e), uh = word(wc, e);
+        const uint32_t a0 = fp8_lo_to_bf16x2(ug), a1 = fp8_lo_to_bf16x2(uh);
+        const uint32_t a2 = fp8_hi_to_bf16x2(ug), a3 = fp8_hi_to_bf16x2(uh);
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+          const uint4& xv = e < 2 ? xa[j] : xb[j];
+          mma_bf16(acc[j], a0, a1, a2, a3, word(xv, 2 * (e & 1)), word(xv, 2 * (e & 1) + 1));
+        }
+      }
+    }
+  } else {
+    const uint32_t wb = slot + warp * C::NG * 1024;
+    const uint32_t meta = slot + C::WSTAGE + warp * C::NG * 48;
+#pragma unroll
+    for (int jg = 0; jg < C::NG; ++jg) {
+      if (jg >= ngroups) break;  // past the end of k (warp-uniform)
+      const uint32_t sc = lds32(meta + jg * 48 + g * 4);
+      const uint32_t zr = lds8(meta + jg * 48 + 32 + g);
+      const uint32_t zlo = int4_zero_pair(zr), zhi = int4_zero_pair(zr >> 4);
+      const uint4 q0 = lds128(wb + jg * 1024 + lane * 16);
+      const uint4 q1 = lds128(wb + jg * 1024 + 512 + lane * 16);
+      float ga[MT][4];
+#pragma unroll
+      for (int j = 0; j < MT; ++j) ga[j][0] = ga[j][1] = ga[j][2] = ga[j][3] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint4 xv[MT];
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+          const int r = 8 * j + g;
+          const int unit = 16 * jg + 4 * c + t;
+          xv[j] = r < ra ? lds128(xbase + r * C::XROWB + ((unit ^ xswz<WT>(r)) << 4)) : zero;
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = 2 * c + e;
+          const Int4Frag f = int4_unpack(word(i < 4 ? q0 : q1, i & 3), zlo, zhi);
+#pragma unroll
+          for (int j = 0; j < MT; ++j)
+            mma_bf16(ga[j], f.a0, f.a1, f.a2, f.a3, word(xv[j], 2 * e), word(xv[j], 2 * e + 1));
+        }
+      }
+      const float slo = __uint_as_float(sc << 16), shi = __uint_as_float(sc & 0xFFFF0000u);
+#pragma unroll
+      for (int j = 0; j < MT; ++j) {
+        acc[j][0] = fmaf(slo, ga[j][0], acc[j][0]);
+        acc[j][1] = fmaf(slo, ga[j][1], acc[j][1]);
+        acc[j][2] = fmaf(shi, ga[j][2], acc[j][2]);
+        acc[j][3] = fmaf(shi, ga[j][3], acc[j][3]);
+      }
+    }
+  }
 }
 
 template <int WT, int MT>
-struct Warp {
-  using C = Cfg<WT, MT>;
-  uint4 w[C::NLD];
-  uint32_t sc[C::NGRP > 0 ? C::NGRP : 1];
-  uint32_t zr[C::NGRP > 0 ? C::NGRP : 1];
-
-  __device__ __forceinline__ void load(const Args& a, int64_t tile, int lane, int64_t kst,
-                                       int64_t kend, bool tile_ok) {
-    const int g = lane >> 2, t = lane & 3;
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    if constexpr (WT == kBF16) {
-      const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-      const bool ok0 = tile_ok && r0 < a.n, ok1 = tile_ok && r1 < a.n;
-#pragma unroll
-      for (int c = 0; c < C::KC / 32; ++c) {
-        int64_t kk = kst + 32 * c + 8 * t;
-        bool kok = kk < kend;
-        w[2 * c] = (ok0 && kok) ? ldg_stream(a.w + (r0 * a.k + kk) * 2) : z;
-        w[2 * c + 1] = (ok1 && kok) ? ldg_stream(a.w + (r1 * a.k + kk) * 2) : z;
-      }
-    } else if constexpr (WT == kFP8) {
-      const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-      const bool ok0 = tile_ok && r0 < a.n, ok1 = tile_ok && r1 < a.n;
-#pragma unroll
-      for (int d = 0; d < C::KC / 64; ++d) {
-        int64_t kk = kst + 64 * d + 16 * t;
-        bool kok = kk < kend;
-        w[2 * d] = (ok0 && kok) ? ldg_stream(a.w + r0 * a.k + kk) : z;
-        w[2 * d + 1] = (ok1 && kok) ? ldg_stream(a.w + r1 * a.k + kk) : z;
-      }
-    } else {
-      const int64_t G = a.k / 128, g0 = kst / 128, gend = kend / 128;
-#pragma unroll
-      for (int j = 0; j < C::NGRP; ++j) {
-        bool ok = tile_ok && g0 + j < gend;
-        int64_t blk = tile * G + g0 + j;
-        w[2 * j] = ok ? ldg_stream(a.w + blk * 1024 + lane * 16) : z;
-        w[2 * j + 1] = ok ? ldg_stream(a.w + blk * 1024 + 512 + lane * 16) : z;
-        sc[j] = ok ? ldg_u32(a.ws + blk * 32 + g * 4) : 0u;
-        zr[j] = ok ? ldg_u8(a.wz + blk * 8 + g) : 0u;
-      }
-    }
-  }
-
-  // acc[j][*]: rows (g, g+8) x token columns (8j + 2t, 8j + 2t + 1).
-  // ngroups: INT4 groups of this stage inside [kbeg, kend) (BF16/FP8 ignore it:
-  // their loads past kend are zero-filled on both operands).
-  __device__ __forceinline__ void compute(float (&acc)[MT][4], uint32_t sx, int lane,
-                                          int ngroups) const {
-    const int g = lane >> 2, t = lane & 3;
-    if constexpr (WT == kBF16) {
-#pragma unroll
-      for (int c = 0; c < C::KC / 32; ++c) {
-        uint4 xv[MT];
-#pragma unroll
-        for (int j = 0; j < MT; ++j) xv[j] = lds128(sx + (8 * j + g) * C::SROW + (32 * c + 8 * t) * 2);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          uint32_t a0 = word(w[2 * c], 2 * e), a1 = word(w[2 * c + 1], 2 * e);
-          uint32_t a2 = word(w[2 * c], 2 * e + 1), a3 = word(w[2 * c + 1], 2 * e + 1);
-#pragma unroll
-          for (int j = 0; j < MT; ++j)
-            mma_bf16(acc[j], a0, a1, a2, a3, word(xv[j], 2 * e), word(xv[j], 2 * e + 1));
-        }
-      }
-    } else if constexpr (WT == kFP8) {
-#pragma unroll
-      for (int d = 0; d < C::KC / 64; ++d) {
-        uint4 xa[MT], xb[MT];
-#pragma unroll
-        for (int j = 0; j < MT; ++j) {
-          uint32_t p = sx + (8 * j + g) * C::SROW + (64 * d + 16 * t) * 2;
-          xa[j] = lds128(p);
-          xb[j] = lds128(p + 16);
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint32_t ug = word(w[2 * d], e), uh = word(w[2 * d + 1], e);
-          uint32_t a0 = fp8_lo_to_bf16x2(ug), a1 = fp8_lo_to_bf16x2(uh);
-          uint32_t a2 = fp8_hi_to_bf16x2(ug), a3 = fp8_hi_to_bf16x2(uh);
-#pragma unroll
-          for (int j = 0; j < MT; ++j) {
-            const uint4& xv = e < 2 ? xa[j] : xb[j];
-            mma_bf16(acc[j], a0, a1, a2, a3, word(xv, 2 * (e & 1)), word(xv, 2 * (e & 1) + 1));
-          }
-        }
-      }
-    } else {
-#pragma unroll
-      for (int jg = 0; jg < C::NGRP; ++jg) {
-        if (jg >= ngroups) break;  // past the end of k (warp-uniform)
-        const uint32_t zlo = int4_zero_pair(zr[jg]), zhi = int4_zero_pair(zr[jg] >> 4);
-        float ga[MT][4];
-#pragma unroll
-        for (int j = 0; j < MT; ++j) ga[j][0] = ga[j][1] = ga[j][2] = ga[j][3] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4 xv[MT];
-#pragma unroll
-          for (int j = 0; j < MT; ++j)
-            xv[j] = lds128(sx + (8 * j + g) * C::SROW + (128 * jg + 32 * c + 8 * t) * 2);
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int i = 2 * c + e;
-            Int4Frag f = int4_unpack(word(w[2 * jg + (i >> 2)], i & 3), zlo, zhi);
-#pragma unroll
-            for (int j = 0; j < MT; ++j)
-              mma_bf16(ga[j], f.a0, f.a1, f.a2, f.a3, word(xv[j], 2 * e), word(xv[j], 2 * e + 1));
-          }
-        }
-        const float slo = __uint_as_float(sc[jg] << 16), shi = __uint_as_float(sc[jg] & 0xFFFF0000u);
-#pragma unroll
-        for (int j = 0; j < MT; ++j) {
-          acc[j][0] = fmaf(slo, ga[j][0], acc[j][0]);
-          acc[j][1] = fmaf(slo, ga[j][1], acc[j][1]);
-          acc[j][2] = fmaf(shi, ga[j][2], acc[j][2]);
-          acc[j][3] = fmaf(shi, ga[j][3], acc[j][3]);
-        }
-      }
-    }
-  }
-};
-
-template <int WT, int MT>
-__global__ void __launch_bounds__(kThreads) dq_gemm_kernel(const Args a) {
+__global__ void __launch_bounds__(Cfg<WT, MT>::THREADS) dq_gemm_kernel(const Args a) {
   using C = Cfg<WT, MT>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int64_t tile = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t tile0 = (int64_t)blockIdx.x * C::WARPS;
+  const int64_t tile = tile0 + warp;
   const int64_t ntiles = (a.n + 15) / 16;
   const bool tile_ok = tile < ntiles;
   const int64_t m0 = (int64_t)blockIdx.z * C::ROWS;
   const int64_t kbeg = (int64_t)blockIdx.y * a.k_per_split;
   const int64_t kend = min(a.k, kbeg + a.k_per_split);
-  const int nst = (int)((kend - kbeg + C::KC - 1) / C::KC);
-  const uint32_t sbuf0 = smem_addr(smem), sbuf1 = sbuf0 + C::STAGE;
+  const int nst = kend > kbeg ? (int)((kend - kbeg + C::KC - 1) / C::KC) : 0;
+  const uint32_t ring = smem_addr(smem);
 
   float acc[MT][4];
 #pragma unroll
   for (int j = 0; j < MT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
-  Warp<WT, MT> wa, wb;
-  if (nst > 0) {
-    stage_x<WT, MT>(sbuf0, a, m0, kbeg, kend);
-    wa.load(a, tile, lane, kbeg, kend, tile_ok);
+  // Weights are constant: their first stages are fetched before waiting for
+  // the preceding kernel; activations (and every write) come after the wait.
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s)
+    if (s < nst) issue_w<WT, MT>(ring + s * a.slot, a, tile0, kbeg + (int64_t)s * C::KC, kend);
+  grid_dependency_wait();
+  allow_dependent_launch();
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < nst) issue_x<WT, MT>(ring + s * a.slot, a, m0, kbeg + (int64_t)s * C::KC, kend);
+    cp_async_commit();
   }
-  for (int s = 0; s < nst; s += 2) {
-    const int64_t k1 = kbeg + (int64_t)(s + 1) * C::KC;
-    if (s + 1 < nst) {
-      stage_x<WT, MT>(sbuf1, a, m0, k1, kend);
-      wb.load(a, tile, lane, k1, kend, tile_ok);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  for (int s = 0; s < nst; ++s) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    const int sn = s + kStages - 1;
+    if (sn < nst) {
+      const uint32_t slot = ring + (sn % kStages) * a.slot;
+      issue_w<WT, MT>(slot, a, tile0, kbeg + (int64_t)sn * C::KC, kend);
+      issue_x<WT, MT>(slot, a, m0, kbeg + (int64_t)sn * C::KC, kend);
     }
-    __syncthreads();
-    if (tile_ok) wa.compute(acc, sbuf0, lane, (int)((kend - (kbeg + (int64_t)s * C::KC) + 127) / 128));
-    __syncthreads();
-    if (s + 1 >= nst) break;
-    const int64_t k2 = k1 + C::KC;
-    if (s + 2 < nst) {
-      stage_x<WT, MT>(sbuf0, a, m0, k2, kend);
-      wa.load(a, tile, lane, k2, kend, tile_ok);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    cp_async_commit();
+    if (tile_ok) {
+      const int64_t kst = kbeg + (int64_t)s * C::KC;
+      compute_stage<WT, MT>(acc, ring + (s % kStages) * a.slot, warp, lane, a.ra,
+                            (int)((kend - kst + 127) / 128));
     }
-    __syncthreads();
-    if (tile_ok) wb.compute(acc, sbuf1, lane, (int)((kend - k1 + 127) / 128));
-    __syncthreads();
   }
+  cp_async_wait<0>();
 
   // ---- epilogue ----
   const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-  auto scale_row = [&](int64_t r) -> float {
-    if constexpr (WT == kFP8) return (tile_ok && r < a.n) ? reinterpret_cast<const float*>(a.ws)[r] : 0.f;
-    return 1.f;
-  };
-  auto store = [&](float (&v)[MT][4]) {
+  if (a.splits == 1) {
     if (!tile_ok) return;
-    const float s0 = scale_row(r0), s1 = scale_row(r1);
+    float s0 = 1.f, s1 = 1.f;
+    if constexpr (WT == kFP8) {
+      const float* sc = reinterpret_cast<const float*>(a.ws);
+      s0 = r0 < a.n ? sc[r0] : 0.f;
+      s1 = r1 < a.n ? sc[r1] : 0.f;
+    }
 #pragma unroll
-    for (int j = 0; j < MT; ++j) {
+    for (int j = 0; j < MT; ++j)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int64_t mm = m0 + 8 * j + 2 * t + (q & 1);
         const int64_t nn = (q & 2) ? r1 : r0;
         if (mm < a.m && nn < a.n) {
-          float val = v[j][q];
-          if constexpr (WT == kFP8) val *= (q & 2) ? s1 : s0;
-          a.y[mm * a.n + nn] = f32_to_bf16(val);
+          float v = acc[j][q];
+          if constexpr (WT == kFP8) v *= (q & 2) ? s1 : s0;
+          a.y[mm * a.n + nn] = f32_to_bf16(v);
         }
       }
-    }
-  };
-
-  if (a.splits == 1) {
-    store(acc);
     return;
   }
   // split-K: publish fp32 partials, then the last-arriving CTA reduces.
@@ -305,12 +352,11 @@ __global__ void __launch_bounds__(kThreads) dq_gemm_kernel(const Args a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // Cooperative reduction of the CTA's 64 x ROWS outputs: each thread owns
-  // whole outputs and sums their split partials in split order (loads issued
-  // ahead of the adds, so they overlap).
-  const int64_t n0 = (int64_t)blockIdx.x * kWarps * 16;
+  // Cooperative reduction of the CTA's outputs: each thread owns whole outputs
+  // and sums their split partials in split order (loads issued ahead of adds).
+  const int64_t n0 = tile0 * 16;
   const int64_t S = a.splits, plane = a.m * a.n;
-  for (int e = threadIdx.x; e < kWarps * 16 * C::ROWS; e += kThreads) {
+  for (int e = threadIdx.x; e < C::WARPS * 16 * C::ROWS; e += C::THREADS) {
     const int64_t nn = n0 + e / C::ROWS, mm = m0 + e % C::ROWS;
     if (nn >= a.n || mm >= a.m) continue;
     const float* p = a.part + mm * a.n + nn;
@@ -331,10 +377,42 @@ __global__ void __launch_bounds__(kThreads) dq_gemm_kernel(const Args a) {
   if (threadIdx.x == 0) *cnt = 0u;  // leave the counter at zero for the next call
 }
 
+struct KernelInfo {
+  int warps, kc, wstage, mstage, xrowb, rows;
+};
+
+template <int WT, int MT>
+KernelInfo info_t() {
+  using C = Cfg<WT, MT>;
+  return {C::WARPS, C::KC, C::WSTAGE, C::MSTAGE, C::XROWB, C::ROWS};
+}
+
+KernelInfo info_of(int wt, int mt) {
+#define DQD_INFO(W)                          \
+  switch (mt) {                              \
+    case 1: return info_t<W, 1>();           \
+    case 2: return info_t<W, 2>();           \
+    case 4: return info_t<W, 4>();           \
+    default: return info_t<W, 8>();          \
+  }
+  if (wt == kBF16) { DQD_INFO(kBF16) }
+  if (wt == kFP8) { DQD_INFO(kFP8) }
+  DQD_INFO(kINT4)
+#undef DQD_INFO
+}
+
 template <int WT, int MT>
 cudaError_t launch_t(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   using C = Cfg<WT, MT>;
-  static_assert(C::SMEM <= 48 * 1024, "x stages must fit the default shared-memory window");
+  static std::atomic<int> configured[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || configured[dev].load(std::memory_order_relaxed) < p.smem_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(dq_gemm_kernel<WT, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev].store(p.smem_bytes, std::memory_order_relaxed);
+  }
   Args a;
   a.w = static_cast<const uint8_t*>(l.data);
   a.ws = static_cast<const uint8_t*>(l.scales);
@@ -349,9 +427,10 @@ cudaError_t launch_t(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   a.k = l.k;
   a.k_per_split = p.k_per_split;
   a.splits = p.splits;
+  a.ra = p.ra;
+  a.slot = p.slot_bytes;
   dim3 grid(p.grid_x, p.splits, p.m_chunks);
-  dq_gemm_kernel<WT, MT><<<grid, kThreads, C::SMEM, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(dq_gemm_kernel<WT, MT>, grid, dim3(C::THREADS), p.smem_bytes, s, a);
 }
 
 template <int WT>
@@ -364,47 +443,42 @@ cudaError_t launch_wt(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   }
 }
 
-template <int WT>
-int kc_of(int mt) {
-  switch (mt) {
-    case 1: return Cfg<WT, 1>::KC;
-    case 2: return Cfg<WT, 2>::KC;
-    case 4: return Cfg<WT, 4>::KC;
-    default: return Cfg<WT, 8>::KC;
-  }
-}
-template <int WT>
-int smem_of(int mt) {
-  switch (mt) {
-    case 1: return Cfg<WT, 1>::SMEM;
-    case 2: return Cfg<WT, 2>::SMEM;
-    case 4: return Cfg<WT, 4>::SMEM;
-    default: return Cfg<WT, 8>::SMEM;
-  }
-}
-
 }  // namespace
 
 GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
   GemmPlan p{};
   p.mt = m <= 8 ? 1 : (m <= 16 ? 2 : (m <= 32 ? 4 : 8));
-  const int64_t rows = 8 * p.mt;
+  const KernelInfo ki = info_of(wtype, p.mt);
+  const int64_t rows = ki.rows;
   p.m_chunks = (int)((m + rows - 1) / rows);
   const int64_t ntiles = (n + 15) / 16;
-  p.grid_x = (int)((ntiles + kWarps - 1) / kWarps);
-  switch (wtype) {
-    case kBF16: p.kc = kc_of<kBF16>(p.mt); p.smem_bytes = smem_of<kBF16>(p.mt); break;
-    case kFP8: p.kc = kc_of<kFP8>(p.mt); p.smem_bytes = smem_of<kFP8>(p.mt); break;
-    default: p.kc = kc_of<kINT4>(p.mt); p.smem_bytes = smem_of<kINT4>(p.mt); break;
-  }
+  p.grid_x = (int)((ntiles + ki.warps - 1) / ki.warps);
+  p.kc = ki.kc;
+  p.ra = (int)std::min<int64_t>(rows, m);
+  p.slot_bytes = (ki.wstage + ki.mstage + p.ra * ki.xrowb + 127) / 128 * 128;
+  p.smem_bytes = kStages * p.slot_bytes;
   const int64_t stages = std::max<int64_t>(1, (k + p.kc - 1) / p.kc);
   const int64_t base = (int64_t)p.grid_x * p.m_chunks;
-  const int64_t slots = (int64_t)std::max(num_sms, 1) * kCtasPerSmTarget;
+  const int cps = std::max(1, std::min(227 * 1024 / std::max(p.smem_bytes, 1), 16 / ki.warps));
+  const int64_t slots = (int64_t)std::max(num_sms, 1) * cps;
+  // Split k only as far as needed to fill the GPU; prefer the smallest split
+  // whose CTA count wastes little of the last wave.
+  const double wbytes = wtype == kBF16 ? 2.0 * n * k : (wtype == kFP8 ? 1.0 * n * k : 0.52 * n * k);
   int64_t splits = 1;
-  if (base < slots) splits = (slots + base - 1) / base;
-  // fp32 partial traffic stays a small fraction of the weight stream
-  const double wbytes = wtype == kBF16 ? 2.0 * n * k : (wtype == kFP8 ? 1.0 * n * k : 0.53 * n * k);
-  while (splits > 1 && 8.0 * splits * m * n > 0.25 * wbytes) --splits;
+  if (base < 2 * slots) {
+    double best = 0.0;
+    for (int64_t sp = 1; sp <= std::min<int64_t>(stages, 64); ++sp) {
+      if (sp > 1 && 8.0 * sp * m * n > 0.25 * wbytes) break;
+      const int64_t ctas = base * sp;
+      const double waves = (double)((ctas + slots - 1) / slots);
+      const double eff = (double)ctas / (waves * slots);
+      if (eff > best + 0.05) {
+        best = eff;
+        splits = sp;
+      }
+      if (eff >= 0.9) break;
+    }
+  }
   // counters must fit their reserved region
   if ((size_t)base * 4 > kCounterBytes) splits = 1;
   // Test hook: DQD_GEMM_SPLITS forces the k split (results must not depend on it

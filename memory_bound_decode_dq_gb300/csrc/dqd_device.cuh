@@ -168,6 +168,19 @@ __device__ __forceinline__ uint32_t fp8_hi_to_bf16x2(uint32_t u) {
   return fp8_pair_to_bf16x2(u, 0xB3A2u);
 }
 
+// ------------------------------------------- programmatic dependent launch ----
+// Kernels are launched so that the next kernel on the stream may start while
+// this one drains. Every kernel waits (griddepcontrol.wait, a hardware wait
+// for the preceding grid to complete and flush) before it reads anything a
+// preceding kernel may have written or writes anything it may read; only
+// constant operands (weights) are prefetched before that point.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------ mbarrier + TMA ----
 
 // Upper bound on polls of one mbarrier phase before a wait gives up. Each

@@ -6,8 +6,28 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 namespace dqd {
+
+// Launch `kernel` on `stream` with programmatic stream serialisation, so that
+// it may begin while the previous kernel on the stream finishes (the kernel
+// itself waits for that kernel before touching dependent data).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 enum WType { kBF16 = 0, kFP8 = 1, kINT4 = 2 };
 
@@ -18,10 +38,12 @@ constexpr size_t kCounterBytes = 65536;  // = DQD_WS_COUNTER_BYTES
 struct GemmPlan {
   int mt;            // m8 tiles per CTA pass (1, 2, 4, 8)
   int m_chunks;      // ceil(m / (8*mt))
-  int grid_x;        // CTAs along n (4 row tiles of 16 each)
+  int grid_x;        // CTAs along n (one 16-row tile per warp)
   int splits;        // CTAs along k
   int64_t k_per_split;
   int kc;            // k per pipeline stage
+  int ra;            // activation rows staged per CTA (<= 8 * mt)
+  int slot_bytes;    // bytes per shared-memory ring slot
   int smem_bytes;    // dynamic shared memory per CTA
   size_t ws_bytes;   // workspace needed (0 if splits == 1)
 };
