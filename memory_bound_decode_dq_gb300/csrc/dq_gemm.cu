@@ -42,6 +42,9 @@ namespace {
 
 constexpr int kStages = 3;
 
+// Per-module device error word (kErrWaitTimeout when a bounded wait gave up).
+__device__ unsigned int g_gemm_error;
+
 __host__ __device__ constexpr int kc_base(int wt) { return wt == kBF16 ? 128 : (wt == kFP8 ? 256 : 512); }
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
@@ -259,57 +262,14 @@ __device__ __forceinline__ void compute_stage(float (&acc)[MT][4], uint32_t slot
   }
 }
 
-template <int WT, int MT>
-__global__ void __launch_bounds__(Cfg<WT, MT>::THREADS) dq_gemm_kernel(const Args a) {
-  using C = Cfg<WT, MT>;
-  extern __shared__ __align__(128) uint8_t smem[];
+// Epilogue shared by the dq_gemm kernels (every thread of the CTA calls it):
+// bf16 output, or fp32 split-K partials reduced by the last-arriving CTA.
+template <int WT, int MT, int WARPS, int THREADS>
+__device__ __forceinline__ void finish(const Args& a, float (&acc)[MT][4], int64_t tile0, int64_t m0,
+                                       bool tile_ok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int64_t tile0 = (int64_t)blockIdx.x * C::WARPS;
   const int64_t tile = tile0 + warp;
-  const int64_t ntiles = (a.n + 15) / 16;
-  const bool tile_ok = tile < ntiles;
-  const int64_t m0 = (int64_t)blockIdx.z * C::ROWS;
-  const int64_t kbeg = (int64_t)blockIdx.y * a.k_per_split;
-  const int64_t kend = min(a.k, kbeg + a.k_per_split);
-  const int nst = kend > kbeg ? (int)((kend - kbeg + C::KC - 1) / C::KC) : 0;
-  const uint32_t ring = smem_addr(smem);
-
-  float acc[MT][4];
-#pragma unroll
-  for (int j = 0; j < MT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-  // Weights are constant: their first stages are fetched before waiting for
-  // the preceding kernel; activations (and every write) come after the wait.
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s)
-    if (s < nst) issue_w<WT, MT>(ring + s * a.slot, a, tile0, kbeg + (int64_t)s * C::KC, kend);
-  grid_dependency_wait();
-  allow_dependent_launch();
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < nst) issue_x<WT, MT>(ring + s * a.slot, a, m0, kbeg + (int64_t)s * C::KC, kend);
-    cp_async_commit();
-  }
-  for (int s = 0; s < nst; ++s) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
-    const int sn = s + kStages - 1;
-    if (sn < nst) {
-      const uint32_t slot = ring + (sn % kStages) * a.slot;
-      issue_w<WT, MT>(slot, a, tile0, kbeg + (int64_t)sn * C::KC, kend);
-      issue_x<WT, MT>(slot, a, m0, kbeg + (int64_t)sn * C::KC, kend);
-    }
-    cp_async_commit();
-    if (tile_ok) {
-      const int64_t kst = kbeg + (int64_t)s * C::KC;
-      compute_stage<WT, MT>(acc, ring + (s % kStages) * a.slot, warp, lane, a.ra,
-                            (int)((kend - kst + 127) / 128));
-    }
-  }
-  cp_async_wait<0>();
-
-  // ---- epilogue ----
   const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
   if (a.splits == 1) {
     if (!tile_ok) return;
@@ -356,8 +316,8 @@ __global__ void __launch_bounds__(Cfg<WT, MT>::THREADS) dq_gemm_kernel(const Arg
   // and sums their split partials in split order (loads issued ahead of adds).
   const int64_t n0 = tile0 * 16;
   const int64_t S = a.splits, plane = a.m * a.n;
-  for (int e = threadIdx.x; e < C::WARPS * 16 * C::ROWS; e += C::THREADS) {
-    const int64_t nn = n0 + e / C::ROWS, mm = m0 + e % C::ROWS;
+  for (int e = threadIdx.x; e < WARPS * 16 * (8 * MT); e += THREADS) {
+    const int64_t nn = n0 + e / (8 * MT), mm = m0 + e % (8 * MT);
     if (nn >= a.n || mm >= a.m) continue;
     const float* p = a.part + mm * a.n + nn;
     float sacc = 0.f;
@@ -377,14 +337,248 @@ __global__ void __launch_bounds__(Cfg<WT, MT>::THREADS) dq_gemm_kernel(const Arg
   if (threadIdx.x == 0) *cnt = 0u;  // leave the counter at zero for the next call
 }
 
+template <int WT, int MT>
+__global__ void __launch_bounds__(Cfg<WT, MT>::THREADS) dq_gemm_kernel(const Args a) {
+  using C = Cfg<WT, MT>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t tile0 = (int64_t)blockIdx.x * C::WARPS;
+  const int64_t tile = tile0 + warp;
+  const int64_t ntiles = (a.n + 15) / 16;
+  const bool tile_ok = tile < ntiles;
+  const int64_t m0 = (int64_t)blockIdx.z * C::ROWS;
+  const int64_t kbeg = (int64_t)blockIdx.y * a.k_per_split;
+  const int64_t kend = min(a.k, kbeg + a.k_per_split);
+  const int nst = kend > kbeg ? (int)((kend - kbeg + C::KC - 1) / C::KC) : 0;
+  const uint32_t ring = smem_addr(smem);
+
+  float acc[MT][4];
+#pragma unroll
+  for (int j = 0; j < MT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+  // Weights are constant: their first stages are fetched before waiting for
+  // the preceding kernel; activations (and every write) come after the wait.
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s)
+    if (s < nst) issue_w<WT, MT>(ring + s * a.slot, a, tile0, kbeg + (int64_t)s * C::KC, kend);
+  grid_dependency_wait();
+  allow_dependent_launch();
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < nst) issue_x<WT, MT>(ring + s * a.slot, a, m0, kbeg + (int64_t)s * C::KC, kend);
+    cp_async_commit();
+  }
+  for (int s = 0; s < nst; ++s) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    const int sn = s + kStages - 1;
+    if (sn < nst) {
+      const uint32_t slot = ring + (sn % kStages) * a.slot;
+      issue_w<WT, MT>(slot, a, tile0, kbeg + (int64_t)sn * C::KC, kend);
+      issue_x<WT, MT>(slot, a, m0, kbeg + (int64_t)sn * C::KC, kend);
+    }
+    cp_async_commit();
+    if (tile_ok) {
+      const int64_t kst = kbeg + (int64_t)s * C::KC;
+      compute_stage<WT, MT>(acc, ring + (s % kStages) * a.slot, warp, lane, a.ra,
+                            (int)((kend - kst + 127) / 128));
+    }
+  }
+  cp_async_wait<0>();
+
+  finish<WT, MT, C::WARPS, C::THREADS>(a, acc, tile0, m0, tile_ok);
+}
+
+// ------------------------------------------------------------------------
+// INT4 g128, warp-specialised: WARPS consumer warps (one 16-row tile each)
+// and one producer warp that moves each k stage with bulk asynchronous copies
+// (the packed codes and scales of a tile are contiguous per stage, and so is
+// each activation row), completing on a per-slot mbarrier. Consumers release
+// a slot through a second mbarrier; nobody touches copy addressing except the
+// producer. Zero points are read with ordinary loads one stage ahead.
+template <int MT>
+struct Int4Cfg {
+  static constexpr int WARPS = MT <= 2 ? 8 : 4;
+  static constexpr int THREADS = (WARPS + 1) * 32;
+  static constexpr int ROWS = 8 * MT;
+  static constexpr int KC = cmin(512, 8192 / ROWS);
+  static constexpr int NG = KC / 128;
+  static constexpr int NS = 3;                               // ring slots
+  static constexpr int CODES = WARPS * NG * 1024;
+  static constexpr int SCALES = WARPS * NG * 32;
+  static constexpr int XSTR = KC * 2 + 64;                    // padded activation row
+};
+
+template <int MT>
+__global__ void __launch_bounds__(Int4Cfg<MT>::THREADS) dq_gemm_int4_kernel(const Args a) {
+  using C = Int4Cfg<MT>;
+  constexpr int NS = C::NS;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[2 * NS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t tile0 = (int64_t)blockIdx.x * C::WARPS;
+  const int64_t ntiles = (a.n + 15) / 16;
+  const bool consumer = warp < C::WARPS;
+  const int64_t tile = tile0 + warp;
+  const bool tile_ok = consumer && tile < ntiles;
+  const int64_t m0 = (int64_t)blockIdx.z * C::ROWS;
+  const int64_t kbeg = (int64_t)blockIdx.y * a.k_per_split;
+  const int64_t kend = min(a.k, kbeg + a.k_per_split);
+  const int nst = kend > kbeg ? (int)((kend - kbeg + C::KC - 1) / C::KC) : 0;
+  const int rows_valid = (int)min((int64_t)a.ra, a.m - m0);
+  const int64_t G = a.k / 128;
+  const uint32_t ring = smem_addr(smem);
+  const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[NS]);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, C::WARPS);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  float acc[MT][4];
+#pragma unroll
+  for (int j = 0; j < MT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  bool ok = true;
+
+  if (!consumer) {
+    // ---------------- producer warp ----------------
+    auto stage_groups = [&](int s) { return (int)min((int64_t)C::NG, (kend - kbeg) / 128 - (int64_t)s * C::NG); };
+    auto stage_bytes = [&](int s) {
+      const int ng = stage_groups(s);
+      int nt = (int)min((int64_t)C::WARPS, ntiles - tile0);
+      return (uint32_t)(nt * ng * (1024 + 32) + rows_valid * ng * 256);
+    };
+    // lane w < WARPS copies tile w's codes and scales; lanes >= 16 copy activation rows
+    auto issue_w = [&](int s) {
+      const uint32_t slot = ring + (s % NS) * a.slot, fb = full0 + 8 * (s % NS);
+      const int ng = stage_groups(s);
+      if (lane == 0) mbar_arrive_expect_tx(fb, stage_bytes(s));
+      __syncwarp();
+      const int64_t g0 = (kbeg + (int64_t)s * C::KC) / 128;
+      if (lane < C::WARPS && tile0 + lane < ntiles) {
+        const int64_t blk = (tile0 + lane) * G + g0;
+        bulk_load(slot + lane * C::NG * 1024, a.w + blk * 1024, ng * 1024, fb);
+        bulk_load(slot + C::CODES + lane * C::NG * 32, a.ws + blk * 32, ng * 32, fb);
+      }
+    };
+    auto issue_x = [&](int s) {
+      const uint32_t slot = ring + (s % NS) * a.slot, fb = full0 + 8 * (s % NS);
+      const int ng = stage_groups(s);
+      const int64_t kst = kbeg + (int64_t)s * C::KC;
+      for (int r = lane; r < rows_valid; r += 32)
+        bulk_load(slot + C::CODES + C::SCALES + r * C::XSTR, a.x + (m0 + r) * a.k + kst, ng * 256, fb);
+    };
+    const int pre = min(NS, nst);
+    for (int s = 0; s < pre; ++s) issue_w(s);  // weights are constant: fetch ahead
+    grid_dependency_wait();
+    allow_dependent_launch();
+    for (int s = 0; s < pre; ++s) issue_x(s);
+    for (int s = NS; s < nst; ++s) {
+      if (!mbar_wait(empty0 + 8 * (s % NS), ((s / NS) - 1) & 1)) {
+        if (lane == 0) atomicOr(&g_gemm_error, kErrWaitTimeout);
+        ok = false;
+        break;
+      }
+      issue_w(s);
+      issue_x(s);
+    }
+  } else {
+    // ---------------- consumer warps ----------------
+    grid_dependency_wait();
+    allow_dependent_launch();
+    uint32_t znext[C::NG];
+    auto load_zeros = [&](int s, uint32_t (&z)[C::NG]) {
+      const int64_t g0 = (kbeg + (int64_t)s * C::KC) / 128, gend = kend / 128;
+#pragma unroll
+      for (int j = 0; j < C::NG; ++j)
+        z[j] = (tile_ok && g0 + j < gend) ? ldg_u8(a.wz + (tile * G + g0 + j) * 8 + g) : 0u;
+    };
+    if (nst > 0) load_zeros(0, znext);
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int s = 0; s < nst; ++s) {
+      const int slot_i = s % NS;
+      if (!mbar_wait(full0 + 8 * slot_i, (s / NS) & 1)) {
+        if (lane == 0) atomicOr(&g_gemm_error, kErrWaitTimeout);
+        ok = false;
+        break;
+      }
+      uint32_t zcur[C::NG];
+#pragma unroll
+      for (int j = 0; j < C::NG; ++j) zcur[j] = znext[j];
+      if (s + 1 < nst) load_zeros(s + 1, znext);
+      const uint32_t slot = ring + slot_i * a.slot;
+      const uint32_t wb = slot + warp * C::NG * 1024;
+      const uint32_t sb = slot + C::CODES + warp * C::NG * 32;
+      const uint32_t xb = slot + C::CODES + C::SCALES;
+      const int64_t kst = kbeg + (int64_t)s * C::KC;
+      const int ngroups = (int)((kend - kst) / 128);
+      if (tile_ok) {
+#pragma unroll
+        for (int jg = 0; jg < C::NG; ++jg) {
+          if (jg >= ngroups) break;
+          const uint32_t sc = lds32(sb + jg * 32 + g * 4);
+          const uint32_t zlo = int4_zero_pair(zcur[jg]), zhi = int4_zero_pair(zcur[jg] >> 4);
+          const uint4 q0 = lds128(wb + jg * 1024 + lane * 16);
+          const uint4 q1 = lds128(wb + jg * 1024 + 512 + lane * 16);
+          float ga[MT][4];
+#pragma unroll
+          for (int j = 0; j < MT; ++j) ga[j][0] = ga[j][1] = ga[j][2] = ga[j][3] = 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4 xv[MT];
+#pragma unroll
+            for (int j = 0; j < MT; ++j) {
+              const int r = 8 * j + g;
+              xv[j] = r < rows_valid ? lds128(xb + r * C::XSTR + (jg * 128 + 32 * c + 8 * t) * 2) : zero;
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = 2 * c + e;
+              const Int4Frag f = int4_unpack(word(i < 4 ? q0 : q1, i & 3), zlo, zhi);
+#pragma unroll
+              for (int j = 0; j < MT; ++j)
+                mma_bf16(ga[j], f.a0, f.a1, f.a2, f.a3, word(xv[j], 2 * e), word(xv[j], 2 * e + 1));
+            }
+          }
+          const float slo = __uint_as_float(sc << 16), shi = __uint_as_float(sc & 0xFFFF0000u);
+#pragma unroll
+          for (int j = 0; j < MT; ++j) {
+            acc[j][0] = fmaf(slo, ga[j][0], acc[j][0]);
+            acc[j][1] = fmaf(slo, ga[j][1], acc[j][1]);
+            acc[j][2] = fmaf(shi, ga[j][2], acc[j][2]);
+            acc[j][3] = fmaf(shi, ga[j][3], acc[j][3]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * slot_i);
+    }
+  }
+  if (!ok) {
+    // Let the copies already in flight land (bounded) before the CTA moves on.
+    for (int i = 0; i < min(NS, nst); ++i) (void)mbar_wait(full0 + 8 * i, 0);
+  }
+  finish<kINT4, MT, C::WARPS, C::THREADS>(a, acc, tile0, m0, tile_ok);
+}
+
 struct KernelInfo {
-  int warps, kc, wstage, mstage, xrowb, rows;
+  int warps, kc, wstage, mstage, xrowb, rows, stages;
 };
 
 template <int WT, int MT>
 KernelInfo info_t() {
-  using C = Cfg<WT, MT>;
-  return {C::WARPS, C::KC, C::WSTAGE, C::MSTAGE, C::XROWB, C::ROWS};
+  if constexpr (WT == kINT4) {
+    using C = Int4Cfg<MT>;
+    return {C::WARPS, C::KC, C::CODES, C::SCALES, C::XSTR, C::ROWS, C::NS};
+  } else {
+    using C = Cfg<WT, MT>;
+    return {C::WARPS, C::KC, C::WSTAGE, C::MSTAGE, C::XROWB, C::ROWS, kStages};
+  }
 }
 
 KernelInfo info_of(int wt, int mt) {
@@ -408,8 +602,10 @@ cudaError_t launch_t(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || configured[dev].load(std::memory_order_relaxed) < p.smem_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(dq_gemm_kernel<WT, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         p.smem_bytes);
+    cudaError_t e = WT == kINT4 ? cudaFuncSetAttribute(dq_gemm_int4_kernel<MT>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes)
+                                : cudaFuncSetAttribute(dq_gemm_kernel<WT, MT>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev].store(p.smem_bytes, std::memory_order_relaxed);
   }
@@ -430,7 +626,10 @@ cudaError_t launch_t(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   a.ra = p.ra;
   a.slot = p.slot_bytes;
   dim3 grid(p.grid_x, p.splits, p.m_chunks);
-  return launch_pdl(dq_gemm_kernel<WT, MT>, grid, dim3(C::THREADS), p.smem_bytes, s, a);
+  if constexpr (WT == kINT4)
+    return launch_pdl(dq_gemm_int4_kernel<MT>, grid, dim3(Int4Cfg<MT>::THREADS), p.smem_bytes, s, a);
+  else
+    return launch_pdl(dq_gemm_kernel<WT, MT>, grid, dim3(C::THREADS), p.smem_bytes, s, a);
 }
 
 template <int WT>
@@ -456,10 +655,10 @@ GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
   p.kc = ki.kc;
   p.ra = (int)std::min<int64_t>(rows, m);
   p.slot_bytes = (ki.wstage + ki.mstage + p.ra * ki.xrowb + 127) / 128 * 128;
-  p.smem_bytes = kStages * p.slot_bytes;
+  p.smem_bytes = ki.stages * p.slot_bytes;
   const int64_t stages = std::max<int64_t>(1, (k + p.kc - 1) / p.kc);
   const int64_t base = (int64_t)p.grid_x * p.m_chunks;
-  const int cps = std::max(1, std::min(227 * 1024 / std::max(p.smem_bytes, 1), 16 / ki.warps));
+  const int cps = std::max(1, std::min((227 * 1024 - 1024) / std::max(p.smem_bytes, 1), 16 / ki.warps));
   const int64_t slots = (int64_t)std::max(num_sms, 1) * cps;
   // Split k only as far as needed to fill the GPU; prefer the smallest split
   // whose CTA count wastes little of the last wave.
@@ -494,6 +693,15 @@ GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
   p.k_per_split = per * p.kc;
   p.ws_bytes = p.splits > 1 ? kCounterBytes + sizeof(float) * (size_t)p.splits * m * n : 0;
   return p;
+}
+
+cudaError_t gemm_take_device_error(uint32_t* flags) {
+  uint32_t v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof v);
+  if (e != cudaSuccess) return e;
+  if (v) e = cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof zero);
+  *flags |= v;
+  return e;
 }
 
 cudaError_t launch_dq_gemm(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {

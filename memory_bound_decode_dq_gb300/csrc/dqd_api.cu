@@ -108,6 +108,7 @@ dqd_status dqd_device_errors(uint32_t* flags) {
   if (!flags) return fail(DQD_ERR_INVALID_ARG, "flags is NULL");
   *flags = 0;
   cudaError_t e = dqd::attn_take_device_error(flags);
+  if (e == cudaSuccess) e = dqd::gemm_take_device_error(flags);
   if (e != cudaSuccess) return fail(DQD_ERR_CUDA, "reading the device error words: %s", cudaGetErrorString(e));
   return DQD_OK;
 }

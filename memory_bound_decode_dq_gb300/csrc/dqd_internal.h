@@ -63,6 +63,9 @@ struct GemmLaunch {
 
 cudaError_t launch_dq_gemm(const GemmLaunch& a, const GemmPlan& p, cudaStream_t s);
 
+// ORs the GEMM module's device error word into *flags and clears it.
+cudaError_t gemm_take_device_error(uint32_t* flags);
+
 // ------------------------------------------------------------ attention --
 
 struct AttnPlan {

@@ -102,12 +102,13 @@ def test_fp8_ragged_k(dev, dqd, k):
 
 @pytest.mark.parametrize("wtype", WT, ids=WT_IDS)
 @pytest.mark.parametrize("split", [1, 2, 3, 7, 64])
-def test_every_split_count(dev, dqd, splits, wtype, split):
+@pytest.mark.parametrize("m", [5, 20, 40])
+def test_every_split_count(dev, dqd, splits, wtype, split, m):
     splits(split)
     c = Case(dqd, dev, wtype, 96, 2048, seed=split)
-    x = synth.normal_bf16(split, "x", (5, 2048))
+    x = synth.normal_bf16(split + m, "x", (m, 2048))
     y = dqd.dq_gemm(c.weight, bf(x, dev))
-    assert_close(f64(y), c.ref(x), what=f"splits={split}")
+    assert_close(f64(y), c.ref(x), what=f"splits={split} m={m}")
 
 
 @pytest.mark.parametrize("wtype", WT, ids=WT_IDS)
