@@ -39,8 +39,6 @@
 #include <atomic>
 #include <cmath>
 #include <cstdlib>
-#include <cstring>
-#include <mutex>
 
 namespace dqd {
 namespace {
@@ -482,71 +480,13 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const Args a) {
   *reinterpret_cast<uint2*>(a.out + row * kD + lane * 4) = o;
 }
 
-// ------------------------------------------------------------ tensor maps --
 // A 4-D tensor map over a KV pool [num_blocks][hkv][16][128] bf16 whose box is
-// 64 head dims x 16 tokens of one (block, kv head), 128-byte swizzled. The
-// encoder is reached through the runtime's driver entry point (no -lcuda).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                   CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encoder() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-struct MapKey {
-  const void* pool;
-  int64_t num_blocks;
-  int hkv;
-  bool operator==(const MapKey& o) const { return pool == o.pool && num_blocks == o.num_blocks && hkv == o.hkv; }
-};
-
-// Small cache: the same pools are used by every decode step.
+// 64 head dims x 16 tokens of one (block, kv head), 128-byte swizzled.
 cudaError_t kv_tensor_map(const void* pool, int hkv, int64_t num_blocks, CUtensorMap* out) {
-  static std::mutex mu;
-  static MapKey keys[16];
-  static CUtensorMap maps[16];
-  static int used = 0, next = 0;
-  const MapKey key{pool, num_blocks, hkv};
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    for (int i = 0; i < used; ++i)
-      if (keys[i] == key) {
-        *out = maps[i];
-        return cudaSuccess;
-      }
-  }
-  EncodeTiledFn fn = encoder();
-  if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kBlk, (cuuint64_t)hkv, (cuuint64_t)num_blocks};
-  const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)kBlk * kD * 2,
-                                 (cuuint64_t)hkv * kBlk * kD * 2};
-  const cuuint32_t box[4] = {64, (cuuint32_t)kBlk, 1, 1};
-  const cuuint32_t elem[4] = {1, 1, 1, 1};
-  CUtensorMap m;
-  std::memset(&m, 0, sizeof m);
-  const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims, strides, box, elem,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  std::lock_guard<std::mutex> lk(mu);
-  keys[next] = key;
-  maps[next] = m;
-  next = (next + 1) % 16;
-  used = std::min(used + 1, 16);
-  *out = m;
-  return cudaSuccess;
+  const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)kBlk, (uint64_t)hkv, (uint64_t)num_blocks};
+  const uint64_t strides[3] = {(uint64_t)kD * 2, (uint64_t)kBlk * kD * 2, (uint64_t)hkv * kBlk * kD * 2};
+  const uint32_t box[4] = {64, (uint32_t)kBlk, 1, 1};
+  return tensor_map(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int QT>

@@ -2,6 +2,7 @@
 // launchers. Host-only declarations.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -31,6 +32,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 enum WType { kBF16 = 0, kFP8 = 1, kINT4 = 2 };
 
+// Tiled TMA tensor map over `base` (rank <= 5; dims innermost first; strides
+// in bytes for dims 1..rank-1), zero fill out of bounds. Encoded maps are
+// cached, keyed by every argument.
+cudaError_t tensor_map(CUtensorMap* out, CUtensorMapDataType dtype, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       CUtensorMapSwizzle swizzle);
+
 constexpr size_t kCounterBytes = 65536;  // = DQD_WS_COUNTER_BYTES
 
 // ---------------------------------------------------------------- dq_gemm --
@@ -50,6 +58,7 @@ struct GemmPlan {
 
 GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms);
 
+
 struct GemmLaunch {
   int wtype;
   const void* data;
@@ -63,7 +72,7 @@ struct GemmLaunch {
 
 cudaError_t launch_dq_gemm(const GemmLaunch& a, const GemmPlan& p, cudaStream_t s);
 
-// ORs the GEMM module's device error word into *flags and clears it.
+// OR the GEMM module's device error word into *flags and clear it.
 cudaError_t gemm_take_device_error(uint32_t* flags);
 
 // ------------------------------------------------------------ attention --

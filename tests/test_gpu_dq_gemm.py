@@ -212,3 +212,21 @@ def test_workspace_too_small_is_rejected(dev, dqd):
     with pytest.raises(dqd.DqdError) as e:
         dqd.dq_gemm(c.weight, x, ws=small)
     assert e.value.status == dqd.DQD_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("wtype", WT, ids=WT_IDS)
+@pytest.mark.parametrize("m,n,k", [(1, 16, 4096), (8, 16, 8192), (3, 48, 128), (1, 8, 256), (2, 40, 2048),
+                                   (1, 17, 8192), (7, 4112, 1024)])
+def test_small_m_stream_shapes(dev, dqd, wtype, m, n, k):
+    """m <= 8 runs the persistent stream: one tile shared by many warps, fewer
+    units than warps, ragged n, and wide grids."""
+    c = Case(dqd, dev, wtype, n, k, seed=m + n + k)
+    x = synth.normal_bf16(m * n + k, "x", (m, k))
+    a = dqd.dq_gemm(c.weight, bf(x, dev))
+    assert_close(f64(a), c.ref(x), what=f"stream {WT_IDS[wtype]} m={m} n={n} k={k}")
+    b = dqd.dq_gemm(c.weight, bf(x, dev))
+    assert np.array_equal(bits(a), bits(b))  # piece order fixed: bit-identical reruns
+
+
+def test_no_device_error_flags(dev, dqd):
+    assert dqd.device_errors() == 0
