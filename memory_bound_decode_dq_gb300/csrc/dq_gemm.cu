@@ -645,6 +645,9 @@ cudaError_t launch_wt(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
 }  // namespace
 
 GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
+  // Test hook: DQD_GEMM_TC=0 keeps wide-m shapes on the warp-MMA kernels.
+  const char* tc_env = std::getenv("DQD_GEMM_TC");
+  if (tc_supported(wtype, m, n, k) && !(tc_env && tc_env[0] == '0')) return plan_dq_gemm_tc(m, n, k);
   GemmPlan p{};
   p.mt = m <= 8 ? 1 : (m <= 16 ? 2 : (m <= 32 ? 4 : 8));
   const KernelInfo ki = info_of(wtype, p.mt);
@@ -701,10 +704,12 @@ cudaError_t gemm_take_device_error(uint32_t* flags) {
   if (e != cudaSuccess) return e;
   if (v) e = cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof zero);
   *flags |= v;
-  return e;
+  if (e != cudaSuccess) return e;
+  return tc_take_device_error(flags);
 }
 
 cudaError_t launch_dq_gemm(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
+  if (p.tc) return launch_dq_gemm_tc(l, p, s);
   switch (l.wtype) {
     case kBF16: return launch_wt<kBF16>(l, p, s);
     case kFP8: return launch_wt<kFP8>(l, p, s);

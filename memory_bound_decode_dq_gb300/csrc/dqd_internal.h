@@ -44,6 +44,7 @@ constexpr size_t kCounterBytes = 65536;  // = DQD_WS_COUNTER_BYTES
 // ---------------------------------------------------------------- dq_gemm --
 
 struct GemmPlan {
+  int tc;            // 1: tensor-core (tcgen05) kernel for wide m, INT4 only
   int mt;            // m8 tiles per CTA pass (1, 2, 4, 8)
   int m_chunks;      // ceil(m / (8*mt))
   int grid_x;        // CTAs along n (one 16-row tile per warp)
@@ -71,6 +72,13 @@ struct GemmLaunch {
 };
 
 cudaError_t launch_dq_gemm(const GemmLaunch& a, const GemmPlan& p, cudaStream_t s);
+
+// tcgen05 path (dq_gemm_tc.cu): whether it takes this shape, its plan, its
+// launch, and its device error word.
+bool tc_supported(int wtype, int64_t m, int64_t n, int64_t k);
+GemmPlan plan_dq_gemm_tc(int64_t m, int64_t n, int64_t k);
+cudaError_t launch_dq_gemm_tc(const GemmLaunch& a, const GemmPlan& p, cudaStream_t s);
+cudaError_t tc_take_device_error(uint32_t* flags);
 
 // OR the GEMM module's device error word into *flags and clear it.
 cudaError_t gemm_take_device_error(uint32_t* flags);

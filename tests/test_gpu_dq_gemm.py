@@ -218,8 +218,8 @@ def test_workspace_too_small_is_rejected(dev, dqd):
 @pytest.mark.parametrize("m,n,k", [(1, 16, 4096), (8, 16, 8192), (3, 48, 128), (1, 8, 256), (2, 40, 2048),
                                    (1, 17, 8192), (7, 4112, 1024)])
 def test_small_m_stream_shapes(dev, dqd, wtype, m, n, k):
-    """m <= 8 runs the persistent stream: one tile shared by many warps, fewer
-    units than warps, ragged n, and wide grids."""
+    """Small m over long k, a single 16-row tile, fewer tiles than warps per
+    CTA, ragged n and wide grids."""
     c = Case(dqd, dev, wtype, n, k, seed=m + n + k)
     x = synth.normal_bf16(m * n + k, "x", (m, k))
     a = dqd.dq_gemm(c.weight, bf(x, dev))

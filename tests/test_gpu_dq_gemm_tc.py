@@ -1,0 +1,81 @@
+"""GPU parity of the tensor-core (tcgen05) INT4 dq_gemm path taken at wide m
+(speculative verify batches), against the float64 oracle and against the
+warp-MMA kernels on the same inputs.
+
+Shapes span several 128-row weight tiles and 128-token chunks with ragged n
+(partial 16-row tiles and CTAs with fewer than eight tiles), ragged m and
+k from one group to 32 groups."""
+import numpy as np
+import pytest
+
+import oracle
+from memory_bound_decode_dq_gb300 import synth
+from gpu_util import assert_close, bf, bits, f64, require_cuda, u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_cuda()
+
+
+@pytest.fixture(scope="module")
+def dqd():
+    from memory_bound_decode_dq_gb300 import dqd as m
+    return m
+
+
+def _weight(dqd, dev, n, k, seed):
+    wq = synth.int4_weight(seed, "w", n, k)
+    p = dqd.pack_int4_g128(u8(wq.codes, dev), bf(wq.scales, dev), u8(wq.zeros, dev))
+    return wq, dqd.Weight.int4(p)
+
+
+SHAPES = [(128, 128, 128), (129, 1000, 256), (256, 2048, 1024), (300, 48, 4096), (1024, 130, 512),
+          (500, 4112, 384), (200, 16, 128), (384, 6144, 4096)]
+
+
+@pytest.mark.parametrize("m,n,k", SHAPES)
+def test_against_oracle(dev, dqd, m, n, k):
+    wq, w = _weight(dqd, dev, n, k, seed=m + n + k)
+    x = synth.normal_bf16(m * 7 + k, "x", (m, k))
+    y = dqd.dq_gemm(w, bf(x, dev))
+    assert y.shape == (m, n)
+    rows = None if n * m * k <= 2 ** 28 else np.unique(np.r_[0, n - 1, np.arange(0, n, 97)])
+    ref = oracle.dq_gemm(oracle.W_INT4_G128, wq.codes, wq.scales, wq.zeros, x, rows=rows)
+    got = f64(y) if rows is None else f64(y)[:, rows]
+    assert_close(got, ref, what=f"tc int4 m={m} n={n} k={k}")
+
+
+@pytest.mark.parametrize("m,n,k", [(128, 256, 512), (777, 1040, 2048)])
+def test_matches_warp_mma_path(dev, dqd, monkeypatch, m, n, k):
+    wq, w = _weight(dqd, dev, n, k, seed=3)
+    x = bf(synth.normal_bf16(3, "x", (m, k)), dev)
+    a = f64(dqd.dq_gemm(w, x))
+    monkeypatch.setenv("DQD_GEMM_TC", "0")
+    b = f64(dqd.dq_gemm(w, x))
+    assert_close(a, b, what="tcgen05 vs mma.sync")
+
+
+def test_rerun_is_bit_identical(dev, dqd):
+    _, w = _weight(dqd, dev, 3000, 1024, seed=11)
+    x = bf(synth.normal_bf16(11, "x", (640, 1024)), dev)
+    assert np.array_equal(bits(dqd.dq_gemm(w, x)), bits(dqd.dq_gemm(w, x)))
+
+
+def test_one_hot_reads_back_dequantised_weights(dev, dqd):
+    """128 one-hot tokens per call: y[t] = bf16((q - z) * s) of column t,
+    bit for bit, over ragged n."""
+    n, k = 200, 384
+    wq, w = _weight(dqd, dev, n, k, seed=21)
+    deq = oracle.int4_dequant(wq.codes, wq.scales, wq.zeros)
+    for start in range(0, k, 128):
+        x = np.zeros((128, k), np.uint16)
+        x[np.arange(128), start + np.arange(128)] = 0x3F80
+        y = bits(dqd.dq_gemm(w, bf(x, dev)))
+        assert np.array_equal(y, deq[:, start:start + 128].T)
+
+
+def test_no_device_error_flags(dev, dqd):
+    assert dqd.device_errors() == 0
