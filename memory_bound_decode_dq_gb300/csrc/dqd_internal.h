@@ -76,7 +76,7 @@ cudaError_t launch_dq_gemm(const GemmLaunch& a, const GemmPlan& p, cudaStream_t 
 // tcgen05 path (dq_gemm_tc.cu): whether it takes this shape, its plan, its
 // launch, and its device error word.
 bool tc_supported(int wtype, int64_t m, int64_t n, int64_t k);
-GemmPlan plan_dq_gemm_tc(int64_t m, int64_t n, int64_t k);
+GemmPlan plan_dq_gemm_tc(int64_t m, int64_t n, int64_t k, int num_sms);
 cudaError_t launch_dq_gemm_tc(const GemmLaunch& a, const GemmPlan& p, cudaStream_t s);
 cudaError_t tc_take_device_error(uint32_t* flags);
 

@@ -79,3 +79,25 @@ def test_one_hot_reads_back_dequantised_weights(dev, dqd):
 
 def test_no_device_error_flags(dev, dqd):
     assert dqd.device_errors() == 0
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 5, 10])
+def test_every_split_count(dev, dqd, monkeypatch, split):
+    """k split on group boundaries (the last split shorter), partials summed
+    by the last-arriving CTA in split order."""
+    monkeypatch.setenv("DQD_GEMM_SPLITS", str(split))
+    m, n, k = 300, 500, 1280
+    wq, w = _weight(dqd, dev, n, k, seed=split)
+    x = synth.normal_bf16(split, "x", (m, k))
+    xd = bf(x, dev)
+    y = dqd.dq_gemm(w, xd)
+    ref = oracle.dq_gemm(oracle.W_INT4_G128, wq.codes, wq.scales, wq.zeros, x)
+    assert_close(f64(y), ref, what=f"tc splits={split}")
+    assert np.array_equal(bits(y), bits(dqd.dq_gemm(w, xd)))
+
+
+def test_planner_splits_a_small_grid(dev, dqd):
+    """384 tokens over a 4096 x 14336 weight is 64 CTAs unsplit: the planner
+    splits k, which needs workspace."""
+    _, w = _weight(dqd, dev, 4096, 14336, seed=1)
+    assert dqd.dq_gemm_workspace_bytes(w, 384) > 0
