@@ -150,11 +150,6 @@ __device__ __forceinline__ void issue_x(uint32_t slot, const Args& a, int64_t m0
   }
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
-  uint32_t r;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(saddr));
-  return r;
-}
 __device__ __forceinline__ uint32_t lds8(uint32_t saddr) {
   uint16_t r;
   asm volatile("ld.shared.u8 %0, [%1];" : "=h"(r) : "r"(saddr));

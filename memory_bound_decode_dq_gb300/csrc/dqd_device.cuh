@@ -40,6 +40,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(saddr));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
