@@ -390,7 +390,9 @@ __global__ void __launch_bounds__(Cfg<WT, MT>::THREADS) dq_gemm_kernel(const Arg
 // (the packed codes and scales of a tile are contiguous per stage, and so is
 // each activation row), completing on a per-slot mbarrier. Consumers release
 // a slot through a second mbarrier; nobody touches copy addressing except the
-// producer. Zero points are read with ordinary loads one stage ahead.
+// producer. Zero points travel with the stage when their 8-byte blocks form
+// 16-byte-aligned runs (an even number of groups in k and per stage);
+// otherwise they are read with ordinary loads one stage ahead.
 template <int MT>
 struct Int4Cfg {
   static constexpr int WARPS = MT <= 2 ? 8 : 4;
@@ -401,6 +403,8 @@ struct Int4Cfg {
   static constexpr int NS = 3;                               // ring slots
   static constexpr int CODES = WARPS * NG * 1024;
   static constexpr int SCALES = WARPS * NG * 32;
+  static constexpr int ZEROS = WARPS * NG * 8;               // staged when their copies align
+  static constexpr int META = SCALES + ZEROS;
   static constexpr int XSTR = KC * 2 + 64;                    // padded activation row
 };
 
@@ -423,6 +427,9 @@ __global__ void __launch_bounds__(Int4Cfg<MT>::THREADS) dq_gemm_int4_kernel(cons
   const int nst = kend > kbeg ? (int)((kend - kbeg + C::KC - 1) / C::KC) : 0;
   const int rows_valid = (int)min((int64_t)a.ra, a.m - m0);
   const int64_t G = a.k / 128;
+  // Zero-point blocks of a tile's stage groups form a 16-byte-aligned run
+  // when G and the groups per stage are even (stages start at even groups).
+  const bool zbulk = (G % 2 == 0) && (C::NG % 2 == 0);
   const uint32_t ring = smem_addr(smem);
   const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[NS]);
 
@@ -446,7 +453,7 @@ __global__ void __launch_bounds__(Int4Cfg<MT>::THREADS) dq_gemm_int4_kernel(cons
     auto stage_bytes = [&](int s) {
       const int ng = stage_groups(s);
       int nt = (int)min((int64_t)C::WARPS, ntiles - tile0);
-      return (uint32_t)(nt * ng * (1024 + 32) + rows_valid * ng * 256);
+      return (uint32_t)(nt * ng * (1024 + 32 + (zbulk ? 8 : 0)) + rows_valid * ng * 256);
     };
     // lane w < WARPS copies tile w's codes and scales; lanes >= 16 copy activation rows
     auto issue_w = [&](int s) {
@@ -459,6 +466,7 @@ __global__ void __launch_bounds__(Int4Cfg<MT>::THREADS) dq_gemm_int4_kernel(cons
         const int64_t blk = (tile0 + lane) * G + g0;
         bulk_load(slot + lane * C::NG * 1024, a.w + blk * 1024, ng * 1024, fb);
         bulk_load(slot + C::CODES + lane * C::NG * 32, a.ws + blk * 32, ng * 32, fb);
+        if (zbulk) bulk_load(slot + C::CODES + C::SCALES + lane * C::NG * 8, a.wz + blk * 8, ng * 8, fb);
       }
     };
     auto issue_x = [&](int s) {
@@ -466,7 +474,7 @@ __global__ void __launch_bounds__(Int4Cfg<MT>::THREADS) dq_gemm_int4_kernel(cons
       const int ng = stage_groups(s);
       const int64_t kst = kbeg + (int64_t)s * C::KC;
       for (int r = lane; r < rows_valid; r += 32)
-        bulk_load(slot + C::CODES + C::SCALES + r * C::XSTR, a.x + (m0 + r) * a.k + kst, ng * 256, fb);
+        bulk_load(slot + C::CODES + C::META + r * C::XSTR, a.x + (m0 + r) * a.k + kst, ng * 256, fb);
     };
     const int pre = min(NS, nst);
     for (int s = 0; s < pre; ++s) issue_w(s);  // weights are constant: fetch ahead
@@ -493,7 +501,7 @@ __global__ void __launch_bounds__(Int4Cfg<MT>::THREADS) dq_gemm_int4_kernel(cons
       for (int j = 0; j < C::NG; ++j)
         z[j] = (tile_ok && g0 + j < gend) ? ldg_u8(a.wz + (tile * G + g0 + j) * 8 + g) : 0u;
     };
-    if (nst > 0) load_zeros(0, znext);
+    if (nst > 0 && !zbulk) load_zeros(0, znext);
     const uint4 zero = make_uint4(0, 0, 0, 0);
     for (int s = 0; s < nst; ++s) {
       const int slot_i = s % NS;
@@ -505,11 +513,12 @@ __global__ void __launch_bounds__(Int4Cfg<MT>::THREADS) dq_gemm_int4_kernel(cons
       uint32_t zcur[C::NG];
 #pragma unroll
       for (int j = 0; j < C::NG; ++j) zcur[j] = znext[j];
-      if (s + 1 < nst) load_zeros(s + 1, znext);
+      if (s + 1 < nst && !zbulk) load_zeros(s + 1, znext);
       const uint32_t slot = ring + slot_i * a.slot;
       const uint32_t wb = slot + warp * C::NG * 1024;
       const uint32_t sb = slot + C::CODES + warp * C::NG * 32;
-      const uint32_t xb = slot + C::CODES + C::SCALES;
+      const uint32_t xb = slot + C::CODES + C::META;
+      const uint32_t zb = slot + C::CODES + C::SCALES + warp * C::NG * 8;
       const int64_t kst = kbeg + (int64_t)s * C::KC;
       const int ngroups = (int)((kend - kst) / 128);
       if (tile_ok) {
@@ -517,7 +526,8 @@ __global__ void __launch_bounds__(Int4Cfg<MT>::THREADS) dq_gemm_int4_kernel(cons
         for (int jg = 0; jg < C::NG; ++jg) {
           if (jg >= ngroups) break;
           const uint32_t sc = lds32(sb + jg * 32 + g * 4);
-          const uint32_t zlo = int4_zero_pair(zcur[jg]), zhi = int4_zero_pair(zcur[jg] >> 4);
+          const uint32_t zz = zbulk ? lds8(zb + jg * 8 + g) : zcur[jg];
+          const uint32_t zlo = int4_zero_pair(zz), zhi = int4_zero_pair(zz >> 4);
           const uint4 q0 = lds128(wb + jg * 1024 + lane * 16);
           const uint4 q1 = lds128(wb + jg * 1024 + 512 + lane * 16);
           float ga[MT][4];
@@ -569,7 +579,7 @@ template <int WT, int MT>
 KernelInfo info_t() {
   if constexpr (WT == kINT4) {
     using C = Int4Cfg<MT>;
-    return {C::WARPS, C::KC, C::CODES, C::SCALES, C::XSTR, C::ROWS, C::NS};
+    return {C::WARPS, C::KC, C::CODES, C::META, C::XSTR, C::ROWS, C::NS};
   } else {
     using C = Cfg<WT, MT>;
     return {C::WARPS, C::KC, C::WSTAGE, C::MSTAGE, C::XROWB, C::ROWS, kStages};
