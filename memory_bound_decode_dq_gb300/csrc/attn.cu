@@ -560,8 +560,12 @@ AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms) 
   const int64_t slots = (int64_t)std::max(num_sms, 1) * cps;
   // About four waves of CTAs so that waves balance; each key-slot group gets
   // at least four blocks, and a chunk's partial (o, m, l) per query row stays
-  // small next to the chunk's K/V bytes (cb >= 1.3 * rows).
-  const int cb_min = std::max(4 * ks, (13 * qr + 9) / 10);
+  // small next to the chunk's K/V bytes (cb >= 1.3 * rows), unless that would
+  // leave SMs idle: a small problem (few sequences and heads) is latency
+  // bound, so its chunks shrink until the CTAs fill one wave.
+  const int64_t per_item = std::max<int64_t>(1, (slots + items - 1) / items);
+  const int cb_wave = std::max<int>(ks, (int)((maxblk + per_item - 1) / per_item));
+  const int cb_min = std::max(4 * ks, std::min((13 * qr + 9) / 10, cb_wave));
   int64_t nch = std::max<int64_t>(1, (4 * slots + items - 1) / items);
   int cb = std::max<int>((int)((maxblk + nch - 1) / nch), cb_min);
   // Test hook: DQD_ATTN_CHUNK_BLOCKS forces the split-KV chunk size.
