@@ -652,7 +652,7 @@ cudaError_t launch_wt(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
 GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
   // Test hook: DQD_GEMM_TC=0 keeps wide-m shapes on the warp-MMA kernels.
   const char* tc_env = std::getenv("DQD_GEMM_TC");
-  if (tc_supported(wtype, m, n, k) && !(tc_env && tc_env[0] == '0')) return plan_dq_gemm_tc(m, n, k, num_sms);
+  if (tc_supported(wtype, m, n, k) && !(tc_env && tc_env[0] == '0')) return plan_dq_gemm_tc(wtype, m, n, k, num_sms);
   GemmPlan p{};
   p.mt = m <= 8 ? 1 : (m <= 16 ? 2 : (m <= 32 ? 4 : 8));
   const KernelInfo ki = info_of(wtype, p.mt);

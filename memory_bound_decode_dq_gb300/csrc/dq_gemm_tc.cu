@@ -1,26 +1,31 @@
-// dq_gemm for wide m (verify batches): INT4 g128 on the 5th-generation tensor
-// cores (tcgen05), where the tile is a dense contraction.
+// dq_gemm for wide m on the 5th-generation tensor cores (tcgen05), where the
+// tile is a dense contraction: INT4 g128 at verify widths, BF16 and FP8-E4M3
+// from m = 32 up.
 //
 // Source: "降低每個 Token 的生成成本" (Making each token cheaper), section
 // "推測式解碼" (speculative decoding): verifying gamma + 1 positions per
 // sequence multiplies the rows of the weight-only GEMM, and with INT4 weights
 // the verify step turns compute-bound; sections "格式" (Formats) and "量化省下
-// 什麼": weight-only INT4 dequantises to 16-bit before the matrix arithmetic.
+// 什麼": weight-only INT4 and FP8 dequantise to 16-bit before the matrix
+// arithmetic, FP8 with one fp32 scale per output channel.
 //
 // One CTA computes D[128 weight rows][N tokens] (N <= 256, a multiple of 16)
 // over its k range (all of k, or one split of it), in 64-wide k slabs:
-//  * warp 0 streams the packed INT4 codes of the CTA's eight 16-row tiles
-//    (half of each 1 KB group block) and their group scales with TMA into a
-//    six-deep ring; these are constants, requested before the wait on the
-//    preceding kernel;
+//  * warp 0 streams the weights with TMA. BF16: the 128 x 64 tile straight
+//    into a 128-byte-swizzled K-major A slot. INT4: the packed codes of the
+//    CTA's eight 16-row tiles (half of each 1 KB group block) and their group
+//    scales into a ring of code slots. FP8: 128 x 128 code tiles (two slabs,
+//    whole 128-byte rows) into a ring of code slots. Weights are constants: they are requested before the
+//    wait on the preceding kernel;
 //  * warp 1 streams the activation slab x[N tokens][64 k] with TMA as one
-//    128-byte-swizzled box (rows past the ends arrive as zeros) into a
-//    128 KB ring (4 to 16 slabs deep, by N), so that activation reads run
-//    well ahead of the MMAs;
-//  * warps 2-9 (one 16-row tile each) dequantise each slab's codes to bf16
+//    128-byte-swizzled box (rows past the ends arrive as zeros) into a ring of
+//    about 128 KB (4 to 16 slabs deep, by N);
+//  * warps 2-9 dequantise each code slab into the A slot, in two groups of
+//    four taking alternate slabs: INT4 two 16-row tiles per warp,
 //    deq = RN((q - z) * s) (the exact bf16 subtraction, then one rounded bf16
-//    multiply; zero points prefetched a group ahead into registers) into a
-//    four-deep ring of K-major 128-byte-swizzled A tiles;
+//    multiply; zero points prefetched a group ahead); FP8 eight codes per
+//    16-byte row chunk, converted exactly to bf16 (the scale is applied to
+//    the fp32 result);
 //  * one thread of warp 10 issues tcgen05.mma (M 128, N, K 16, bf16 in, fp32
 //    accumulate in tensor memory) once both operands of a slab are in place,
 //    and commits the slab's MMAs to the "empty" mbarriers of both slots;
@@ -45,22 +50,55 @@ __device__ unsigned int g_tc_error;
 constexpr int kRows = 128;    // weight rows per CTA (MMA M)
 constexpr int kMaxN = 256;    // tokens per CTA at most (MMA N)
 constexpr int kSlabK = 64;    // k per slab: one 128-byte swizzle row of bf16
-constexpr int kASlots = 4;    // dequantised weight tiles (A)
-constexpr int kBRing = 128 * 1024;            // activation slabs (B): N x 128 bytes each
-constexpr int kMaxBSlots = 16;
-constexpr int kCSlots = 6;    // code slots
 constexpr int kABytes = kRows * kSlabK * 2;   // 16 KB
-constexpr int kCodeBytes = 8 * 512;           // 8 tiles x half a group block
-constexpr int kScaleBytes = 8 * 32;           // group scales of the 8 tiles
-constexpr int kCSlot = kCodeBytes + kScaleBytes;
+constexpr int kMaxASlots = 12;
+constexpr int kMaxBSlots = 16;
+constexpr int kMaxCSlots = 12;
+constexpr int kI4Codes = 8 * 512;             // INT4: 8 tiles x half a group block
+constexpr int kI4Scales = 8 * 32;             // INT4: group scales of the 8 tiles
 constexpr int kDeqWarps = 8;
 constexpr int kDeq0 = 2;                      // first dequantising warp
 constexpr int kMmaWarp = kDeq0 + kDeqWarps;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
-constexpr int kSmem = kASlots * kABytes + kBRing + kCSlots * kCSlot + 1024;  // + alignment slack
-static_assert(kABytes % 1024 == 0 && kCSlot % 128 == 0, "slot alignment");
-static_assert(kBRing >= 4 * kMaxN * kSlabK * 2, "at least four activation slabs");
+constexpr int kRingBytes = 222 * 1024;        // all rings
+constexpr int kSmem = kRingBytes + 1024;      // + alignment slack
 static_assert(kSmem + 1024 <= 227 * 1024, "shared memory");
+
+// Code slot bytes per weight type (INT4: codes + scales of one 64-k slab;
+// FP8: a 128 x 128 code tile, two slabs, so that every row is one full
+// 128-byte line; BF16 has none: its weight tiles land straight in the A slots).
+__host__ __device__ constexpr int code_slot(int wt) {
+  return wt == kINT4 ? kI4Codes + kI4Scales : (wt == kFP8 ? kRows * 2 * kSlabK : 0);
+}
+
+// Ring depths for N tokens per CTA: the activation ring gets about 32 KB
+// (3 to 16 slabs: activations come from L2); BF16 weight tiles take the rest
+// (they stream from HBM, so they need the depth). Dequantised weights get up
+// to eight A slots (the dequantise -> MMA -> release round trip spans the A
+// ring), keeping room for a few code slots, and the code ring the rest.
+struct Rings {
+  int nas, nbs, ncs;
+};
+__host__ __device__ inline Rings rings(int wt, int ntok) {
+  const int bslot = ntok * kSlabK * 2;
+  Rings r;
+  r.nbs = min(kMaxBSlots, max(3, (32 * 1024) / bslot));
+  const int rest = kRingBytes - r.nbs * bslot;
+  if (wt == kBF16) {
+    r.nas = min(kMaxASlots, rest / kABytes);
+    r.ncs = 0;
+  } else {
+    // INT4: even slot counts, so that slab i's slots (i % n) always serve the
+    // same one of the two dequantising groups (which take alternate slabs)
+    // and every waiter sees each phase of its slots' barriers. FP8 code
+    // slots hold a slab pair, one slab for each group.
+    const int min_codes = wt == kINT4 ? 8 : 3;  // at least ~32-48 KB of weights in flight
+    r.nas = max(4, min(8, (rest - min_codes * code_slot(wt)) / kABytes)) & ~1;
+    r.ncs = min(kMaxCSlots, (rest - r.nas * kABytes) / code_slot(wt));
+    if (wt == kINT4) r.ncs &= ~1;
+  }
+  return r;
+}
 
 // tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row
 // groups 1024 bytes apart.
@@ -137,14 +175,15 @@ __device__ __forceinline__ void deq_barrier() {
 }
 
 struct TcArgs {
-  const uint8_t* wz;  // packed zeros
+  const uint8_t* wz;     // INT4 packed zeros
+  const float* wscale;   // FP8 per-row scales
   uint16_t* y;
-  unsigned* counters; // split-K tickets (splits > 1)
-  float* part;        // split-K fp32 partials [split][m][n]
+  unsigned* counters;    // split-K tickets (splits > 1)
+  float* part;           // split-K fp32 partials [split][m][n]
   int64_t m, n, k;
-  int ntok;           // N: tokens per CTA
+  int ntok;              // N: tokens per CTA
   int splits;
-  int slabs_per_split;  // even: splits fall on group boundaries
+  int slabs_per_split;   // INT4 and FP8: even (splits fall on groups / code slots)
 };
 
 __device__ __forceinline__ float4 ldcg4(const float* p) {
@@ -193,6 +232,15 @@ __device__ __forceinline__ void reduce_splits(const TcArgs& a, int64_t r0, int r
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q)
+        if (live[q] && a.wscale) {
+          const float4 sc = *reinterpret_cast<const float4*>(a.wscale + r0 + 4 * ((u0 + q * nthreads) % per_tok));
+          acc[q].x *= sc.x;
+          acc[q].y *= sc.y;
+          acc[q].z *= sc.z;
+          acc[q].w *= sc.w;
+        }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
         if (live[q]) {
           uint2 o;
           o.x = pack_bf16x2(acc[q].x, acc[q].y);
@@ -206,47 +254,52 @@ __device__ __forceinline__ void reduce_splits(const TcArgs& a, int64_t r0, int r
       const int64_t off = (m0 + u / rows) * a.n + r0 + u % rows;
       float acc = 0.f;
       for (int sp = 0; sp < a.splits; ++sp) acc += __ldcg(part + sp * plane + off);
-      a.y[off] = f32_to_bf16(acc);
+      a.y[off] = f32_to_bf16(a.wscale ? acc * a.wscale[r0 + u % rows] : acc);
     }
   }
 }
 
+template <int WT>
 __global__ void __launch_bounds__(kThreads, 1)
-    dq_gemm_int4_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
-                           const __grid_constant__ CUtensorMap tms, const TcArgs a) {
+    dq_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+                      const __grid_constant__ CUtensorMap tms, const TcArgs a) {
+  constexpr int CSLOT = code_slot(WT);
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * kCSlots + 2 * kASlots + 2 * kMaxBSlots + 1];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxCSlots + 2 * kMaxASlots + 2 * kMaxBSlots + 1];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int last_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t aring = (smem_addr(smem_raw) + 1023u) & ~1023u;
-  const uint32_t bring = aring + kASlots * kABytes;
-  const uint32_t cring = bring + kBRing;
-  const uint32_t cfull = smem_addr(&bars[0]), cempty = cfull + 8 * kCSlots;
-  const uint32_t afull = cempty + 8 * kCSlots, aempty = afull + 8 * kASlots;
-  const uint32_t bfull = aempty + 8 * kASlots, bempty = bfull + 8 * kMaxBSlots;
-  const uint32_t done = bempty + 8 * kMaxBSlots;
+  const Rings R = rings(WT, a.ntok);
   const uint32_t bslot_bytes = (uint32_t)a.ntok * kSlabK * 2;
-  const int nbs = min(kMaxBSlots, (int)(kBRing / bslot_bytes));  // activation slots
-  // blockIdx.x walks the token chunks fastest, so the CTAs that dequantise
-  // the same weight tile run together and share it through L2.
+  const int nbs = R.nbs, nas = R.nas, ncs = R.ncs;
+  const uint32_t aring = (smem_addr(smem_raw) + 1023u) & ~1023u;
+  const uint32_t bring = aring + nas * kABytes;
+  const uint32_t cring = bring + nbs * bslot_bytes;
+  const uint32_t cfull = smem_addr(&bars[0]), cempty = cfull + 8 * kMaxCSlots;
+  const uint32_t afull = cempty + 8 * kMaxCSlots, aempty = afull + 8 * kMaxASlots;
+  const uint32_t bfull = aempty + 8 * kMaxASlots, bempty = bfull + 8 * kMaxBSlots;
+  const uint32_t done = bempty + 8 * kMaxBSlots;
+  // blockIdx.x walks the token chunks fastest, so the CTAs that use the same
+  // weight tile run together and share it through L2.
   const int64_t tile0 = (int64_t)blockIdx.y * 8;  // first 16-row tile
+  const int64_t row0 = tile0 * 16;
   const int64_t ntiles = (a.n + 15) / 16;
   const int64_t m0 = (int64_t)blockIdx.x * a.ntok;
-  const int G = (int)(a.k / 128);
+  const int nslabs = (int)((a.k + kSlabK - 1) / kSlabK);
   const int jb = (int)blockIdx.z * a.slabs_per_split;
-  const int nl = min(2 * G - jb, a.slabs_per_split);  // slabs of this CTA (even, >= 2)
+  const int nl = min(nslabs - jb, a.slabs_per_split);  // slabs of this CTA (>= 1)
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kCSlots; ++i) {
+    for (int i = 0; i < ncs; ++i) {
       mbar_init(cfull + 8 * i, 1);
-      mbar_init(cempty + 8 * i, kDeqWarps * 32);
+      // INT4: one group of four warps per slot; FP8: both groups
+      mbar_init(cempty + 8 * i, WT == kFP8 ? kDeqWarps * 32 : kDeqWarps * 16);
     }
-    for (int i = 0; i < kASlots; ++i) {
-      mbar_init(afull + 8 * i, kDeqWarps * 32);
+    for (int i = 0; i < nas; ++i) {
+      mbar_init(afull + 8 * i, WT == kBF16 ? 1 : kDeqWarps * 16);
       mbar_init(aempty + 8 * i, 1);
     }
-    for (int i = 0; i < kMaxBSlots; ++i) {
+    for (int i = 0; i < nbs; ++i) {
       mbar_init(bfull + 8 * i, 1);
       mbar_init(bempty + 8 * i, 1);
     }
@@ -263,22 +316,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Slot cursors: slot index and the parity of its current use; a slot's
   // "empty" barrier is waited on with the opposite parity (its previous use).
   if (warp == 0) {
-    // ---------------- codes + scales (constants) ----------------
+    // ---------------- weights (constants) ----------------
     if (lane == 0) {
       allow_dependent_launch();
       int cs = 0;
       uint32_t ph = 0;
-      for (int i = 0; i < nl; ++i) {
+      const int NSL = WT == kBF16 ? nas : ncs;
+      const uint32_t empty = WT == kBF16 ? aempty : cempty, full = WT == kBF16 ? afull : cfull;
+      const int step = WT == kFP8 ? 2 : 1;  // slabs per weight slot
+      for (int i = 0, slot_i = 0; i < nl; i += step, ++slot_i) {
         const int j = jb + i;
-        if (i >= kCSlots && !mbar_wait(cempty + 8 * cs, ph ^ 1u)) {
+        if (slot_i >= NSL && !mbar_wait(empty + 8 * cs, ph ^ 1u)) {
           atomicOr(&g_tc_error, kErrWaitTimeout);
           break;
         }
-        const uint32_t dst = cring + cs * kCSlot, fb = cfull + 8 * cs;
-        mbar_arrive_expect_tx(fb, kCSlot);
-        tma_load_2d(dst, &tmw, fb, j * 128, (int)tile0);
-        tma_load_2d(dst + kCodeBytes, &tms, fb, (j >> 1) * 8, (int)tile0);
-        if (++cs == kCSlots) {
+        const uint32_t fb = full + 8 * cs;
+        if constexpr (WT == kBF16) {
+          mbar_arrive_expect_tx(fb, kABytes);
+          tma_load_2d(aring + cs * kABytes, &tmw, fb, j * kSlabK, (int)row0);
+        } else if constexpr (WT == kFP8) {
+          mbar_arrive_expect_tx(fb, CSLOT);  // slabs j, j + 1 (j even)
+          tma_load_2d(cring + cs * CSLOT, &tmw, fb, j * kSlabK, (int)row0);
+        } else {
+          const uint32_t dst = cring + cs * CSLOT;
+          mbar_arrive_expect_tx(fb, CSLOT);
+          tma_load_2d(dst, &tmw, fb, j * 128, (int)tile0);
+          tma_load_2d(dst + kI4Codes, &tms, fb, (j >> 1) * 8, (int)tile0);
+        }
+        if (++cs == NSL) {
           cs = 0;
           ph ^= 1u;
         }
@@ -305,75 +370,162 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < kMmaWarp) {
-    // ---------------- dequantisers: warp w owns 16-row tile w - 2 ----------------
-    const int tt = warp - kDeq0, g = lane >> 2, t = lane & 3;
     grid_dependency_wait();
     allow_dependent_launch();
-    const int64_t tile = tile0 + tt;
-    const uint8_t* zp = a.wz + tile * G * 8 + g;  // zero byte of group gr at zp[8 gr]
-    const bool live = tile < ntiles;
-    int gr = jb >> 1;
-    uint32_t znext = live ? ldg_u8(zp + 8 * gr) : 0u;
-    // Lanes of odd g store their two 32-k halves in the opposite order, so
-    // that each quarter-warp's 16-byte stores cover all 32 banks once.
-    const uint32_t godd = g & 1;
-    const uint32_t row_lo = 2 * tt * 1024 + g * 128;  // row 16 tt + g; row + 8 is 1024 bytes on
-    const uint32_t o0 = row_lo + (((4 * godd + t) ^ g) << 4);
-    const uint32_t o1 = row_lo + (((4 * (godd ^ 1u) + t) ^ g) << 4);
-    const uint32_t csrc0 = cring + tt * 512 + lane * 16, ssrc0 = cring + kCodeBytes + tt * 32 + g * 4;
-    int cs = 0, s = 0;
+    // Two groups of four warps take alternate slabs (group 0 the even ones),
+    // so that two slabs are dequantised at once and each warp has twice the
+    // independent work between its barrier round trips. Slot cursors advance
+    // by two slabs per iteration.
+    const int grp = (warp - kDeq0) >> 2, gw = (warp - kDeq0) & 3;
+    int cs = grp, s = grp;
     uint32_t cph = 0, sph = 0;
-    uint32_t zlo = 0, zhi = 0;
-    for (int i = 0; i < nl; ++i) {
-      if ((i & 1) == 0) {  // a new group: take its zero points, prefetch the next group's
-        zlo = int4_zero_pair(znext);
-        zhi = int4_zero_pair(znext >> 4);
-        ++gr;
-        znext = (live && gr < G) ? ldg_u8(zp + 8 * gr) : 0u;
-      }
-      if (!mbar_wait(cfull + 8 * cs, cph)) {
-        ok = false;
-        break;
-      }
-      uint4 u = lds128(csrc0 + cs * kCSlot);
-      const uint32_t sc = lds32(ssrc0 + cs * kCSlot);
-      if (i >= kASlots && !mbar_wait(aempty + 8 * s, sph ^ 1u)) {
-        ok = false;
-        break;
-      }
-      if (godd) {
-        const uint32_t x0 = u.x, x1 = u.y;
-        u.x = u.z;
-        u.y = u.w;
-        u.z = x0;
-        u.w = x1;
-      }
-      const uint32_t slo = prmt(sc, 0u, 0x1010u), shi = prmt(sc, 0u, 0x3232u);
-      const uint32_t base = aring + s * kABytes;
-      // words 2c, 2c+1 (after the swap) hold k = 32c' + 8t .. +7 of rows g
-      // and g + 8, with c' = c ^ godd
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const Int4Frag f0 = int4_unpack(word(u, 2 * c), zlo, zhi);
-        const Int4Frag f1 = int4_unpack(word(u, 2 * c + 1), zlo, zhi);
-        const uint32_t a_lo = base + (c == 0 ? o0 : o1);
-        sts128(a_lo, bf16x2_mul(f0.a0, slo), bf16x2_mul(f0.a2, slo), bf16x2_mul(f1.a0, slo),
-               bf16x2_mul(f1.a2, slo));
-        sts128(a_lo + 1024, bf16x2_mul(f0.a1, shi), bf16x2_mul(f0.a3, shi), bf16x2_mul(f1.a1, shi),
-               bf16x2_mul(f1.a3, shi));
-      }
-      fence_proxy_async_smem();  // make the generic-proxy stores visible to the tensor core
-      mbar_arrive(afull + 8 * s);
-      // Release the code slot only now: an arrive does not wait for shared
-      // loads still in flight, so it must follow the use of their values.
-      mbar_arrive(cempty + 8 * cs);
-      if (++cs == kCSlots) {
-        cs = 0;
+    auto advance = [&]() {
+      if ((cs += 2) >= ncs) {
+        cs -= ncs;
         cph ^= 1u;
       }
-      if (++s == kASlots) {
-        s = 0;
+      if ((s += 2) >= nas) {
+        s -= nas;
         sph ^= 1u;
+      }
+    };
+    if constexpr (WT == kINT4) {
+      // ---------------- INT4: warp gw of a group owns 16-row tiles 2 gw, 2 gw + 1 ----------------
+      // Group 0 dequantises the first 64-k half of every 128-k group, group 1
+      // the second, so each iteration starts a new group: zero points are
+      // fetched one iteration ahead.
+      const int g = lane >> 2, t = lane & 3;
+      const int G = (int)(a.k / 128);
+      const uint8_t* zp[2];
+      bool live[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int64_t tile = tile0 + 2 * gw + q;
+        live[q] = tile < ntiles;
+        zp[q] = a.wz + tile * G * 8 + g;  // zero byte of group gr at zp[q][8 gr]
+      }
+      int gr = (jb + grp) >> 1;
+      uint32_t znext[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) znext[q] = (live[q] && gr < G) ? ldg_u8(zp[q] + 8 * gr) : 0u;
+      // Lanes of odd g store their two 32-k halves in the opposite order, so
+      // that each quarter-warp's 16-byte stores cover all 32 banks once.
+      const uint32_t godd = g & 1;
+      for (int i = grp; i < nl; i += 2) {
+        uint32_t zcur[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          zcur[q] = znext[q];
+          znext[q] = (live[q] && gr + 1 < G) ? ldg_u8(zp[q] + 8 * (gr + 1)) : 0u;
+        }
+        ++gr;
+        if (!mbar_wait(cfull + 8 * cs, cph)) {
+          ok = false;
+          break;
+        }
+        uint4 u[2];
+        uint32_t sc[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int tt = 2 * gw + q;
+          u[q] = lds128(cring + cs * CSLOT + tt * 512 + lane * 16);
+          sc[q] = lds32(cring + cs * CSLOT + kI4Codes + tt * 32 + g * 4);
+        }
+        if (i >= nas && !mbar_wait(aempty + 8 * s, sph ^ 1u)) {
+          ok = false;
+          break;
+        }
+        const uint32_t base = aring + s * kABytes;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int tt = 2 * gw + q;
+          uint4 w = u[q];
+          if (godd) {
+            const uint32_t x0 = w.x, x1 = w.y;
+            w.x = w.z;
+            w.y = w.w;
+            w.z = x0;
+            w.w = x1;
+          }
+          const uint32_t slo = prmt(sc[q], 0u, 0x1010u), shi = prmt(sc[q], 0u, 0x3232u);
+          const uint32_t zlo = int4_zero_pair(zcur[q]), zhi = int4_zero_pair(zcur[q] >> 4);
+          const uint32_t row_lo = 2 * tt * 1024 + g * 128;  // row 16 tt + g; row + 8 is 1024 bytes on
+          // words 2c, 2c+1 (after the swap) hold k = 32c' + 8t .. +7 of rows g
+          // and g + 8, with c' = c ^ godd
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const Int4Frag f0 = int4_unpack(word(w, 2 * c), zlo, zhi);
+            const Int4Frag f1 = int4_unpack(word(w, 2 * c + 1), zlo, zhi);
+            const uint32_t a_lo = base + row_lo + (((4 * ((uint32_t)c ^ godd) + t) ^ g) << 4);
+            sts128(a_lo, bf16x2_mul(f0.a0, slo), bf16x2_mul(f0.a2, slo), bf16x2_mul(f1.a0, slo),
+                   bf16x2_mul(f1.a2, slo));
+            sts128(a_lo + 1024, bf16x2_mul(f0.a1, shi), bf16x2_mul(f0.a3, shi), bf16x2_mul(f1.a1, shi),
+                   bf16x2_mul(f1.a3, shi));
+          }
+        }
+        fence_proxy_async_smem();  // make the generic-proxy stores visible to the tensor core
+        mbar_arrive(afull + 8 * s);
+        // Release the code slot only now: an arrive does not wait for shared
+        // loads still in flight, so it must follow the use of their values.
+        mbar_arrive(cempty + 8 * cs);
+        advance();
+      }
+    } else if constexpr (WT == kFP8) {
+      // ---------------- FP8 ----------------
+      // A code slot holds rows of 128 codes (slabs 2c, 2c + 1, 128-byte
+      // swizzled); group h converts the h-th 64-code half of each row. Pass p:
+      // thread d takes row 32 p + 8 (d >> 5) + 4 ((d >> 2) & 1) + ((d >> 3) & 3),
+      // 16-code chunk d & 3: a quarter-warp reads rows r and r + 4, whose
+      // swizzled chunks are disjoint, and the lanes of row r + 4 store their
+      // odd 8-code chunk first, so loads and stores are free of conflicts.
+      const int d = gw * 32 + lane, c4 = d & 3, rsel = (d >> 2) & 1;
+      const int rbase = 8 * (d >> 5) + 4 * rsel + ((d >> 3) & 3);
+      int ks = 0;
+      uint32_t kph = 0;  // code slot cursor: one slot per slab pair
+      for (int i = grp; i < nl; i += 2) {
+        if (!mbar_wait(cfull + 8 * ks, kph)) {
+          ok = false;
+          break;
+        }
+        uint4 cw[4];
+#pragma unroll
+        for (int pass = 0; pass < 4; ++pass) {
+          const int r = 32 * pass + rbase;
+          cw[pass] = lds128(cring + ks * CSLOT + r * 128 + (((4 * grp + c4) ^ (r & 7)) << 4));
+        }
+        if (i >= nas && !mbar_wait(aempty + 8 * s, sph ^ 1u)) {
+          ok = false;
+          break;
+        }
+        const uint32_t base = aring + s * kABytes;
+#pragma unroll
+        for (int pass = 0; pass < 4; ++pass) {
+          const int r = 32 * pass + rbase;
+          const uint32_t rowb = base + (r >> 3) * 1024 + (r & 7) * 128;
+          const uint32_t e0 = rowb + (((2 * c4) ^ (r & 7)) << 4), e1 = rowb + (((2 * c4 + 1) ^ (r & 7)) << 4);
+          const uint32_t lo0 = fp8_lo_to_bf16x2(cw[pass].x), lo1 = fp8_hi_to_bf16x2(cw[pass].x);
+          const uint32_t lo2 = fp8_lo_to_bf16x2(cw[pass].y), lo3 = fp8_hi_to_bf16x2(cw[pass].y);
+          const uint32_t hi0 = fp8_lo_to_bf16x2(cw[pass].z), hi1 = fp8_hi_to_bf16x2(cw[pass].z);
+          const uint32_t hi2 = fp8_lo_to_bf16x2(cw[pass].w), hi3 = fp8_hi_to_bf16x2(cw[pass].w);
+          if (rsel) {
+            sts128(e1, hi0, hi1, hi2, hi3);
+            sts128(e0, lo0, lo1, lo2, lo3);
+          } else {
+            sts128(e0, lo0, lo1, lo2, lo3);
+            sts128(e1, hi0, hi1, hi2, hi3);
+          }
+        }
+        fence_proxy_async_smem();  // make the generic-proxy stores visible to the tensor core
+        mbar_arrive(afull + 8 * s);
+        mbar_arrive(cempty + 8 * ks);  // after the loaded codes were used
+        if (++ks == ncs) {
+          ks = 0;
+          kph ^= 1u;
+        }
+        if ((s += 2) >= nas) {
+          s -= nas;
+          sph ^= 1u;
+        }
       }
     }
     if (!ok && lane == 0) atomicOr(&g_tc_error, kErrWaitTimeout);
@@ -397,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // both slots are free once these MMAs have read them
         umma_commit(aempty + 8 * sa);
         umma_commit(bempty + 8 * sb);
-        if (++sa == kASlots) {
+        if (++sa == nas) {
           sa = 0;
           pa ^= 1u;
         }
@@ -418,9 +570,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!good && lane == 0) atomicOr(&g_tc_error, kErrWaitTimeout);
     __syncwarp();  // tcgen05.ld is warp-collective
     tc_fence_after();
-    const int64_t row = tile0 * 16 + quarter * 32 + lane;  // weight row = output column
+    const int64_t row = row0 + quarter * 32 + lane;  // weight row = output column
     const int nchunks = (a.ntok + 31) / 32;
     float* part = a.splits > 1 ? a.part + (int64_t)blockIdx.z * a.m * a.n : nullptr;
+    const float rscale = (WT == kFP8 && row < a.n) ? a.wscale[row] : 1.f;
 #pragma unroll 1
     for (int cc = half; cc < nchunks; cc += 2) {
       uint32_t r[32];
@@ -433,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (part)
               part[mm * a.n + row] = __uint_as_float(r[j]);
             else
-              a.y[mm * a.n + row] = f32_to_bf16(__uint_as_float(r[j]));
+              a.y[mm * a.n + row] = f32_to_bf16(__uint_as_float(r[j]) * rscale);
           }
         }
       }
@@ -447,10 +600,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       deq_barrier();
       if (last_sh) {
         __threadfence();
-        const int64_t r0 = tile0 * 16;
-        const int rows = (int)min((int64_t)kRows, a.n - r0);
+        const int rows = (int)min((int64_t)kRows, a.n - row0);
         const int toks = (int)min((int64_t)a.ntok, a.m - m0);
-        reduce_splits(a, r0, rows, m0, toks, threadIdx.x - kDeq0 * 32, kDeqWarps * 32);
+        reduce_splits(a, row0, rows, m0, toks, threadIdx.x - kDeq0 * 32, kDeqWarps * 32);
         if (warp == kDeq0 && lane == 0) *cnt = 0u;  // leave the ticket at zero for the next call
       }
     }
@@ -463,14 +615,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int WT>
+void* tc_kernel() {
+  return reinterpret_cast<void*>(dq_gemm_tc_kernel<WT>);
+}
+
 }  // namespace
 
 bool tc_supported(int wtype, int64_t m, int64_t n, int64_t k) {
-  return wtype == kINT4 && m >= 128 && m <= (int64_t)INT32_MAX && k % 128 == 0 && k > 0 &&
-         k / 128 <= 65535 && n > 0 && (n + 127) / 128 <= 65535;
+  if (m > (int64_t)INT32_MAX || n <= 0 || (n + 127) / 128 > 65535 || k <= 0) return false;
+  switch (wtype) {
+    case kINT4: return m >= 128 && k % 128 == 0 && k / 128 <= 65535;
+    // FP8 at m = 32 stays on the warp-MMA kernel: on large matrices the
+    // tcgen05 kernel's FP8 dequantisation pipeline tops out near 2.5 TB/s.
+    case kFP8: return m >= 48 && k % 16 == 0;
+    case kBF16: return m >= 32 && k % 8 == 0;
+    default: return false;
+  }
 }
 
-GemmPlan plan_dq_gemm_tc(int64_t m, int64_t n, int64_t k, int num_sms) {
+GemmPlan plan_dq_gemm_tc(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
   GemmPlan p{};
   p.tc = 1;
   p.mt = 8;
@@ -478,28 +642,34 @@ GemmPlan plan_dq_gemm_tc(int64_t m, int64_t n, int64_t k, int num_sms) {
   p.slot_bytes = kABytes;
   p.smem_bytes = kSmem;
   p.grid_x = (int)((((n + 15) / 16) + 7) / 8);
-  // Choose tokens per CTA (N, a multiple of 16 in [64, 256] covering m in
+  // Choose tokens per CTA (N, a multiple of 16 in [16, 256] covering m in
   // equal chunks) and the k split from a cost model: CTAs run in waves of one
-  // per SM; a 64-wide slab costs the larger of its MMAs (2 N cycles at the
-  // dense bf16 rate) and the dequantisation (about 330 cycles of issue for
-  // 128 x 64 weights), plus a fixed 6 slabs of fill, drain and epilogue; a
-  // split adds its fp32 partial traffic at about 6 TB/s.
-  const int64_t G = k / 128, sms = std::max(num_sms, 1);
+  // per SM; a 64-wide slab costs its shared-memory traffic (weights in,
+  // dequantised tile out and back to the tensor core, activations in and
+  // back: about base + 2 N cycles) or, with every SM streaming, its share of
+  // HBM (weight bytes at about 21 bytes per SM cycle), whichever is larger;
+  // plus a fixed 6 slabs of fill, drain and epilogue; a split adds its fp32
+  // partial traffic at about 6 TB/s.
+  const int64_t nslabs = (k + kSlabK - 1) / kSlabK, sms = std::max(num_sms, 1);
+  const int unit = wtype == kBF16 ? 1 : 2;  // INT4 splits on groups, FP8 on code slots (slab pairs)
+  const int64_t units = (nslabs + unit - 1) / unit;
+  const double base = wtype == kINT4 ? 330.0 : (wtype == kFP8 ? 380.0 : 260.0);
+  const double wslab = wtype == kINT4 ? 4352.0 : (wtype == kFP8 ? 8192.0 : 16384.0);
   const char* env = std::getenv("DQD_GEMM_SPLITS");
   const long forced = env ? std::strtol(env, nullptr, 10) : 0;
   double best = -1.0;
   int64_t best_n = kMaxN, best_sp = 1;
-  for (int64_t cap = kMaxN; cap >= 64; cap -= 16) {
+  for (int64_t cap = kMaxN; cap >= 16; cap -= 16) {
     const int64_t chunks = (m + cap - 1) / cap;
     const int64_t ntok = ((m + chunks - 1) / chunks + 15) / 16 * 16;  // <= cap
-    const int64_t base = chunks * p.grid_x;
-    const double slab = std::max(2.0 * ntok, 330.0) + 20.0;
-    for (int64_t sp = 1; sp <= std::min<int64_t>(G, 32); ++sp) {
-      if (sp > 1 && (base * sp > (int64_t)(kCounterBytes / 4) || G / sp < 2)) break;
-      if (forced >= 1 && sp != std::min<int64_t>(forced, G)) continue;
-      const int64_t gps = (G + sp - 1) / sp;
-      const double waves = (double)((base * sp + sms - 1) / sms);
-      double cycles = waves * (2.0 * gps + 6.0) * slab;
+    const int64_t ctas = chunks * p.grid_x;
+    for (int64_t sp = 1; sp <= std::min<int64_t>(units, 32); ++sp) {
+      if (sp > 1 && (ctas * sp > (int64_t)(kCounterBytes / 4) || units / sp < 2)) break;
+      if (forced >= 1 && sp != std::min<int64_t>(forced, units)) continue;
+      const int64_t per = (units + sp - 1) / sp * unit;  // slabs per split
+      const double waves = (double)((ctas * sp + sms - 1) / sms);
+      const double slab = std::max(base + 2.0 * ntok, ctas * sp >= sms ? wslab / 21.0 : 0.0);
+      double cycles = waves * (per + 6.0) * slab;
       if (sp > 1) cycles += 8.0 * sp * m * n / 6e12 * 1.9e9;
       if (best < 0 || cycles < best * 0.97) {
         best = cycles;
@@ -510,16 +680,17 @@ GemmPlan plan_dq_gemm_tc(int64_t m, int64_t n, int64_t k, int num_sms) {
   }
   p.ra = (int)best_n;
   p.m_chunks = (int)((m + best_n - 1) / best_n);
-  const int64_t gps = (G + best_sp - 1) / best_sp;
-  p.splits = (int)((G + gps - 1) / gps);
-  p.k_per_split = gps * 128;
+  const int64_t per_units = (units + best_sp - 1) / best_sp;
+  p.splits = (int)((units + per_units - 1) / per_units);
+  p.k_per_split = per_units * unit * kSlabK;
   p.ws_bytes = p.splits > 1 ? kCounterBytes + sizeof(float) * (size_t)p.splits * m * n : 0;
   return p;
 }
 
 cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
-  const int64_t ntiles = (l.n + 15) / 16, G = l.k / 128;
+  const int64_t ntiles = (l.n + 15) / 16;
   CUtensorMap tmx, tmw, tms;
+  std::memset(&tms, 0, sizeof tms);
   {
     const uint64_t dims[2] = {(uint64_t)l.k, (uint64_t)l.m};
     const uint64_t strides[1] = {(uint64_t)l.k * 2};
@@ -528,32 +699,47 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
         tensor_map(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, l.x, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
   }
-  {  // packed codes as 32-bit words: [tile][G * 256]
-    const uint64_t dims[2] = {(uint64_t)G * 256, (uint64_t)ntiles};
-    const uint64_t strides[1] = {(uint64_t)G * 1024};
-    const uint32_t box[2] = {128, 8};
-    cudaError_t e =
-        tensor_map(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, l.data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (l.wtype == kBF16) {  // W [n][k] bf16, 128 x 64 tiles, swizzled as the tensor core reads them
+    const uint64_t dims[2] = {(uint64_t)l.k, (uint64_t)l.n};
+    const uint64_t strides[1] = {(uint64_t)l.k * 2};
+    const uint32_t box[2] = {kSlabK, kRows};
+    e = tensor_map(&tmw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, l.data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else if (l.wtype == kFP8) {  // W [n][k] E4M3 codes, 128 x 128 tiles (full 128-byte rows), swizzled
+    const uint64_t dims[2] = {(uint64_t)l.k, (uint64_t)l.n};
+    const uint64_t strides[1] = {(uint64_t)l.k};
+    const uint32_t box[2] = {2 * kSlabK, kRows};
+    e = tensor_map(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, l.data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    const int64_t G = l.k / 128;
+    {  // packed codes as 32-bit words: [tile][G * 256]
+      const uint64_t dims[2] = {(uint64_t)G * 256, (uint64_t)ntiles};
+      const uint64_t strides[1] = {(uint64_t)G * 1024};
+      const uint32_t box[2] = {128, 8};
+      e = tensor_map(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, l.data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (e == cudaSuccess) {  // packed scales as 32-bit words: [tile][G * 8]
+      const uint64_t dims[2] = {(uint64_t)G * 8, (uint64_t)ntiles};
+      const uint64_t strides[1] = {(uint64_t)G * 32};
+      const uint32_t box[2] = {8, 8};
+      e = tensor_map(&tms, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, l.scales, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
   }
-  {  // packed scales as 32-bit words: [tile][G * 8]
-    const uint64_t dims[2] = {(uint64_t)G * 8, (uint64_t)ntiles};
-    const uint64_t strides[1] = {(uint64_t)G * 32};
-    const uint32_t box[2] = {8, 8};
-    cudaError_t e = tensor_map(&tms, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, l.scales, dims, strides, box,
-                               CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (e != cudaSuccess) return e;
-  }
-  static std::atomic<int> configured[64];
+  if (e != cudaSuccess) return e;
+  static std::atomic<int> configured[64][3];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
-    cudaError_t e = cudaFuncSetAttribute(dq_gemm_int4_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  const int wi = l.wtype == kBF16 ? 0 : (l.wtype == kFP8 ? 1 : 2);
+  if (dev < 0 || dev >= 64 || !configured[dev][wi].load(std::memory_order_relaxed)) {
+    void* fn = wi == 0 ? tc_kernel<kBF16>() : (wi == 1 ? tc_kernel<kFP8>() : tc_kernel<kINT4>());
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_relaxed);
+    if (dev >= 0 && dev < 64) configured[dev][wi].store(1, std::memory_order_relaxed);
   }
   TcArgs a;
   a.wz = static_cast<const uint8_t*>(l.zeros);
+  a.wscale = l.wtype == kFP8 ? static_cast<const float*>(l.scales) : nullptr;
   a.y = l.y;
   a.counters = static_cast<unsigned*>(l.workspace);
   a.part = l.workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(l.workspace) + kCounterBytes) : nullptr;
@@ -563,8 +749,12 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
   a.ntok = p.ra;
   a.splits = p.splits;
   a.slabs_per_split = (int)(p.k_per_split / kSlabK);
-  return launch_pdl(dq_gemm_int4_tc_kernel, dim3(p.m_chunks, p.grid_x, p.splits), dim3(kThreads), (size_t)kSmem,
-                    s, tmx, tmw, tms, a);
+  const dim3 grid(p.m_chunks, p.grid_x, p.splits);
+  switch (wi) {
+    case 0: return launch_pdl(dq_gemm_tc_kernel<kBF16>, grid, dim3(kThreads), (size_t)p.smem_bytes, s, tmx, tmw, tms, a);
+    case 1: return launch_pdl(dq_gemm_tc_kernel<kFP8>, grid, dim3(kThreads), (size_t)p.smem_bytes, s, tmx, tmw, tms, a);
+    default: return launch_pdl(dq_gemm_tc_kernel<kINT4>, grid, dim3(kThreads), (size_t)p.smem_bytes, s, tmx, tmw, tms, a);
+  }
 }
 
 cudaError_t tc_take_device_error(uint32_t* flags) {

@@ -44,7 +44,7 @@ constexpr size_t kCounterBytes = 65536;  // = DQD_WS_COUNTER_BYTES
 // ---------------------------------------------------------------- dq_gemm --
 
 struct GemmPlan {
-  int tc;            // 1: tensor-core (tcgen05) kernel for wide m, INT4 only
+  int tc;            // 1: tensor-core (tcgen05) kernel for wide m
   int mt;            // m8 tiles per CTA pass (1, 2, 4, 8)
   int m_chunks;      // ceil(m / (8*mt))
   int grid_x;        // CTAs along n (one 16-row tile per warp)
@@ -76,7 +76,7 @@ cudaError_t launch_dq_gemm(const GemmLaunch& a, const GemmPlan& p, cudaStream_t 
 // tcgen05 path (dq_gemm_tc.cu): whether it takes this shape, its plan, its
 // launch, and its device error word.
 bool tc_supported(int wtype, int64_t m, int64_t n, int64_t k);
-GemmPlan plan_dq_gemm_tc(int64_t m, int64_t n, int64_t k, int num_sms);
+GemmPlan plan_dq_gemm_tc(int wtype, int64_t m, int64_t n, int64_t k, int num_sms);
 cudaError_t launch_dq_gemm_tc(const GemmLaunch& a, const GemmPlan& p, cudaStream_t s);
 cudaError_t tc_take_device_error(uint32_t* flags);
 

@@ -1,6 +1,6 @@
-"""GPU parity of the tensor-core (tcgen05) INT4 dq_gemm path taken at wide m
-(speculative verify batches), against the float64 oracle and against the
-warp-MMA kernels on the same inputs.
+"""GPU parity of the tensor-core (tcgen05) dq_gemm path taken at wide m (INT4
+from 128 rows, BF16 and FP8 from 32), against the float64 oracle and against
+the warp-MMA kernels on the same inputs.
 
 Shapes span several 128-row weight tiles and 128-token chunks with ragged n
 (partial 16-row tiles and CTAs with fewer than eight tiles), ragged m and
@@ -101,3 +101,57 @@ def test_planner_splits_a_small_grid(dev, dqd):
     splits k, which needs workspace."""
     _, w = _weight(dqd, dev, 4096, 14336, seed=1)
     assert dqd.dq_gemm_workspace_bytes(w, 384) > 0
+
+
+def _dense(dqd, dev, wtype, n, k, seed):
+    w = synth.bf16_weight(seed, "w", n, k, std=0.02, outlier_channels=6)
+    if wtype == oracle.W_BF16:
+        return dqd.Weight.bf16(bf(w, dev)), (w, None, None)
+    codes, scales = dqd.quant_fp8_rowwise(bf(w, dev))
+    rc, rs = oracle.quant_fp8_rowwise(w)
+    return dqd.Weight.fp8(codes, scales), (rc, rs, None)
+
+
+DENSE = [oracle.W_BF16, oracle.W_FP8_E4M3]
+
+
+@pytest.mark.parametrize("wtype", DENSE, ids=["bf16", "fp8"])
+@pytest.mark.parametrize("m,n,k", [(48, 130, 512), (49, 1000, 80), (64, 16, 4096), (100, 2050, 272),
+                                   (300, 64, 1024), (48, 10240, 8192), (1024, 300, 128)])
+def test_dense_against_oracle(dev, dqd, wtype, m, n, k):
+    """Ragged k (a partial last slab), ragged n and m, one-slab k, big shapes
+    (FP8 takes this path from 48 rows, BF16 from 32)."""
+    w, host = _dense(dqd, dev, wtype, n, k, seed=m + n + k)
+    x = synth.normal_bf16(m + 2 * k, "x", (m, k))
+    y = dqd.dq_gemm(w, bf(x, dev))
+    rows = None if n * m * k <= 2 ** 28 else np.unique(np.r_[0, n - 1, np.arange(0, n, 127)])
+    ref = oracle.dq_gemm(wtype, *host, x, rows=rows)
+    got = f64(y) if rows is None else f64(y)[:, rows]
+    assert_close(got, ref, what=f"tc {wtype} m={m} n={n} k={k}")
+
+
+@pytest.mark.parametrize("wtype", DENSE, ids=["bf16", "fp8"])
+@pytest.mark.parametrize("split", [1, 2, 3, 7])
+def test_dense_every_split(dev, dqd, monkeypatch, wtype, split):
+    monkeypatch.setenv("DQD_GEMM_SPLITS", str(split))
+    m, n, k = 56, 300, 1008
+    w, host = _dense(dqd, dev, wtype, n, k, seed=split)
+    x = synth.normal_bf16(split, "x", (m, k))
+    xd = bf(x, dev)
+    y = dqd.dq_gemm(w, xd)
+    assert_close(f64(y), oracle.dq_gemm(wtype, *host, x), what=f"tc {wtype} splits={split}")
+    assert np.array_equal(bits(y), bits(dqd.dq_gemm(w, xd)))
+
+
+@pytest.mark.parametrize("wtype", DENSE, ids=["bf16", "fp8"])
+def test_dense_matches_warp_mma_path(dev, dqd, monkeypatch, wtype):
+    w, _ = _dense(dqd, dev, wtype, 2000, 2048, seed=4)
+    x = bf(synth.normal_bf16(4, "x", (64, 2048)), dev)
+    a = f64(dqd.dq_gemm(w, x))
+    monkeypatch.setenv("DQD_GEMM_TC", "0")
+    b = f64(dqd.dq_gemm(w, x))
+    assert_close(a, b, what="tcgen05 vs mma.sync")
+
+
+def test_dense_no_device_error_flags(dev, dqd):
+    assert dqd.device_errors() == 0
