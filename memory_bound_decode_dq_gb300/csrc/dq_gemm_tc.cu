@@ -646,8 +646,10 @@ GemmPlan plan_dq_gemm_tc(int wtype, int64_t m, int64_t n, int64_t k, int num_sms
   // equal chunks) and the k split from a cost model: CTAs run in waves of one
   // per SM; a 64-wide slab costs its shared-memory traffic (weights in,
   // dequantised tile out and back to the tensor core, activations in and
-  // back: about base + 2 N cycles) or, with every SM streaming, its share of
-  // HBM (weight bytes at about 21 bytes per SM cycle), whichever is larger;
+  // back: about base + 2 N cycles; measured never below about 700 cycles, the
+  // latency of one slab's barrier, copy and MMA round trip) or, with every SM
+  // streaming, its share of HBM (weight bytes at about 21 bytes per SM
+  // cycle), whichever is larger;
   // plus a fixed 6 slabs of fill, drain and epilogue; a split adds its fp32
   // partial traffic at about 6 TB/s.
   const int64_t nslabs = (k + kSlabK - 1) / kSlabK, sms = std::max(num_sms, 1);
@@ -668,7 +670,7 @@ GemmPlan plan_dq_gemm_tc(int wtype, int64_t m, int64_t n, int64_t k, int num_sms
       if (forced >= 1 && sp != std::min<int64_t>(forced, units)) continue;
       const int64_t per = (units + sp - 1) / sp * unit;  // slabs per split
       const double waves = (double)((ctas * sp + sms - 1) / sms);
-      const double slab = std::max(base + 2.0 * ntok, ctas * sp >= sms ? wslab / 21.0 : 0.0);
+      const double slab = std::max(std::max(base + 2.0 * ntok, 700.0), ctas * sp >= sms ? wslab / 21.0 : 0.0);
       double cycles = waves * (per + 6.0) * slab;
       if (sp > 1) cycles += 8.0 * sp * m * n / 6e12 * 1.9e9;
       if (best < 0 || cycles < best * 0.97) {
