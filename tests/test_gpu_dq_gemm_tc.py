@@ -1,6 +1,6 @@
 """GPU parity of the tensor-core (tcgen05) dq_gemm path taken at wide m (INT4
-from 128 rows, BF16 and FP8 from 32), against the float64 oracle and against
-the warp-MMA kernels on the same inputs.
+from 128 rows, FP8 from 48, BF16 from 9), against the float64 oracle and
+against the warp-MMA kernels on the same inputs.
 
 Shapes span several 128-row weight tiles and 128-token chunks with ragged n
 (partial 16-row tiles and CTAs with fewer than eight tiles), ragged m and
@@ -120,7 +120,7 @@ DENSE = [oracle.W_BF16, oracle.W_FP8_E4M3]
                                    (300, 64, 1024), (48, 10240, 8192), (1024, 300, 128)])
 def test_dense_against_oracle(dev, dqd, wtype, m, n, k):
     """Ragged k (a partial last slab), ragged n and m, one-slab k, big shapes
-    (FP8 takes this path from 48 rows, BF16 from 32)."""
+    (FP8 takes this path from 48 rows, BF16 from 9)."""
     w, host = _dense(dqd, dev, wtype, n, k, seed=m + n + k)
     x = synth.normal_bf16(m + 2 * k, "x", (m, k))
     y = dqd.dq_gemm(w, bf(x, dev))
@@ -155,3 +155,14 @@ def test_dense_matches_warp_mma_path(dev, dqd, monkeypatch, wtype):
 
 def test_dense_no_device_error_flags(dev, dqd):
     assert dqd.device_errors() == 0
+
+
+@pytest.mark.parametrize("m,n,k", [(9, 300, 1024), (16, 6144, 4096), (12, 17, 72)])
+def test_bf16_small_m_on_tensor_cores(dev, dqd, m, n, k):
+    """BF16 from 9 rows: N = 16 tokens per CTA, most of them zero padding."""
+    w, host = _dense(dqd, dev, oracle.W_BF16, n, k, seed=m + n)
+    x = synth.normal_bf16(m + k, "x", (m, k))
+    rows = None if n <= 1024 else np.unique(np.r_[0, n - 1, np.arange(0, n, 97)])
+    got = f64(dqd.dq_gemm(w, bf(x, dev)))
+    ref = oracle.dq_gemm(oracle.W_BF16, *host, x, rows=rows)
+    assert_close(got if rows is None else got[:, rows], ref, what=f"tc bf16 m={m}")
