@@ -1,5 +1,5 @@
 """GPU parity of the tensor-core (tcgen05) dq_gemm path taken at wide m (INT4
-from 128 rows, FP8 from 48, BF16 from 9), against the float64 oracle and
+from 17 rows, FP8 from 48, BF16 from 9), against the float64 oracle and
 against the warp-MMA kernels on the same inputs.
 
 Shapes span several 128-row weight tiles and 128-token chunks with ragged n
@@ -33,7 +33,8 @@ def _weight(dqd, dev, n, k, seed):
 
 
 SHAPES = [(128, 128, 128), (129, 1000, 256), (256, 2048, 1024), (300, 48, 4096), (1024, 130, 512),
-          (500, 4112, 384), (200, 16, 128), (384, 6144, 4096)]
+          (500, 4112, 384), (200, 16, 128), (384, 6144, 4096), (17, 300, 1024), (32, 4096, 4096),
+          (64, 28672, 4096)]
 
 
 @pytest.mark.parametrize("m,n,k", SHAPES)
