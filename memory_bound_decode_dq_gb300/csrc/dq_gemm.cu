@@ -78,6 +78,7 @@ struct Args {
   int64_t m, n, k;
   int64_t k_per_split;
   int splits;
+  int cluster;             // splits reduce through distributed shared memory
   int ra;                  // activation rows held per stage (<= ROWS)
   int slot;                // bytes per ring slot
 };
@@ -257,6 +258,20 @@ __device__ __forceinline__ void compute_stage(float (&acc)[MT][4], uint32_t slot
   }
 }
 
+// Cluster-wide barrier over every thread of every CTA of the cluster, with
+// release/acquire ordering of shared-memory writes.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// fp32 load from the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t saddr, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 // Epilogue shared by the dq_gemm kernels (every thread of the CTA calls it):
 // bf16 output, or fp32 split-K partials reduced by the last-arriving CTA.
 template <int WT, int MT, int WARPS, int THREADS>
@@ -286,6 +301,43 @@ __device__ __forceinline__ void finish(const Args& a, float (&acc)[MT][4], int64
           a.y[mm * a.n + nn] = f32_to_bf16(v);
         }
       }
+    return;
+  }
+  if (a.cluster) {
+    // split-K inside a thread-block cluster (the splits of this tile set, in
+    // cluster rank order along y): every CTA stages its fp32 partial in its
+    // own shared memory, column-major [token][tile row]; after a cluster
+    // barrier, CTA r sums the r-th share of the valid outputs over the
+    // cluster's CTAs in rank (= split) order, reading them through
+    // distributed shared memory, and writes y. A second barrier keeps every
+    // CTA alive until its partial has been read.
+    constexpr int RT = WARPS * 16;          // tile rows of the CTA
+    extern __shared__ __align__(128) uint8_t fin_smem[];
+    float* stage = reinterpret_cast<float*>(fin_smem);
+    __syncthreads();  // the ring is no longer read
+    if (warp < WARPS) {
+#pragma unroll
+      for (int j = 0; j < MT; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          stage[(8 * j + 2 * t + (q & 1)) * RT + warp * 16 + g + 8 * (q >> 1)] = tile_ok ? acc[j][q] : 0.f;
+    }
+    cluster_sync_all();
+    const int S = a.splits, rank = (int)blockIdx.y;
+    const int cols = (int)min((int64_t)(8 * MT), a.m - m0);
+    const int ev = cols * RT, e0 = (int)((int64_t)rank * ev / S), e1 = (int)((int64_t)(rank + 1) * ev / S);
+    const uint32_t sbase = smem_addr(stage);
+    for (int e = e0 + threadIdx.x; e < e1; e += THREADS) {
+      const int col = e / RT, rid = e % RT;
+      const int64_t nn = tile0 * 16 + rid, mm = m0 + col;
+      float v = 0.f;
+      for (int p = 0; p < S; ++p) v += ld_dsmem_f32(sbase + 4u * (uint32_t)e, (uint32_t)p);
+      if (nn < a.n) {
+        if constexpr (WT == kFP8) v *= reinterpret_cast<const float*>(a.ws)[nn];
+        a.y[mm * a.n + nn] = f32_to_bf16(v);
+      }
+    }
+    cluster_sync_all();
     return;
   }
   // split-K: publish fp32 partials, then the last-arriving CTA reduces.
@@ -630,11 +682,19 @@ cudaError_t launch_t(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   a.splits = p.splits;
   a.ra = p.ra;
   a.slot = p.slot_bytes;
+  a.cluster = p.cluster;
   dim3 grid(p.grid_x, p.splits, p.m_chunks);
-  if constexpr (WT == kINT4)
+  if constexpr (WT == kINT4) {
+    if (p.cluster)
+      return launch_pdl_cluster(dq_gemm_int4_kernel<MT>, grid, dim3(Int4Cfg<MT>::THREADS), p.smem_bytes, s,
+                                (unsigned)p.splits, a);
     return launch_pdl(dq_gemm_int4_kernel<MT>, grid, dim3(Int4Cfg<MT>::THREADS), p.smem_bytes, s, a);
-  else
+  } else {
+    if (p.cluster)
+      return launch_pdl_cluster(dq_gemm_kernel<WT, MT>, grid, dim3(C::THREADS), p.smem_bytes, s, (unsigned)p.splits,
+                                a);
     return launch_pdl(dq_gemm_kernel<WT, MT>, grid, dim3(C::THREADS), p.smem_bytes, s, a);
+  }
 }
 
 template <int WT>
@@ -699,7 +759,17 @@ GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
   splits = (stages + per - 1) / per;
   p.splits = (int)splits;
   p.k_per_split = per * p.kc;
-  p.ws_bytes = p.splits > 1 ? kCounterBytes + sizeof(float) * (size_t)p.splits * m * n : 0;
+  // Up to 8 splits (the portable cluster size) reduce inside a cluster
+  // through distributed shared memory when the whole grid fits in 85% of one
+  // wave; measured, clusters lose on multi-wave or nearly full grids, where
+  // co-scheduling whole clusters leaves slots idle. Otherwise the splits go
+  // through global partials. Test hook: DQD_GEMM_CLUSTER=0 / 1 forces the
+  // global / cluster path (1 still needs 2..8 splits).
+  const char* cl_env = std::getenv("DQD_GEMM_CLUSTER");
+  p.cluster = p.splits > 1 && p.splits <= 8 && (double)base * p.splits <= 0.85 * (double)slots;
+  if (cl_env && cl_env[0] == '0') p.cluster = 0;
+  if (cl_env && cl_env[0] == '1') p.cluster = p.splits > 1 && p.splits <= 8;
+  p.ws_bytes = p.splits > 1 && !p.cluster ? kCounterBytes + sizeof(float) * (size_t)p.splits * m * n : 0;
   return p;
 }
 

@@ -30,6 +30,28 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// As launch_pdl, with CTAs grouped in thread-block clusters of cluster_y CTAs
+// along y (grid.y must be a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                               unsigned cluster_y, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = cluster_y;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 enum WType { kBF16 = 0, kFP8 = 1, kINT4 = 2 };
 
 // Tiled TMA tensor map over `base` (rank <= 5; dims innermost first; strides
@@ -49,6 +71,7 @@ struct GemmPlan {
   int m_chunks;      // ceil(m / (8*mt))
   int grid_x;        // CTAs along n (one 16-row tile per warp)
   int splits;        // CTAs along k
+  int cluster;       // 1: the splits of a tile form a thread-block cluster and reduce through DSMEM
   int64_t k_per_split;
   int kc;            // k per pipeline stage
   int ra;            // activation rows staged per CTA (<= 8 * mt)

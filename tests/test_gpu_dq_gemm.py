@@ -100,11 +100,23 @@ def test_fp8_ragged_k(dev, dqd, k):
     assert_close(f64(dqd.dq_gemm(c.weight, bf(x, dev))), c.ref(x), what=f"fp8 k={k}")
 
 
+@pytest.fixture
+def cluster(monkeypatch):
+    def set_cluster(on):
+        monkeypatch.setenv("DQD_GEMM_CLUSTER", "1" if on else "0")
+    yield set_cluster
+    monkeypatch.delenv("DQD_GEMM_CLUSTER", raising=False)
+
+
 @pytest.mark.parametrize("wtype", WT, ids=WT_IDS)
-@pytest.mark.parametrize("split", [1, 2, 3, 7, 64])
+@pytest.mark.parametrize("split", [1, 2, 3, 7, 8, 64])
 @pytest.mark.parametrize("m", [5, 20, 40])
-def test_every_split_count(dev, dqd, splits, wtype, split, m):
+@pytest.mark.parametrize("on", [True, False], ids=["dsmem", "global"])
+def test_every_split_count(dev, dqd, splits, cluster, wtype, split, m, on):
+    """Up to 8 splits reduce inside a thread-block cluster; more, or with the
+    cluster path switched off, through global partials and a ticket."""
     splits(split)
+    cluster(on)
     c = Case(dqd, dev, wtype, 96, 2048, seed=split)
     x = synth.normal_bf16(split + m, "x", (m, 2048))
     y = dqd.dq_gemm(c.weight, bf(x, dev))
@@ -112,14 +124,18 @@ def test_every_split_count(dev, dqd, splits, wtype, split, m):
 
 
 @pytest.mark.parametrize("wtype", WT, ids=WT_IDS)
-def test_deterministic_with_split_k(dev, dqd, wtype):
+@pytest.mark.parametrize("on", [True, False], ids=["dsmem", "global"])
+def test_deterministic_with_split_k(dev, dqd, splits, cluster, wtype, on):
+    splits(4)
+    cluster(on)
     c = Case(dqd, dev, wtype, 512, 4096, seed=9)
     x = bf(synth.normal_bf16(9, "x", (4, 4096)), dev)
     ws_need = dqd.dq_gemm_workspace_bytes(c.weight, 4)
-    assert ws_need > 0  # this shape takes the split-K path
+    assert (ws_need == 0) if on else (ws_need > 0)  # split-K inside a cluster needs no workspace
     a = bits(dqd.dq_gemm(c.weight, x))
     b = bits(dqd.dq_gemm(c.weight, x))
     assert np.array_equal(a, b)
+    assert dqd.device_errors() == 0
 
 
 def _one_hot(m_rows, k, cols):
@@ -203,7 +219,8 @@ def test_empty_and_degenerate(dev, dqd):
     assert y.shape == (3, 20) and torch.count_nonzero(y.float()).item() == 0
 
 
-def test_workspace_too_small_is_rejected(dev, dqd):
+def test_workspace_too_small_is_rejected(dev, dqd, cluster):
+    cluster(False)  # the global split-K path needs a workspace
     c = Case(dqd, dev, oracle.W_INT4_G128, 256, 4096)
     need = dqd.dq_gemm_workspace_bytes(c.weight, 2)
     assert need > 0
