@@ -728,11 +728,20 @@ GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
   const int64_t base = (int64_t)p.grid_x * p.m_chunks;
   const int cps = std::max(1, std::min((227 * 1024 - 1024) / std::max(p.smem_bytes, 1), 16 / ki.warps));
   const int64_t slots = (int64_t)std::max(num_sms, 1) * cps;
-  // Split k only as far as needed to fill the GPU; prefer the smallest split
-  // whose CTA count wastes little of the last wave.
+  // Split k: when 2..8 splits keep the whole grid within 85% of one wave,
+  // take as many as fit (they reduce inside a thread-block cluster, cheaply;
+  // measured: a 6144 x 4096 BF16 GEMV takes 10.7 us with 5 such splits, 14.4
+  // us with 6 global ones). Otherwise split only as far as needed to fill the
+  // GPU, preferring the smallest split whose CTA count wastes little of the
+  // last wave.
   const double wbytes = wtype == kBF16 ? 2.0 * n * k : (wtype == kFP8 ? 1.0 * n * k : 0.52 * n * k);
+  const char* cl_env = std::getenv("DQD_GEMM_CLUSTER");
+  const bool cluster_ok = !(cl_env && cl_env[0] == '0');
+  const int64_t fit = std::min<int64_t>(8, (int64_t)(0.85 * (double)slots) / std::max<int64_t>(base, 1));
   int64_t splits = 1;
-  if (base < 2 * slots) {
+  if (cluster_ok && fit >= 2 && stages >= 2) {
+    splits = fit;
+  } else if (base < 2 * slots) {
     double best = 0.0;
     for (int64_t sp = 1; sp <= std::min<int64_t>(stages, 64); ++sp) {
       if (sp > 1 && 8.0 * sp * m * n > 0.25 * wbytes) break;
@@ -765,7 +774,6 @@ GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
   // co-scheduling whole clusters leaves slots idle. Otherwise the splits go
   // through global partials. Test hook: DQD_GEMM_CLUSTER=0 / 1 forces the
   // global / cluster path (1 still needs 2..8 splits).
-  const char* cl_env = std::getenv("DQD_GEMM_CLUSTER");
   p.cluster = p.splits > 1 && p.splits <= 8 && (double)base * p.splits <= 0.85 * (double)slots;
   if (cl_env && cl_env[0] == '0') p.cluster = 0;
   if (cl_env && cl_env[0] == '1') p.cluster = p.splits > 1 && p.splits <= 8;
