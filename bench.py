@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps (capped at 2000)")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-call-protocol", action="store_true",
+                   help="skip the per-call graph protocol (50 back-to-back calls, L2-cold copies)")
     return p.parse_args()
 
 
@@ -144,8 +146,11 @@ class ClockSampler:
 # ------------------------------------------------------- device workload ----
 
 class Call:
-    def __init__(self, name, kind, nbytes, flops, fn, launches):
+    def __init__(self, name, kind, nbytes, flops, fn, launches, clone=None):
         self.name, self.kind, self.nbytes, self.flops, self.fn, self.launches = name, kind, nbytes, flops, fn, launches
+        # clone() -> a call of the same shape on fresh copies of the resident
+        # operands (weights, KV pools) and the same small inputs and outputs
+        self.clone = clone
 
 
 def build_calls(wl, dev, dqd):
@@ -178,8 +183,14 @@ def build_calls(wl, dev, dqd):
 
         def fn(weight=weight, x=x, y=y, ws=ws):
             dqd.dq_gemm(weight, x, y=y, ws=ws)
+
+        def clone(weight=weight, x=x, y=y, ws=ws):
+            wc = dqd.Weight(weight.type, weight.n, weight.k, weight.data.clone(),
+                            None if weight.scales is None else weight.scales.clone(),
+                            None if weight.zeros is None else weight.zeros.clone())
+            return lambda: dqd.dq_gemm(wc, x, y=y, ws=ws)
         calls.append(Call(c.name, "dq_gemm", bounds.dq_gemm_bytes(c.wtype, c.m, c.n, c.k),
-                          bounds.dq_gemm_flops(c.m, c.n, c.k), fn, 1))
+                          bounds.dq_gemm_flops(c.m, c.n, c.k), fn, 1, clone))
         io.append((c.name, [x], [y]))
     for a in wl.attns:
         seed = wl.seed
@@ -198,8 +209,12 @@ def build_calls(wl, dev, dqd):
 
         def fn(q=q, kp=kp, vp=vp, table_t=table_t, ctx_t=ctx_t, out=out, ws=ws, maxc=maxc):
             dqd.gqa_decode_attn(q, kp, vp, table_t, ctx_t, maxc, out=out, ws=ws)
+
+        def clone(q=q, kp=kp, vp=vp, table_t=table_t, ctx_t=ctx_t, out=out, ws=ws, maxc=maxc):
+            kc, vc = kp.clone(), vp.clone()
+            return lambda: dqd.gqa_decode_attn(q, kc, vc, table_t, ctx_t, maxc, out=out, ws=ws)
         calls.append(Call(a.name, "gqa_decode_attn", bounds.attn_bytes(ctx, a.width, a.hq, a.hkv, a.d),
-                          bounds.attn_flops(ctx, a.width, a.hq, a.d), fn, 2 if need else 1))
+                          bounds.attn_flops(ctx, a.width, a.hq, a.d), fn, 2 if need else 1, clone))
         io.append((a.name, [q, table_t, ctx_t], [out]))
     return calls, io
 
@@ -314,8 +329,61 @@ def run_ours(args, rank, world, dev):
 
     # end-to-end through the public API with pinned host buffers
     e2e = run_e2e(args, calls, io, dev, dqd, step_bytes, world)
+    # each call on its own (after the timed region)
+    proto = call_protocol(calls, dev) if not args.no_call_protocol else {}
     return dict(wl=wl, calls=calls, step_bytes=step_bytes, launches=launches_per_step, max_ms=max_ms,
-                per_call=per_call, clocks=clocks, e2e=e2e, K=K, diag=diag)
+                per_call=per_call, clocks=clocks, e2e=e2e, K=K, diag=diag, proto=proto)
+
+
+def call_protocol(calls, dev, n_calls=50, reps=7):
+    """Per-call device time, each call on its own: n_calls back-to-back calls
+    captured in a CUDA graph, rotating through copies of the resident operands
+    so that the copies span at least 4x the L2 (cold lines every call); the
+    graph is replayed `reps` times, each timed with CUDA events. Also the
+    latency of one call launched alone (events around a single eager call)."""
+    import torch
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20) or (128 << 20))
+    out = {}
+    for c in calls:
+        copies = max(1, min(64, math.ceil(4 * l2 / max(c.nbytes, 1)), int((8 << 30) // max(c.nbytes, 1))))
+        fns = [c.fn] + [c.clone() for _ in range(copies - 1)] if c.clone else [c.fn]
+        n = max(n_calls, len(fns))
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for f in fns:
+                f()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                fns[i % len(fns)]()
+        g.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / n)
+        single = []
+        for _ in range(10):
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            c.fn()
+            e1.record()
+            torch.cuda.synchronize()
+            single.append(e0.elapsed_time(e1) * 1e3)
+        out[c.name] = {"median": statistics.median(times), "min": min(times), "copies": len(fns), "calls": n,
+                       "single": statistics.median(single)}
+        del g, fns
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, calls, io, dev, dqd, step_bytes, world):
@@ -454,6 +522,21 @@ def run_reference(args, rank, world):
 METRIC = "effective HBM GB/s (% of GB300 peak) and us/call for dq_gemm + gqa_decode_attn"
 
 
+def cpu_model() -> str:
+    """The host CPU's model string (x86 'model name', Arm implementer/part)."""
+    try:
+        txt = open("/proc/cpuinfo").read()
+    except Exception:
+        return "unknown"
+    for key in ("model name", "Model", "Hardware"):
+        for line in txt.splitlines():
+            if line.lower().startswith(key.lower()) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    parts = [line.split(":", 1)[1].strip() for line in txt.splitlines()
+             if line.startswith(("CPU implementer", "CPU part")) and ":" in line][:2]
+    return "arm " + " ".join(parts) if parts else "unknown"
+
+
 def traffic_for(kernel_call_name, workload_name):
     """dram bytes per launch from the committed ncu summary, if it was taken on
     the current kernel sources."""
@@ -499,8 +582,20 @@ def main():
         for c in calls:
             us = per_call.get(c.name, 0.0) * 1e3
             gbs = c.nbytes / (us * 1e-6) / 1e9 if us > 0 else None
-            calls_info[c.name] = {"us": round(us, 3), "GB/s": round(gbs, 1) if gbs else None,
-                                  "frac_hbm": round(gbs / hbm, 4) if gbs else None, "bytes": int(c.nbytes)}
+            info = {"us": round(us, 3), "GB/s": round(gbs, 1) if gbs else None,
+                    "frac_hbm": round(gbs / hbm, 4) if gbs else None, "bytes": int(c.nbytes)}
+            pr = r["proto"].get(c.name)
+            if pr:
+                # each call alone: back-to-back in a CUDA graph, L2-cold copies
+                med = pr["median"]
+                info["alone"] = {"us_median": round(med, 3), "us_min": round(pr["min"], 3),
+                                 "GB/s": round(c.nbytes / (med * 1e-6) / 1e9, 1),
+                                 "frac_hbm": round(c.nbytes / (med * 1e-6) / 1e9 / hbm, 4),
+                                 "TFLOP/s": round(c.flops / (med * 1e-6) / 1e12, 2),
+                                 "frac_tensor_bf16": round(c.flops / (med * 1e-6) / 1e12 / tf, 4),
+                                 "copies": pr["copies"], "calls": pr["calls"],
+                                 "single_launch_us": round(pr["single"], 3)}
+            calls_info[c.name] = info
         dom = max(calls, key=lambda c: per_call.get(c.name, 0.0)) if per_call else None
         roof = None
         if dom is not None and per_call.get(dom.name, 0) > 0:
@@ -512,10 +607,16 @@ def main():
                     "algorithmic_bytes": int(dom.nbytes), "us_per_launch": round(per_call[dom.name] * 1e3, 3)}
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
+            # about cpu_seconds of oracle work: a sample sized for a third of
+            # it, run at least 3 times and until the budget is spent
             sample = OracleSample(wl, args.cpu_seconds / 3)
-            secs = sum(sample.run() for _ in range(3))
-            cpu = {"value": round(3 * sample.covered / secs / 1e9, 4), "unit": "GB/s", "cores": sample.threads,
-                   "kind": "oracle", "sample": sample.desc + f"; 3 runs, {secs:.1f} s"}
+            secs, runs = 0.0, 0
+            while runs < 3 or (secs < args.cpu_seconds and runs < 1000):
+                secs += sample.run()
+                runs += 1
+            cpu = {"value": round(runs * sample.covered / secs / 1e9, 4), "unit": "GB/s", "cores": sample.threads,
+                   "cpu_model": cpu_model(), "kind": "oracle",
+                   "sample": sample.desc + f"; {runs} runs, {secs:.1f} s"}
         ws_mb = working_set_bytes(calls) / 1e6
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size / 1e6
         line = {
