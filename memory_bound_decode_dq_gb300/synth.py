@@ -187,3 +187,52 @@ def paged_kv(seed: int, name: str, context_lens, hkv: int, d: int = 128,
 def context_lengths(seed: int, name: str, batch: int, lo: int, hi: int) -> np.ndarray:
     """Per-sequence context lengths uniform on [lo, hi]."""
     return rng(seed, name).integers(lo, hi + 1, size=batch).astype(np.int32)
+
+
+def e4m3_codes(seed: int, name: str, shape, exp_lo: int = 0, exp_hi: int = 15, device=None):
+    """FP8-E4M3 code bytes s.eeee.mmm drawn in code space: sign and 3-bit
+    mantissa uniform, exponent field uniform on [exp_lo, exp_hi]. The NaN
+    codes (0x7F, 0xFF) are replaced by the largest finite code of the same
+    sign (0x7E, 0xFE)."""
+    shape = tuple(int(s) for s in shape)
+    count = int(np.prod(shape)) if shape else 1
+    if _is_cuda(device) and count >= DEVICE_DRAW_THRESHOLD:
+        g = _torch_gen(seed, name, device)
+        sign = torch.randint(0, 2, shape, generator=g, device=device, dtype=torch.uint8)
+        expo = torch.randint(exp_lo, exp_hi + 1, shape, generator=g, device=device, dtype=torch.uint8)
+        mant = torch.randint(0, 8, shape, generator=g, device=device, dtype=torch.uint8)
+        c = (sign << 7) | (expo << 3) | mant
+        return torch.where((c & 0x7F) == 0x7F, c - 1, c)
+    r = rng(seed, name)
+    sign = r.integers(0, 2, size=shape, dtype=np.uint8)
+    expo = r.integers(exp_lo, exp_hi + 1, size=shape, dtype=np.uint8)
+    mant = r.integers(0, 8, size=shape, dtype=np.uint8)
+    c = (sign << 7) | (expo << 3) | mant
+    c[(c & 0x7F) == 0x7F] -= 1
+    return _out(c, device)
+
+
+@dataclass
+class PagedKVFp8:
+    """Paged FP8-E4M3 KV cache: code pools [num_blocks, Hkv, 16, D] uint8 plus
+    the block table and context lengths of :class:`PagedKV`."""
+    k_codes: object
+    v_codes: object
+    block_table: np.ndarray
+    context_lens: np.ndarray
+    num_blocks: int
+
+
+def paged_kv_fp8(seed: int, name: str, context_lens, hkv: int, d: int = 128,
+                 shuffle: bool = True, spare_blocks: int = 0, exp_lo: int = 0,
+                 exp_hi: int = 15, device=None) -> PagedKVFp8:
+    """K and V code pools from :func:`e4m3_codes` behind a block table. With
+    the default exponent range the codes cover every finite E4M3 value,
+    subnormals and both zeros included."""
+    table, nblk = block_table(seed, name + ".table", context_lens, shuffle, spare_blocks)
+    shape = (nblk, hkv, 16, d)
+    return PagedKVFp8(k_codes=e4m3_codes(seed, name + ".k", shape, exp_lo, exp_hi, device),
+                      v_codes=e4m3_codes(seed, name + ".v", shape, exp_lo, exp_hi, device),
+                      block_table=table,
+                      context_lens=np.asarray(context_lens, dtype=np.int32),
+                      num_blocks=nblk)

@@ -337,19 +337,30 @@ ORC_EXPORT int orc_dq_gemm(int wtype, const void* data, const void* scales,
 /*   K/V read through a block table of 16-token blocks [LIF §3.1, CS10 §7.3]; */
 /*   Hq query heads share Hkv KV heads [LIF §2.3]; causal inside the draft    */
 /*   block [ATC, Algorithm 1: later candidates cannot affect earlier ones].   */
-/* q: bf16 [B][W][Hq][D]; k_pool, v_pool: bf16 [blocks][Hkv][16][D];          */
+/* q: bf16 [B][W][Hq][D]; k_pool, v_pool: [blocks][Hkv][16][D] elements;      */
 /* block_table: int32 [B][max_blocks]; ctx: int32 [B].                        */
 /* Output rows are r = (b*W + i)*Hq + h; out is [nrows][D] double.            */
 /* Returns 0, or -1 on bad arguments / a violated precondition.               */
+/*                                                                            */
+/* KV element formats: KV_BF16 (bf16 bits, read exactly) and KV_FP8 (E4M3     */
+/* codes; the element's value is the code's value times one scale per pool,   */
+/* k_scale for K and v_scale for V) [LIF §4.2 C: K/V cached as FP8; MTC,      */
+/* speculative-decoding exercises: a 1-byte FP8 KV cache whose scale factors  */
+/* the pages leave open — one fp32 scale per tensor is the plain reading].    */
 /* ------------------------------------------------------------------------ */
 
-ORC_EXPORT int orc_gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool,
-                                   const uint16_t* v_pool,
-                                   const int32_t* block_table, int64_t max_blocks,
-                                   const int32_t* ctx, int64_t num_blocks,
-                                   int64_t B, int64_t W, int64_t Hq, int64_t Hkv,
-                                   int64_t D, double scale, const int64_t* rows,
-                                   int64_t nrows, double* out) {
+enum { KV_BF16 = 0, KV_FP8 = 1 };
+
+static double kv_elem(const void* pool, int fmt, int64_t idx, double scale) {
+  if (fmt == KV_FP8) return orc_e4m3_decode(((const uint8_t*)pool)[idx]) * scale;
+  return bf16_to_double(((const uint16_t*)pool)[idx]);
+}
+
+static int attn_core(const uint16_t* q, const void* k_pool, const void* v_pool, int fmt,
+                     double k_scale, double v_scale, const int32_t* block_table,
+                     int64_t max_blocks, const int32_t* ctx, int64_t num_blocks, int64_t B,
+                     int64_t W, int64_t Hq, int64_t Hkv, int64_t D, double scale,
+                     const int64_t* rows, int64_t nrows, double* out) {
   const int64_t BS = 16;
   if (B < 0 || W < 1 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return -1;
   if (rows == NULL && nrows != B * W * Hq) return -1;
@@ -369,9 +380,10 @@ ORC_EXPORT int orc_gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool,
     for (int64_t j = 0; j < nk; ++j) {
       int32_t phys = block_table[b * max_blocks + j / BS];
       if (phys < 0 || phys >= num_blocks) { err |= 1; phys = 0; }
-      const uint16_t* kr = k_pool + ((phys * Hkv + g) * BS + j % BS) * D;
+      const int64_t kr = ((phys * Hkv + g) * BS + j % BS) * D;
       double dot = 0.0;
-      for (int64_t d = 0; d < D; ++d) dot += bf16_to_double(qr[d]) * bf16_to_double(kr[d]);
+      for (int64_t d = 0; d < D; ++d)
+        dot += bf16_to_double(qr[d]) * kv_elem(k_pool, fmt, kr + d, k_scale);
       s[j] = scale * dot;
       if (s[j] > smax) smax = s[j];
     }
@@ -384,13 +396,37 @@ ORC_EXPORT int orc_gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool,
     for (int64_t j = 0; j < nk; ++j) {
       int32_t phys = block_table[b * max_blocks + j / BS];
       if (phys < 0 || phys >= num_blocks) phys = 0;
-      const uint16_t* vr = v_pool + ((phys * Hkv + g) * BS + j % BS) * D;
+      const int64_t vr = ((phys * Hkv + g) * BS + j % BS) * D;
       double p = s[j] / denom;
-      for (int64_t d = 0; d < D; ++d) out[ri * D + d] += p * bf16_to_double(vr[d]);
+      for (int64_t d = 0; d < D; ++d) out[ri * D + d] += p * kv_elem(v_pool, fmt, vr + d, v_scale);
     }
     free(s);
   }
   return err ? -1 : 0;
+}
+
+ORC_EXPORT int orc_gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool,
+                                   const uint16_t* v_pool,
+                                   const int32_t* block_table, int64_t max_blocks,
+                                   const int32_t* ctx, int64_t num_blocks,
+                                   int64_t B, int64_t W, int64_t Hq, int64_t Hkv,
+                                   int64_t D, double scale, const int64_t* rows,
+                                   int64_t nrows, double* out) {
+  return attn_core(q, k_pool, v_pool, KV_BF16, 1.0, 1.0, block_table, max_blocks, ctx,
+                   num_blocks, B, W, Hq, Hkv, D, scale, rows, nrows, out);
+}
+
+/* The same attention over an FP8-E4M3 cache: k_pool, v_pool hold one code per
+ * element, K = decode(code) * k_scale and V = decode(code) * v_scale. */
+ORC_EXPORT int orc_gqa_decode_attn_fp8kv(const uint16_t* q, const uint8_t* k_pool,
+                                         const uint8_t* v_pool, double k_scale,
+                                         double v_scale, const int32_t* block_table,
+                                         int64_t max_blocks, const int32_t* ctx,
+                                         int64_t num_blocks, int64_t B, int64_t W,
+                                         int64_t Hq, int64_t Hkv, int64_t D, double scale,
+                                         const int64_t* rows, int64_t nrows, double* out) {
+  return attn_core(q, k_pool, v_pool, KV_FP8, k_scale, v_scale, block_table, max_blocks, ctx,
+                   num_blocks, B, W, Hq, Hkv, D, scale, rows, nrows, out);
 }
 
 ORC_EXPORT int orc_num_threads(void) {

@@ -73,6 +73,10 @@ def _L():
         lib.orc_gqa_decode_attn.restype = ctypes.c_int
         lib.orc_gqa_decode_attn.argtypes = [P, P, P, P, I64, P, I64, I64, I64, I64, I64,
                                             I64, ctypes.c_double, P, I64, P]
+        lib.orc_gqa_decode_attn_fp8kv.restype = ctypes.c_int
+        lib.orc_gqa_decode_attn_fp8kv.argtypes = [P, P, P, ctypes.c_double, ctypes.c_double, P,
+                                                  I64, P, I64, I64, I64, I64, I64, I64,
+                                                  ctypes.c_double, P, I64, P]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -241,4 +245,32 @@ def gqa_decode_attn(q_bf16, k_pool, v_pool, block_table, context_lens, hkv: int,
                                   B, W, Hq, hkv, D, float(softmax_scale), _p(r), nrows, _p(out))
     if rc != 0:
         raise ValueError("orc_gqa_decode_attn rejected its arguments")
+    return out.reshape(B, W, Hq, D) if r is None else out
+
+
+def gqa_decode_attn_fp8kv(q_bf16, k_codes, v_codes, block_table, context_lens, hkv: int,
+                          softmax_scale: float, k_scale: float, v_scale: float,
+                          rows=None) -> np.ndarray:
+    """:func:`gqa_decode_attn` over an FP8-E4M3 cache, in float64.
+
+    k_codes, v_codes [blocks, Hkv, 16, D] uint8 E4M3 codes; the cached values
+    are decode(code) * k_scale and decode(code) * v_scale. Other arguments and
+    the result as in :func:`gqa_decode_attn`."""
+    q = _c(q_bf16, np.uint16)
+    kp = _c(k_codes, np.uint8)
+    vp = _c(v_codes, np.uint8)
+    bt = _c(block_table, np.int32)
+    cl = _c(context_lens, np.int32)
+    B, W, Hq, D = q.shape
+    nblk = kp.shape[0]
+    assert kp.shape == (nblk, hkv, 16, D) and vp.shape == kp.shape
+    assert bt.ndim == 2 and bt.shape[0] == B and cl.shape == (B,)
+    r = None if rows is None else _c(rows, np.int64)
+    nrows = B * W * Hq if r is None else r.size
+    out = np.empty((nrows, D), np.float64)
+    rc = _L().orc_gqa_decode_attn_fp8kv(_p(q), _p(kp), _p(vp), float(k_scale), float(v_scale),
+                                        _p(bt), bt.shape[1], _p(cl), nblk, B, W, Hq, hkv, D,
+                                        float(softmax_scale), _p(r), nrows, _p(out))
+    if rc != 0:
+        raise ValueError("orc_gqa_decode_attn_fp8kv rejected its arguments")
     return out.reshape(B, W, Hq, D) if r is None else out
