@@ -197,24 +197,35 @@ def build_calls(wl, dev, dqd):
         ctx = list(a.context)
         table, nblk = synth.block_table(seed, a.name + ".table", ctx, a.shuffle)
         shape = (nblk, a.hkv, 16, a.d)
-        kp = synth.normal_bf16(seed, a.name + ".k", shape, 1.0, device=dev)
-        vp = synth.normal_bf16(seed, a.name + ".v", shape, 1.0, device=dev)
+        if a.kv_fp8:
+            kp = synth.e4m3_codes(seed, a.name + ".k", shape, device=dev)
+            vp = synth.e4m3_codes(seed, a.name + ".v", shape, device=dev)
+        else:
+            kp = synth.normal_bf16(seed, a.name + ".k", shape, 1.0, device=dev)
+            vp = synth.normal_bf16(seed, a.name + ".v", shape, 1.0, device=dev)
         q = synth.normal_bf16(seed, a.name + ".q", (a.batch, a.width, a.hq, a.d), device=dev)
         table_t = torch.from_numpy(table).to(dev)
         ctx_t = torch.tensor(ctx, dtype=torch.int32, device=dev)
         out = torch.empty_like(q)
         maxc = max(ctx)
-        need = dqd.gqa_decode_attn_workspace_bytes(a.batch, a.width, a.hq, a.hkv, a.d, maxc)
+        if a.kv_fp8:
+            need = dqd.gqa_decode_attn_fp8kv_workspace_bytes(a.batch, a.width, a.hq, a.hkv, a.d, maxc)
+        else:
+            need = dqd.gqa_decode_attn_workspace_bytes(a.batch, a.width, a.hq, a.hkv, a.d, maxc)
         ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev) if need else None
 
-        def fn(q=q, kp=kp, vp=vp, table_t=table_t, ctx_t=ctx_t, out=out, ws=ws, maxc=maxc):
-            dqd.gqa_decode_attn(q, kp, vp, table_t, ctx_t, maxc, out=out, ws=ws)
+        def attn_call(kp, vp, q=q, table_t=table_t, ctx_t=ctx_t, out=out, ws=ws, maxc=maxc, a=a):
+            if a.kv_fp8:
+                return lambda: dqd.gqa_decode_attn_fp8kv(q, kp, vp, table_t, ctx_t, maxc, a.k_scale, a.v_scale,
+                                                         out=out, ws=ws)
+            return lambda: dqd.gqa_decode_attn(q, kp, vp, table_t, ctx_t, maxc, out=out, ws=ws)
 
-        def clone(q=q, kp=kp, vp=vp, table_t=table_t, ctx_t=ctx_t, out=out, ws=ws, maxc=maxc):
-            kc, vc = kp.clone(), vp.clone()
-            return lambda: dqd.gqa_decode_attn(q, kc, vc, table_t, ctx_t, maxc, out=out, ws=ws)
-        calls.append(Call(a.name, "gqa_decode_attn", bounds.attn_bytes(ctx, a.width, a.hq, a.hkv, a.d),
-                          bounds.attn_flops(ctx, a.width, a.hq, a.d), fn, 2 if need else 1, clone))
+        def clone(kp=kp, vp=vp, attn_call=attn_call):
+            return attn_call(kp.clone(), vp.clone())
+        calls.append(Call(a.name, "gqa_decode_attn_fp8kv" if a.kv_fp8 else "gqa_decode_attn",
+                          bounds.attn_bytes(ctx, a.width, a.hq, a.hkv, a.d,
+                                            kv_bytes_per_element=1 if a.kv_fp8 else 2),
+                          bounds.attn_flops(ctx, a.width, a.hq, a.d), attn_call(kp, vp), 2 if need else 1, clone))
         io.append((a.name, [q, table_t, ctx_t], [out]))
     return calls, io
 
@@ -472,7 +483,10 @@ class OracleSample:
             G = a.hq // a.hkv
             b = int(rng.integers(0, a.batch))
             ctx = [a.context[b]]
-            kv = synth.paged_kv(seed, a.name + ".cpu", ctx, 1, a.d, shuffle=a.shuffle)
+            if a.kv_fp8:
+                kv = synth.paged_kv_fp8(seed, a.name + ".cpu", ctx, 1, a.d, shuffle=a.shuffle)
+            else:
+                kv = synth.paged_kv(seed, a.name + ".cpu", ctx, 1, a.d, shuffle=a.shuffle)
             q = synth.normal_bf16(seed, a.name + ".cpu.q", (1, a.width, G, a.d))
             rows_all = a.batch * a.width * a.hq
             want = max(1, int(round(rows_all * frac)))
@@ -480,9 +494,15 @@ class OracleSample:
             rel = a.context[b] / (sum(a.context) / a.batch)
             nrows = max(1, min(a.width * G, int(round(want / max(rel, 1e-9)))))
             pick = np.sort(rng.choice(a.width * G, nrows, replace=False))
-            self.jobs.append(lambda kv=kv, q=q, pick=pick, d=a.d: oracle.gqa_decode_attn(
-                q, kv.k_pool, kv.v_pool, kv.block_table, kv.context_lens, 1, 1 / math.sqrt(d), rows=pick))
-            per_row = bounds.attn_bytes(a.context, a.width, a.hq, a.hkv, a.d) / rows_all
+            if a.kv_fp8:
+                self.jobs.append(lambda kv=kv, q=q, pick=pick, a=a: oracle.gqa_decode_attn_fp8kv(
+                    q, kv.k_codes, kv.v_codes, kv.block_table, kv.context_lens, 1, 1 / math.sqrt(a.d),
+                    a.k_scale, a.v_scale, rows=pick))
+            else:
+                self.jobs.append(lambda kv=kv, q=q, pick=pick, d=a.d: oracle.gqa_decode_attn(
+                    q, kv.k_pool, kv.v_pool, kv.block_table, kv.context_lens, 1, 1 / math.sqrt(d), rows=pick))
+            per_row = bounds.attn_bytes(a.context, a.width, a.hq, a.hkv, a.d,
+                                        kv_bytes_per_element=1 if a.kv_fp8 else 2) / rows_all
             self.covered += per_row * rel * nrows
         self.threads = oracle.num_threads()
         self.desc = (f"oracle on a random {frac:.4g} of every projection's output rows and on "

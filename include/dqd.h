@@ -6,7 +6,8 @@
  *
  *   dq_gemm          y = x * deq(W)^T, a weight-only quantised skinny GEMM.
  *   gqa_decode_attn  GQA attention of the new tokens' queries over a paged
- *                    BF16 KV cache, causal inside the verify block.
+ *                    BF16 KV cache, causal inside the verify block
+ *                    (gqa_decode_attn_fp8kv: the same over an FP8-E4M3 cache).
  *   pack_int4_g128   re-lay INT4 g128 codes/scales/zeros for dq_gemm.
  *   quant_fp8_rowwise  BF16 W -> FP8 E4M3 codes + per-output-row fp32 scales.
  *
@@ -231,6 +232,37 @@ DQD_API dqd_status gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool,
                            int32_t b, int32_t w, int32_t hq, int32_t hkv, int32_t d,
                            float softmax_scale, uint16_t* out, void* workspace,
                            size_t ws_bytes, dqd_stream stream);
+
+/* ------------------------------------------------------------------------
+ * gqa_decode_attn_fp8kv — gqa_decode_attn over an FP8-E4M3 KV cache.
+ *
+ * Sources: [LIF §4.2 C, KV-cache quantisation] K/V cached as FP8 halve the
+ * cache bytes and are close to lossless; [MTC, speculative-decoding
+ * exercises] the step bound with an idealised 1-byte FP8 KV. The pages leave
+ * the scale factors open; here each pool has one fp32 scale:
+ *   K_j = e4m3(k_pool code) * k_scale,  V_j = e4m3(v_pool code) * v_scale
+ * and the result is gqa_decode_attn's formula on those K_j, V_j.
+ *
+ * k_pool,v_pool: uint8 E4M3 codes [num_blocks][hkv][16][d]  (device); the
+ *               NaN codes 0x7F and 0xFF must not occur (the kernel reads
+ *               them as +-480)
+ * k_scale, v_scale: finite host floats (0 allowed)
+ * Every other argument, the layouts, requirements and results are those of
+ * gqa_decode_attn; the workspace size comes from
+ * gqa_decode_attn_fp8kv_workspace_bytes.
+ * ---------------------------------------------------------------------- */
+DQD_API dqd_status gqa_decode_attn_fp8kv_workspace_bytes(int32_t b, int32_t w, int32_t hq,
+                                                 int32_t hkv, int32_t d,
+                                                 int32_t max_context, size_t* bytes);
+
+DQD_API dqd_status gqa_decode_attn_fp8kv(const uint16_t* q, const uint8_t* k_pool,
+                                 const uint8_t* v_pool, int64_t num_blocks,
+                                 const int32_t* block_table, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens, int32_t max_context,
+                                 int32_t b, int32_t w, int32_t hq, int32_t hkv, int32_t d,
+                                 float softmax_scale, float k_scale, float v_scale,
+                                 uint16_t* out, void* workspace, size_t ws_bytes,
+                                 dqd_stream stream);
 
 /* ------------------------------------------------------------------------
  * gqa_decode_attn_static_ws — gqa_decode_attn without a caller workspace.

@@ -55,12 +55,14 @@ def dq_gemm_flops(m: int, n: int, k: int) -> float:
     return 2.0 * m * n * k
 
 
-def attn_bytes(context_lens, w: int, hq: int, hkv: int, d: int = 128, block: int = 16) -> float:
-    """K and V of every cached token of every sequence (bf16), plus q and out
-    (bf16), plus the block-table entries the call reads."""
+def attn_bytes(context_lens, w: int, hq: int, hkv: int, d: int = 128, block: int = 16,
+               kv_bytes_per_element: int = 2) -> float:
+    """K and V of every cached token of every sequence (2 bytes per element in
+    bf16, 1 in FP8), plus q and out (bf16), plus the block-table entries the
+    call reads."""
     ctx = [int(c) for c in context_lens]
     b = len(ctx)
-    kv = sum(ctx) * hkv * d * 2 * 2
+    kv = sum(ctx) * hkv * d * 2 * kv_bytes_per_element
     qo = 2 * (2 * b * w * hq * d)
     table = 4 * sum(math.ceil(c / block) for c in ctx)
     return float(kv + qo + table)

@@ -38,6 +38,9 @@ class AttnCase:
     context: tuple      # per-sequence context lengths (include the W new tokens)
     shuffle: bool = True
     d: int = 128
+    kv_fp8: bool = False  # FP8-E4M3 cache codes instead of bf16
+    k_scale: float = 1.0  # FP8 cache: cached K = code * k_scale
+    v_scale: float = 1.0  # FP8 cache: cached V = code * v_scale
 
 
 @dataclass(frozen=True)
@@ -118,4 +121,28 @@ def longctx_70b_b1() -> Workload:
                     attns=(AttnCase("attn_64_8_b1_ctx131072", 1, 1, 64, 8, (131072,)),))
 
 
-ALL = (tiny, llama3_8b_b1, dense70b_b32, verify_8b, longctx_70b_b8, longctx_70b_b1)
+# FP8 cache scales of the FP8-KV workloads: codes span +-448, so K = code/64
+# and V = code/128 keep the cached values within a few units.
+FP8_K_SCALE, FP8_V_SCALE = 1.0 / 64, 1.0 / 128
+
+
+def int4_70b_b32_fp8kv() -> Workload:
+    """70B-fixture decode layer at batch 32 with INT4 g128 projections and an
+    FP8-E4M3 KV cache: attention 64/8 heads over 2048 paged tokens per
+    sequence, codes drawn over every finite E4M3 value."""
+    g = tuple(GemmCase(f"{name}_int4_g128", W_INT4_G128, 32, n, k) for name, n, k in DENSE70B_PROJ)
+    return Workload("int4_70b_b32_fp8kv_ctx2048", 6, gemms=g,
+                    attns=(AttnCase("attn_fp8kv_64_8_b32_ctx2048", 32, 1, 64, 8, (2048,) * 32,
+                                    kv_fp8=True, k_scale=FP8_K_SCALE, v_scale=FP8_V_SCALE),))
+
+
+def longctx_70b_b8_fp8kv() -> Workload:
+    """The long-context attention of longctx_70b_b8 over an FP8-E4M3 cache:
+    8 sequences x 131072 paged tokens, 64/8 heads (2 GiB of KV codes)."""
+    return Workload("longctx_70b_b8_fp8kv_ctx131072", 7,
+                    attns=(AttnCase("attn_fp8kv_64_8_b8_ctx131072", 8, 1, 64, 8, (131072,) * 8,
+                                    kv_fp8=True, k_scale=FP8_K_SCALE, v_scale=FP8_V_SCALE),))
+
+
+ALL = (tiny, llama3_8b_b1, dense70b_b32, verify_8b, longctx_70b_b8, longctx_70b_b1,
+       int4_70b_b32_fp8kv, longctx_70b_b8_fp8kv)

@@ -15,17 +15,18 @@
 // g*G + r % G). A CTA has 4 warps: warp = (query tile, key slot); the KS = 4/QT
 // key slots split each pipeline stage's blocks between them.
 //
-//  * K/V blocks (4 KB each per kv head) are gathered through the block table
-//    with cp.async into a 3-stage shared-memory ring. 16-byte unit u of key row
-//    r is stored at u ^ sigma(r), sigma(r) = ((r>>1)&3)<<1 ^ (r&1)<<2, which
-//    makes both the K loads (lanes differ in key and d) and the V loads (lanes
-//    differ in key pair and d) conflict-free.
+//  * K/V blocks (4 KB each per kv head in bf16, 2 KB in FP8) are gathered
+//    through the block table by TMA into a shared-memory ring per key slot,
+//    128-byte swizzled (16-byte unit u of a 128-byte row r sits at u ^ (r & 7)).
 //  * S = Q K^T and O += P V run on mma.m16n8k16 (bf16 in, fp32 accumulate).
-//    For QK^T the head dimension is permuted inside each 32-wide chunk exactly
-//    like dq_gemm's k (lane t owns d = 32c + 8t .. +7) for both Q and K. For
-//    PV the B operand needs V[key 2t][d], V[key 2t+1][d] in one register: the
-//    lane loads 8 consecutive d of four keys and pairs them with prmt; the
-//    output column of n8 tile (h, jj), slot s is d = 64h + 8s + jj.
+//    The head dimension is permuted the same way for Q and K (lane t owns 16
+//    consecutive d per 64 in bf16, per 32 in FP8). For PV the B operand needs
+//    V[key 2t][d], V[key 2t+1][d] in one register: the lane loads consecutive
+//    d of four keys and pairs them with prmt.
+//  * FP8-E4M3 cache ("LLM 推理是怎么变快的" §4.2 C, KV cache quantisation):
+//    codes are widened to bf16 exactly in registers (every E4M3 value is a
+//    bf16 value); k_scale folds into the logit scale and v_scale into the
+//    output, so the MMAs see the codes' values unscaled.
 //  * Online softmax in the log2 domain (ex2), masked keys -> -inf by select:
 //    key j is visible to row r iff j <= ctx - W + r / G. V rows past the
 //    context are zeroed before the MMA so stale pool contents cannot leak.
@@ -51,8 +52,6 @@ constexpr float kNegInf = -INFINITY;
 
 struct Args {
   const uint16_t* q;
-  const uint16_t* kp;
-  const uint16_t* vp;
   const int32_t* table;
   const int32_t* ctx;
   uint16_t* out;
@@ -61,7 +60,8 @@ struct Args {
   int64_t num_blocks;
   int max_blocks, B, W, Hq, Hkv, G, QR;
   int chunk_blocks, nchunks, qgroups;
-  float scale_log2;
+  float scale_log2;  // softmax scale (times k_scale for FP8) times log2(e)
+  float v_scale;     // 1 for bf16
 };
 
 __device__ __forceinline__ int seq_ctx(const Args& a, int b) {
@@ -72,11 +72,13 @@ __device__ __forceinline__ int seq_ctx(const Args& a, int b) {
 // Per-module device error word (kErrWaitTimeout when a bounded wait gave up).
 __device__ unsigned int g_attn_error;
 
-template <int QT>
+template <int QT, bool F8>
 struct Cfg {
-  static constexpr int KS = 4 / QT;                        // key-slot groups per CTA
-  static constexpr int NS = QT == 1 ? 3 : (QT == 2 ? 4 : 6);  // ring slots per group
-  static constexpr int SLOT = 2 * kBlockBytes;            // K (2 x 2 KB) + V (2 x 2 KB)
+  static constexpr int KS = 4 / QT;  // key-slot groups per CTA
+  // ring slots per group: bf16 96/64/48 KB in all, FP8 64/64/48 KB
+  static constexpr int NS = F8 ? (QT == 1 ? 4 : (QT == 2 ? 8 : 12)) : (QT == 1 ? 3 : (QT == 2 ? 4 : 6));
+  // bf16: K (2 x 2 KB) + V (2 x 2 KB); FP8: K (2 KB) + V (2 KB)
+  static constexpr int SLOT = F8 ? kBlockBytes : 2 * kBlockBytes;
   static constexpr int RING = KS * NS * SLOT;
   static constexpr int MERGE = 4 * 16 * (kD + 2) * 4;     // (o, m, l) per warp-row
   static constexpr int BODY = RING > MERGE ? RING : MERGE;
@@ -84,18 +86,27 @@ struct Cfg {
   static constexpr int BYTES = 1024 + BODY + BARS;        // + alignment slack
 };
 
-// K and V of one (block, kv head) arrive as four 2 KB TMA boxes of 16 rows x
-// 64 head dims, 128-byte swizzled: 16-byte unit u of row r sits at unit
+// bf16: K and V of one (block, kv head) arrive as four 2 KB TMA boxes of 16
+// rows x 64 head dims, 128-byte swizzled: 16-byte unit u of row r sits at unit
 // u ^ (r & 7) of that row. Offsets inside a slot: K d<64, K d>=64, V d<64, V d>=64.
+// FP8: two 2 KB boxes of 16 rows x 128 codes, same swizzle: K, then V.
 __device__ __forceinline__ uint32_t kv_unit(uint32_t half_base, int row, int unit) {
   return half_base + row * 128 + ((unit ^ (row & 7)) << 4);
 }
 
-template <int QT>
+// Two E4M3 codes -> one bf16x2: prmt picks the low-half code and its
+// sign-replicated byte from (lo, hi) and likewise the high-half code; the
+// shift, mask and exact multiply by 2^120 are those of fp8_pair_to_bf16x2.
+__device__ __forceinline__ uint32_t fp8_sel_to_bf16x2(uint32_t lo, uint32_t hi, uint32_t sel) {
+  const uint32_t h = prmt(lo, hi, sel);
+  return bf16x2_mul((h << 4) & 0x87F087F0u, 0x7B807B80u);
+}
+
+template <int QT, bool F8>
 __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_constant__ CUtensorMap tmk,
                                                               const __grid_constant__ CUtensorMap tmv,
                                                               const Args a) {
-  using C = Cfg<QT>;
+  using C = Cfg<QT, F8>;
   constexpr int KS = C::KS, NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -165,18 +176,25 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
       const uint32_t dst = slot_addr(s), fb = full_bar(s);
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(fb, C::SLOT);
-      tma_load_4d(dst, &tmk, fb, 0, 0, g, phys);
-      tma_load_4d(dst + 2048, &tmk, fb, 64, 0, g, phys);
-      tma_load_4d(dst + 4096, &tmv, fb, 0, 0, g, phys);
-      tma_load_4d(dst + 6144, &tmv, fb, 64, 0, g, phys);
+      if constexpr (F8) {
+        tma_load_4d(dst, &tmk, fb, 0, 0, g, phys);
+        tma_load_4d(dst + 2048, &tmv, fb, 0, 0, g, phys);
+      } else {
+        tma_load_4d(dst, &tmk, fb, 0, 0, g, phys);
+        tma_load_4d(dst + 2048, &tmk, fb, 64, 0, g, phys);
+        tma_load_4d(dst + 4096, &tmv, fb, 0, 0, g, phys);
+        tma_load_4d(dst + 6144, &tmv, fb, 64, 0, g, phys);
+      }
     }
   };
   if (leader)
     for (int i = 0; i < min(NS, nb); ++i) issue(i);
 
-  // Q fragments for this warp's 16 query rows. The head dimension is permuted
-  // inside each 64-wide half: lane t owns d = 16t .. 16t+15 (16-byte units 2t
-  // and 2t+1), MMA i of the half reads d = 16t + 4i .. +3. K is read the same way.
+  // Q fragments for this warp's 16 query rows. The head dimension is permuted:
+  // in pass dh (0, 1) lane t owns 16 consecutive d starting at 64dh + 16t
+  // (bf16: 16-byte units 2t, 2t+1 of the 64-wide half dh) or 32t + 16dh (FP8:
+  // unit 2t + dh of the 128-code row); MMA i of the pass reads 4i .. 4i+3 of
+  // them. K is read the same way.
   uint32_t qf[2][4][4];
   int pos_lo, pos_hi;  // last visible key index of rows gq and gq+8 (-1: none)
   {
@@ -189,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
     for (int dh = 0; dh < 2; ++dh)
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int d = 64 * dh + 16 * t + 8 * u;
+        const int d = (F8 ? 32 * t + 16 * dh : 64 * dh + 16 * t) + 8 * u;
         const uint4 vl = okl ? *reinterpret_cast<const uint4*>(a.q + ql + d) : z;
         const uint4 vh = okh ? *reinterpret_cast<const uint4*>(a.q + qh + d) : z;
 #pragma unroll
@@ -218,7 +236,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
       ok = false;
       break;
     }
-    const uint32_t kb = slot_addr(s), vb = kb + 4096;
+    const uint32_t kb = slot_addr(s), vb = kb + (F8 ? 2048 : 4096);
     const int key0 = (blk0 + grp + KS * i) * kBlk;
     const int ntok = min(kBlk, ctx - key0);
 
@@ -230,13 +248,25 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
       const int r = 8 * h + gq;
 #pragma unroll
       for (int dh = 0; dh < 2; ++dh) {
-        const uint4 k0 = lds128(kv_unit(kb + 2048 * dh, r, 2 * t));
-        const uint4 k1 = lds128(kv_unit(kb + 2048 * dh, r, 2 * t + 1));
         float(&acc)[4] = dh ? sb : sa;
-        mma_bf16(acc, qf[dh][0][0], qf[dh][0][1], qf[dh][0][2], qf[dh][0][3], k0.x, k0.y);
-        mma_bf16(acc, qf[dh][1][0], qf[dh][1][1], qf[dh][1][2], qf[dh][1][3], k0.z, k0.w);
-        mma_bf16(acc, qf[dh][2][0], qf[dh][2][1], qf[dh][2][2], qf[dh][2][3], k1.x, k1.y);
-        mma_bf16(acc, qf[dh][3][0], qf[dh][3][1], qf[dh][3][2], qf[dh][3][3], k1.z, k1.w);
+        if constexpr (F8) {
+          // lanes t = 0..3 of rows gq, gq+1 hit units 2t+dh and (2t+dh)^1:
+          // eight distinct 16-byte bank groups per quarter warp
+          const uint4 c = lds128(kv_unit(kb, r, 2 * t + dh));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t u = word(c, i);
+            mma_bf16(acc, qf[dh][i][0], qf[dh][i][1], qf[dh][i][2], qf[dh][i][3], fp8_lo_to_bf16x2(u),
+                     fp8_hi_to_bf16x2(u));
+          }
+        } else {
+          const uint4 k0 = lds128(kv_unit(kb + 2048 * dh, r, 2 * t));
+          const uint4 k1 = lds128(kv_unit(kb + 2048 * dh, r, 2 * t + 1));
+          mma_bf16(acc, qf[dh][0][0], qf[dh][0][1], qf[dh][0][2], qf[dh][0][3], k0.x, k0.y);
+          mma_bf16(acc, qf[dh][1][0], qf[dh][1][1], qf[dh][1][2], qf[dh][1][3], k0.z, k0.w);
+          mma_bf16(acc, qf[dh][2][0], qf[dh][2][1], qf[dh][2][2], qf[dh][2][3], k1.x, k1.y);
+          mma_bf16(acc, qf[dh][3][0], qf[dh][3][1], qf[dh][3][2], qf[dh][3][3], k1.z, k1.w);
+        }
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) sc[h][q] = sa[q] + sb[q];
@@ -288,8 +318,33 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
     const uint32_t pa0 = pack_bf16x2(p[0][0], p[0][1]), pa1 = pack_bf16x2(p[0][2], p[0][3]);
     const uint32_t pa2 = pack_bf16x2(p[1][0], p[1][1]), pa3 = pack_bf16x2(p[1][2], p[1][3]);
 
-    // ---- O += P V: n8 tile (h, jj), slot s <-> d = 64h + 8s + jj ----
+    // ---- O += P V ----
     const int k0 = 2 * t, k1 = 2 * t + 1, k2 = 2 * t + 8, k3 = 2 * t + 9;
+    if constexpr (F8) {
+      // n8 tile jt, column s <-> d = 16s + jt: the lane loads unit gq (d =
+      // 16gq .. +15) of its four keys and pairs code jt of key 2t with code jt
+      // of key 2t+1 (and 2t+8 with 2t+9) while widening them.
+      uint4 va = lds128(kv_unit(vb, k0, gq));
+      uint4 vv = lds128(kv_unit(vb, k1, gq));
+      uint4 vc = lds128(kv_unit(vb, k2, gq));
+      uint4 vd = lds128(kv_unit(vb, k3, gq));
+      if (ntok < kBlk) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        if (k0 >= ntok) va = z;
+        if (k1 >= ntok) vv = z;
+        if (k2 >= ntok) vc = z;
+        if (k3 >= ntok) vd = z;
+      }
+#pragma unroll
+      for (int jt = 0; jt < 16; ++jt) {
+        // bytes: code jt&3 of the first word, its sign, the same of the second
+        const uint32_t sel = 0xC480u + 0x1111u * (jt & 3);
+        const uint32_t b0 = fp8_sel_to_bf16x2(word(va, jt >> 2), word(vv, jt >> 2), sel);
+        const uint32_t b1 = fp8_sel_to_bf16x2(word(vc, jt >> 2), word(vd, jt >> 2), sel);
+        mma_bf16(o[jt], pa0, pa1, pa2, pa3, b0, b1);
+      }
+    } else {
+    // n8 tile (h, jj), column s <-> d = 64h + 8s + jj
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint32_t hb = vb + 2048 * h;
@@ -311,6 +366,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
         const uint32_t b1 = prmt(word(vc, jj >> 1), word(vd, jj >> 1), sel);
         mma_bf16(o[8 * h + jj], pa0, pa1, pa2, pa3, b0, b1);
       }
+    }
     }
 
     // ---- release the slot and refill it ----
@@ -346,15 +402,15 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
   {
     float* wbase = mo + warp * 16 * (kD + 2);
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const int d0 = 64 * h + 8 * (2 * t) + jj, d1 = d0 + 8;
-        wbase[gq * (kD + 2) + d0] = o[8 * h + jj][0];
-        wbase[gq * (kD + 2) + d1] = o[8 * h + jj][1];
-        wbase[(gq + 8) * (kD + 2) + d0] = o[8 * h + jj][2];
-        wbase[(gq + 8) * (kD + 2) + d1] = o[8 * h + jj][3];
-      }
+    for (int j = 0; j < 16; ++j) {
+      // columns 2t, 2t+1 of tile j
+      const int d0 = F8 ? 32 * t + j : 64 * (j >> 3) + 16 * t + (j & 7);
+      const int d1 = d0 + (F8 ? 16 : 8);
+      wbase[gq * (kD + 2) + d0] = o[j][0];
+      wbase[gq * (kD + 2) + d1] = o[j][1];
+      wbase[(gq + 8) * (kD + 2) + d0] = o[j][2];
+      wbase[(gq + 8) * (kD + 2) + d1] = o[j][3];
+    }
     if (t == 0) {
       wbase[gq * (kD + 2) + kD] = m_lo;
       wbase[gq * (kD + 2) + kD + 1] = l_lo;
@@ -388,7 +444,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
   }
   const int64_t orow = ((int64_t)b * a.W + r / a.G) * a.Hq + g * a.G + r % a.G;
   if (a.nchunks == 1) {
-    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const float inv = (L > 0.f ? 1.f / L : 0.f) * a.v_scale;
     for (int c = 0; c < CPT; c += 2) {
       float v0 = 0.f, v1 = 0.f;
 #pragma unroll
@@ -408,7 +464,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
         const float* wb = mo + (j * QT + mqt) * 16 * (kD + 2) + mrow * (kD + 2);
         v += wgt[j] * wb[col0 + c];
       }
-      po[col0 + c] = v;
+      po[col0 + c] = v * a.v_scale;
     }
     if (threadIdx.x % TPR == 0) {
       a.part_ml[(orow * a.nchunks + chunk) * 2] = mstar;
@@ -480,36 +536,49 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const Args a) {
   *reinterpret_cast<uint2*>(a.out + row * kD + lane * 4) = o;
 }
 
-// A 4-D tensor map over a KV pool [num_blocks][hkv][16][128] bf16 whose box is
-// 64 head dims x 16 tokens of one (block, kv head), 128-byte swizzled.
-cudaError_t kv_tensor_map(const void* pool, int hkv, int64_t num_blocks, CUtensorMap* out) {
+// A 4-D tensor map over a KV pool [num_blocks][hkv][16][128] whose box is 16
+// tokens of one (block, kv head), 128 bytes wide (64 bf16 head dims or 128
+// FP8 codes), 128-byte swizzled.
+cudaError_t kv_tensor_map(const void* pool, bool f8, int hkv, int64_t num_blocks, CUtensorMap* out) {
+  const uint64_t es = f8 ? 1 : 2;
   const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)kBlk, (uint64_t)hkv, (uint64_t)num_blocks};
-  const uint64_t strides[3] = {(uint64_t)kD * 2, (uint64_t)kBlk * kD * 2, (uint64_t)hkv * kBlk * kD * 2};
-  const uint32_t box[4] = {64, (uint32_t)kBlk, 1, 1};
-  return tensor_map(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pool, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint64_t strides[3] = {(uint64_t)kD * es, (uint64_t)kBlk * kD * es, (uint64_t)hkv * kBlk * kD * es};
+  const uint32_t box[4] = {f8 ? 128u : 64u, (uint32_t)kBlk, 1, 1};
+  return tensor_map(out, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pool, dims,
+                    strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int QT>
+template <int QT, bool F8>
 cudaError_t launch_split(const Args& a, const AttnPlan& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
                          cudaStream_t s) {
-  using C = Cfg<QT>;
+  using C = Cfg<QT, F8>;
   static std::atomic<int> configured[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
-    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<QT, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_relaxed);
   }
   dim3 grid(p.nchunks, a.Hkv, a.B * p.qgroups);
-  return launch_pdl(attn_split_kernel<QT>, grid, dim3(kThreads), C::BYTES, s, tmk, tmv, a);
+  return launch_pdl(attn_split_kernel<QT, F8>, grid, dim3(kThreads), C::BYTES, s, tmk, tmv, a);
 }
 
-template <int QT>
+template <int QT, bool F8>
 constexpr int ctas_per_sm() {
   // shared memory (227 KB per SM usable) and registers (~165 per thread -> 3 CTAs)
-  return std::min(227 * 1024 / Cfg<QT>::BYTES, 3);
+  return std::min(227 * 1024 / Cfg<QT, F8>::BYTES, 3);
+}
+
+template <bool F8>
+int ctas_per_sm_of(int qt) {
+  return qt == 1 ? ctas_per_sm<1, F8>() : (qt == 2 ? ctas_per_sm<2, F8>() : ctas_per_sm<4, F8>());
+}
+
+template <bool F8>
+int smem_of(int qt) {
+  return qt == 1 ? Cfg<1, F8>::BYTES : (qt == 2 ? Cfg<2, F8>::BYTES : Cfg<4, F8>::BYTES);
 }
 
 // Fixed scratch for gqa_decode_attn_static_ws, for callers that cannot
@@ -546,7 +615,7 @@ cudaError_t attn_static_scratch(void** ptr) {
   return cudaSuccess;
 }
 
-AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms) {
+AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms, bool kv_fp8) {
   AttnPlan p{};
   const int G = hq / hkv;
   const int qr = G * w;
@@ -556,7 +625,7 @@ AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms) 
   const int ks = 4 / p.qt;
   const int maxblk = std::max(1, (max_context + kBlk - 1) / kBlk);
   const int64_t items = (int64_t)b * hkv * p.qgroups;
-  const int cps = p.qt == 1 ? ctas_per_sm<1>() : (p.qt == 2 ? ctas_per_sm<2>() : ctas_per_sm<4>());
+  const int cps = kv_fp8 ? ctas_per_sm_of<true>(p.qt) : ctas_per_sm_of<false>(p.qt);
   const int64_t slots = (int64_t)std::max(num_sms, 1) * cps;
   // About four waves of CTAs so that waves balance; each key-slot group gets
   // at least four blocks, and a chunk's partial (o, m, l) per query row stays
@@ -577,7 +646,8 @@ AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms) 
   cb = (cb + ks - 1) / ks * ks;
   p.chunk_blocks = cb;
   p.nchunks = (maxblk + cb - 1) / cb;
-  p.smem_bytes = p.qt == 1 ? Cfg<1>::BYTES : (p.qt == 2 ? Cfg<2>::BYTES : Cfg<4>::BYTES);
+  p.smem_bytes = kv_fp8 ? smem_of<true>(p.qt) : smem_of<false>(p.qt);
+  p.kv_fp8 = kv_fp8 ? 1 : 0;
   const size_t rows = (size_t)b * w * hq;
   p.ws_bytes = p.nchunks > 1 ? kCounterBytes + rows * p.nchunks * (kD + 2) * sizeof(float) : 0;
   return p;
@@ -595,8 +665,6 @@ cudaError_t attn_take_device_error(uint32_t* flags) {
 cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) {
   Args a;
   a.q = l.q;
-  a.kp = l.k_pool;
-  a.vp = l.v_pool;
   a.table = l.block_table;
   a.ctx = l.context_lens;
   a.out = l.out;
@@ -619,15 +687,25 @@ cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) 
   a.chunk_blocks = p.chunk_blocks;
   a.nchunks = p.nchunks;
   a.qgroups = p.qgroups;
-  a.scale_log2 = l.softmax_scale * 1.4426950408889634f;
+  const bool f8 = p.kv_fp8 != 0;
+  a.scale_log2 = f8 ? l.softmax_scale * l.k_scale * 1.4426950408889634f : l.softmax_scale * 1.4426950408889634f;
+  a.v_scale = f8 ? l.v_scale : 1.f;
   CUtensorMap tmk, tmv;
-  cudaError_t e = kv_tensor_map(l.k_pool, l.hkv, l.num_blocks, &tmk);
-  if (e == cudaSuccess) e = kv_tensor_map(l.v_pool, l.hkv, l.num_blocks, &tmv);
+  cudaError_t e = kv_tensor_map(l.k_pool, f8, l.hkv, l.num_blocks, &tmk);
+  if (e == cudaSuccess) e = kv_tensor_map(l.v_pool, f8, l.hkv, l.num_blocks, &tmv);
   if (e != cudaSuccess) return e;
-  switch (p.qt) {
-    case 1: e = launch_split<1>(a, p, tmk, tmv, s); break;
-    case 2: e = launch_split<2>(a, p, tmk, tmv, s); break;
-    default: e = launch_split<4>(a, p, tmk, tmv, s); break;
+  if (f8) {
+    switch (p.qt) {
+      case 1: e = launch_split<1, true>(a, p, tmk, tmv, s); break;
+      case 2: e = launch_split<2, true>(a, p, tmk, tmv, s); break;
+      default: e = launch_split<4, true>(a, p, tmk, tmv, s); break;
+    }
+  } else {
+    switch (p.qt) {
+      case 1: e = launch_split<1, false>(a, p, tmk, tmv, s); break;
+      case 2: e = launch_split<2, false>(a, p, tmk, tmv, s); break;
+      default: e = launch_split<4, false>(a, p, tmk, tmv, s); break;
+    }
   }
   if (e != cudaSuccess || p.nchunks == 1) return e;
   const int64_t blocks = ((int64_t)rows + 3) / 4;

@@ -223,25 +223,44 @@ dqd_status gqa_decode_attn_workspace_bytes(int32_t b, int32_t w, int32_t hq, int
   if (st != DQD_OK) return st;
   int sms = 0;
   if ((st = sm_count(&sms)) != DQD_OK) return st;
-  *bytes = dqd::plan_attn(b, w, hq, hkv, max_context, sms).ws_bytes;
+  *bytes = dqd::plan_attn(b, w, hq, hkv, max_context, sms, false).ws_bytes;
   return DQD_OK;
 }
 
-dqd_status gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
-                           int64_t num_blocks, const int32_t* block_table,
-                           int32_t max_blocks_per_seq, const int32_t* context_lens,
-                           int32_t max_context, int32_t b, int32_t w, int32_t hq, int32_t hkv,
-                           int32_t d, float softmax_scale, uint16_t* out, void* workspace,
-                           size_t ws_bytes, dqd_stream stream) {
+dqd_status gqa_decode_attn_fp8kv_workspace_bytes(int32_t b, int32_t w, int32_t hq, int32_t hkv,
+                                                 int32_t d, int32_t max_context, size_t* bytes) {
   g_last_error.clear();
+  if (!bytes) return fail(DQD_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = 0;
+  dqd_status st = check_attn_shape(b, w, hq, hkv, d, max_context);
+  if (st != DQD_OK) return st;
+  int sms = 0;
+  if ((st = sm_count(&sms)) != DQD_OK) return st;
+  *bytes = dqd::plan_attn(b, w, hq, hkv, max_context, sms, true).ws_bytes;
+  return DQD_OK;
+}
+
+}  // extern "C"
+
+// Argument checks and the plan shared by the attention entry points; fills
+// everything in *l but the workspace.
+static dqd_status prepare_attn(const uint16_t* q, const void* k_pool, const void* v_pool,
+                               int64_t num_blocks, const int32_t* block_table,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               int32_t max_context, int32_t b, int32_t w, int32_t hq, int32_t hkv,
+                               int32_t d, float softmax_scale, bool kv_fp8, float k_scale,
+                               float v_scale, uint16_t* out, dqd::AttnLaunch* l,
+                               dqd::AttnPlan* plan) {
   dqd_status st = check_attn_shape(b, w, hq, hkv, d, max_context);
   if (st != DQD_OK) return st;
   if (num_blocks < 1) return fail(DQD_ERR_INVALID_ARG, "num_blocks must be >= 1");
   if (max_blocks_per_seq < 1 || (int64_t)max_context > 16 * (int64_t)max_blocks_per_seq)
     return fail(DQD_ERR_INVALID_ARG, "max_context (%d) exceeds 16 * max_blocks_per_seq (%d)", max_context,
                 max_blocks_per_seq);
-  if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
-    return fail(DQD_ERR_INVALID_ARG, "softmax_scale must be finite");
+  const float scales[] = {softmax_scale, k_scale, v_scale};
+  for (float v : scales)
+    if (!(v == v) || v == INFINITY || v == -INFINITY)
+      return fail(DQD_ERR_INVALID_ARG, "softmax_scale, k_scale and v_scale must be finite");
   const void* ptrs[] = {q, k_pool, v_pool, out};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return fail(DQD_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned device pointers");
@@ -250,34 +269,71 @@ dqd_status gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool, const uint
     return fail(DQD_ERR_INVALID_ARG, "block_table and context_lens must be 4-byte aligned device pointers");
   int sms = 0;
   if ((st = sm_count(&sms)) != DQD_OK) return st;
-  const dqd::AttnPlan plan = dqd::plan_attn(b, w, hq, hkv, max_context, sms);
-  if ((int64_t)b * plan.qgroups > 65535)
+  *plan = dqd::plan_attn(b, w, hq, hkv, max_context, sms, kv_fp8);
+  if ((int64_t)b * plan->qgroups > 65535)
     return fail(DQD_ERR_UNSUPPORTED, "b * query groups exceeds the grid limit (b=%d)", b);
+  l->q = q;
+  l->k_pool = k_pool;
+  l->v_pool = v_pool;
+  l->num_blocks = num_blocks;
+  l->block_table = block_table;
+  l->max_blocks = max_blocks_per_seq;
+  l->context_lens = context_lens;
+  l->b = b;
+  l->w = w;
+  l->hq = hq;
+  l->hkv = hkv;
+  l->softmax_scale = softmax_scale;
+  l->k_scale = k_scale;
+  l->v_scale = v_scale;
+  l->out = out;
+  l->workspace = nullptr;
+  return DQD_OK;
+}
+
+static dqd_status attn_with_workspace(const char* who, dqd::AttnLaunch& l, const dqd::AttnPlan& plan,
+                                      void* workspace, size_t ws_bytes, dqd_stream stream) {
   if (plan.ws_bytes > 0) {
     if (!workspace || !aligned16(workspace))
-      return fail(DQD_ERR_WORKSPACE, "gqa_decode_attn needs a 16-byte aligned workspace of %zu bytes",
-                  plan.ws_bytes);
+      return fail(DQD_ERR_WORKSPACE, "%s needs a 16-byte aligned workspace of %zu bytes", who, plan.ws_bytes);
     if (ws_bytes < plan.ws_bytes)
-      return fail(DQD_ERR_WORKSPACE, "gqa_decode_attn workspace too small: %zu < %zu bytes", ws_bytes,
-                  plan.ws_bytes);
+      return fail(DQD_ERR_WORKSPACE, "%s workspace too small: %zu < %zu bytes", who, ws_bytes, plan.ws_bytes);
+    l.workspace = workspace;
   }
+  return check_launch(dqd::launch_attn(l, plan, reinterpret_cast<cudaStream_t>(stream)), who);
+}
+
+extern "C" {
+
+dqd_status gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                           int64_t num_blocks, const int32_t* block_table,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t max_context, int32_t b, int32_t w, int32_t hq, int32_t hkv,
+                           int32_t d, float softmax_scale, uint16_t* out, void* workspace,
+                           size_t ws_bytes, dqd_stream stream) {
+  g_last_error.clear();
   dqd::AttnLaunch l;
-  l.q = q;
-  l.k_pool = k_pool;
-  l.v_pool = v_pool;
-  l.num_blocks = num_blocks;
-  l.block_table = block_table;
-  l.max_blocks = max_blocks_per_seq;
-  l.context_lens = context_lens;
-  l.b = b;
-  l.w = w;
-  l.hq = hq;
-  l.hkv = hkv;
-  l.softmax_scale = softmax_scale;
-  l.out = out;
-  l.workspace = plan.ws_bytes > 0 ? workspace : nullptr;
-  return check_launch(dqd::launch_attn(l, plan, reinterpret_cast<cudaStream_t>(stream)),
-                      "gqa_decode_attn launch");
+  dqd::AttnPlan plan;
+  dqd_status st = prepare_attn(q, k_pool, v_pool, num_blocks, block_table, max_blocks_per_seq, context_lens,
+                               max_context, b, w, hq, hkv, d, softmax_scale, false, 1.f, 1.f, out, &l, &plan);
+  if (st != DQD_OK) return st;
+  return attn_with_workspace("gqa_decode_attn", l, plan, workspace, ws_bytes, stream);
+}
+
+dqd_status gqa_decode_attn_fp8kv(const uint16_t* q, const uint8_t* k_pool, const uint8_t* v_pool,
+                                 int64_t num_blocks, const int32_t* block_table,
+                                 int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                 int32_t max_context, int32_t b, int32_t w, int32_t hq, int32_t hkv,
+                                 int32_t d, float softmax_scale, float k_scale, float v_scale,
+                                 uint16_t* out, void* workspace, size_t ws_bytes, dqd_stream stream) {
+  g_last_error.clear();
+  dqd::AttnLaunch l;
+  dqd::AttnPlan plan;
+  dqd_status st = prepare_attn(q, k_pool, v_pool, num_blocks, block_table, max_blocks_per_seq, context_lens,
+                               max_context, b, w, hq, hkv, d, softmax_scale, true, k_scale, v_scale, out, &l,
+                               &plan);
+  if (st != DQD_OK) return st;
+  return attn_with_workspace("gqa_decode_attn_fp8kv", l, plan, workspace, ws_bytes, stream);
 }
 
 dqd_status gqa_decode_attn_static_ws(const uint16_t* q, const uint16_t* k_pool,
@@ -287,52 +343,22 @@ dqd_status gqa_decode_attn_static_ws(const uint16_t* q, const uint16_t* k_pool,
                                      int32_t w, int32_t hq, int32_t hkv, int32_t d,
                                      float softmax_scale, uint16_t* out, dqd_stream stream) {
   g_last_error.clear();
-  dqd_status st = check_attn_shape(b, w, hq, hkv, d, max_context);
+  dqd::AttnLaunch l;
+  dqd::AttnPlan plan;
+  dqd_status st = prepare_attn(q, k_pool, v_pool, num_blocks, block_table, max_blocks_per_seq, context_lens,
+                               max_context, b, w, hq, hkv, d, softmax_scale, false, 1.f, 1.f, out, &l, &plan);
   if (st != DQD_OK) return st;
-  if (num_blocks < 1) return fail(DQD_ERR_INVALID_ARG, "num_blocks must be >= 1");
-  if (max_blocks_per_seq < 1 || (int64_t)max_context > 16 * (int64_t)max_blocks_per_seq)
-    return fail(DQD_ERR_INVALID_ARG, "max_context (%d) exceeds 16 * max_blocks_per_seq (%d)", max_context,
-                max_blocks_per_seq);
-  if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
-    return fail(DQD_ERR_INVALID_ARG, "softmax_scale must be finite");
-  const void* ptrs[] = {q, k_pool, v_pool, out};
-  for (const void* p : ptrs)
-    if (!p || !aligned16(p)) return fail(DQD_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned device pointers");
-  if (!block_table || !context_lens || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
-      (reinterpret_cast<uintptr_t>(context_lens) & 3u))
-    return fail(DQD_ERR_INVALID_ARG, "block_table and context_lens must be 4-byte aligned device pointers");
-  int sms = 0;
-  if ((st = sm_count(&sms)) != DQD_OK) return st;
-  const dqd::AttnPlan plan = dqd::plan_attn(b, w, hq, hkv, max_context, sms);
-  if ((int64_t)b * plan.qgroups > 65535)
-    return fail(DQD_ERR_UNSUPPORTED, "b * query groups exceeds the grid limit (b=%d)", b);
   const size_t cap = dqd::attn_static_scratch_bytes();
   if (plan.ws_bytes > cap)
     return fail(DQD_ERR_WORKSPACE,
                 "gqa_decode_attn_static_ws: this call needs %zu bytes of scratch but the library's "
                 "static scratch holds %zu; use gqa_decode_attn with a caller workspace",
                 plan.ws_bytes, cap);
-  void* scratch = nullptr;
   if (plan.ws_bytes > 0) {
-    cudaError_t e = dqd::attn_static_scratch(&scratch);
+    cudaError_t e = dqd::attn_static_scratch(&l.workspace);
     if (e != cudaSuccess)
       return fail(DQD_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(e));
   }
-  dqd::AttnLaunch l;
-  l.q = q;
-  l.k_pool = k_pool;
-  l.v_pool = v_pool;
-  l.num_blocks = num_blocks;
-  l.block_table = block_table;
-  l.max_blocks = max_blocks_per_seq;
-  l.context_lens = context_lens;
-  l.b = b;
-  l.w = w;
-  l.hq = hq;
-  l.hkv = hkv;
-  l.softmax_scale = softmax_scale;
-  l.out = out;
-  l.workspace = scratch;
   return check_launch(dqd::launch_attn(l, plan, reinterpret_cast<cudaStream_t>(stream)),
                       "gqa_decode_attn_static_ws launch");
 }

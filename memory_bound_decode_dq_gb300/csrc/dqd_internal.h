@@ -114,21 +114,23 @@ struct AttnPlan {
   int chunk_blocks;  // 16-token blocks per split-KV chunk
   int nchunks;
   int smem_bytes;
+  int kv_fp8;        // 1: FP8-E4M3 cache codes, 0: bf16 cache
   size_t ws_bytes;   // 0 if nchunks == 1
 };
 
-AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms);
+AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms, bool kv_fp8);
 
 struct AttnLaunch {
   const uint16_t* q;
-  const uint16_t* k_pool;
-  const uint16_t* v_pool;
+  const void* k_pool;  // bf16 or FP8-E4M3 codes, as the plan says
+  const void* v_pool;
   int64_t num_blocks;
   const int32_t* block_table;
   int max_blocks;
   const int32_t* context_lens;
   int b, w, hq, hkv;
   float softmax_scale;
+  float k_scale, v_scale;  // FP8 cache only
   uint16_t* out;
   void* workspace;
 };

@@ -54,6 +54,11 @@ _SIGS = {
                                                        ctypes.POINTER(_SZ)]),
     "gqa_decode_attn": (ctypes.c_int, [_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
                                        _I32, ctypes.c_float, _P, _P, _SZ, _P]),
+    "gqa_decode_attn_fp8kv_workspace_bytes": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32,
+                                                             ctypes.POINTER(_SZ)]),
+    "gqa_decode_attn_fp8kv": (ctypes.c_int, [_P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32,
+                                             _I32, _I32, ctypes.c_float, ctypes.c_float,
+                                             ctypes.c_float, _P, _P, _SZ, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -264,25 +269,28 @@ def gqa_decode_attn_workspace_bytes(b: int, w: int, hq: int, hkv: int, d: int, m
     return int(out.value)
 
 
-def gqa_decode_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
-                    block_table: torch.Tensor, context_lens: torch.Tensor, max_context: int,
-                    softmax_scale: float | None = None, out: torch.Tensor | None = None,
-                    ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Paged GQA decode/verify attention. q bf16 [B, W, Hq, D]; pools bf16
-    [num_blocks, Hkv, 16, D]; block_table int32 [B, max_blocks]; context_lens
-    int32 [B] (device, includes the W new tokens); max_context: host bound."""
+def gqa_decode_attn_fp8kv_workspace_bytes(b: int, w: int, hq: int, hkv: int, d: int,
+                                          max_context: int) -> int:
+    out = _SZ(0)
+    _check(_lib.gqa_decode_attn_fp8kv_workspace_bytes(b, w, hq, hkv, d, max_context,
+                                                      ctypes.byref(out)),
+           "gqa_decode_attn_fp8kv_workspace_bytes")
+    return int(out.value)
+
+
+def _attn_args(name, q, k_pool, v_pool, pool_types, block_table, context_lens, softmax_scale, out):
     _need(q, "q", _B16)
     dev = q.device
-    _need(k_pool, "k_pool", _B16, dev)
-    _need(v_pool, "v_pool", _B16, dev)
+    _need(k_pool, "k_pool", pool_types, dev)
+    _need(v_pool, "v_pool", pool_types, dev)
     _need(block_table, "block_table", _I32T, dev)
     _need(context_lens, "context_lens", _I32T, dev)
     B, W, Hq, D = q.shape
     nblk, Hkv, bs, D2 = k_pool.shape
     if bs != 16 or D2 != D or v_pool.shape != k_pool.shape:
-        raise ValueError("gqa_decode_attn: pools must be [num_blocks, Hkv, 16, D] and equal shapes")
+        raise ValueError(f"{name}: pools must be [num_blocks, Hkv, 16, D] and equal shapes")
     if block_table.dim() != 2 or block_table.shape[0] != B or context_lens.shape != (B,):
-        raise ValueError("gqa_decode_attn: block_table must be [B, max_blocks], context_lens [B]")
+        raise ValueError(f"{name}: block_table must be [B, max_blocks], context_lens [B]")
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -290,13 +298,49 @@ def gqa_decode_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
     else:
         _need(out, "out", _B16, dev)
         if out.shape != q.shape:
-            raise ValueError("gqa_decode_attn: out must have q's shape")
+            raise ValueError(f"{name}: out must have q's shape")
+    return (B, W, Hq, Hkv, D, nblk), float(softmax_scale), out
+
+
+def gqa_decode_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                    block_table: torch.Tensor, context_lens: torch.Tensor, max_context: int,
+                    softmax_scale: float | None = None, out: torch.Tensor | None = None,
+                    ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Paged GQA decode/verify attention. q bf16 [B, W, Hq, D]; pools bf16
+    [num_blocks, Hkv, 16, D]; block_table int32 [B, max_blocks]; context_lens
+    int32 [B] (device, includes the W new tokens); max_context: host bound."""
+    (B, W, Hq, Hkv, D, nblk), scale, out = _attn_args(
+        "gqa_decode_attn", q, k_pool, v_pool, _B16, block_table, context_lens, softmax_scale, out)
     need = gqa_decode_attn_workspace_bytes(B, W, Hq, Hkv, D, int(max_context))
     if ws is None:
-        ws = workspace(need, dev, stream)
+        ws = workspace(need, q.device, stream)
     _check(_lib.gqa_decode_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), nblk, _ptr(block_table),
                                 block_table.shape[1], _ptr(context_lens), int(max_context), B, W, Hq,
-                                Hkv, D, float(softmax_scale), _ptr(out), _ptr(ws),
+                                Hkv, D, scale, _ptr(out), _ptr(ws),
                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
            "gqa_decode_attn")
+    return out
+
+
+def gqa_decode_attn_fp8kv(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                          block_table: torch.Tensor, context_lens: torch.Tensor, max_context: int,
+                          k_scale: float, v_scale: float, softmax_scale: float | None = None,
+                          out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """:func:`gqa_decode_attn` over an FP8-E4M3 cache: pools uint8 (or
+    float8_e4m3fn) codes [num_blocks, Hkv, 16, D]; cached values are
+    code * k_scale and code * v_scale."""
+    pool_types = _U8 + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+    (B, W, Hq, Hkv, D, nblk), scale, out = _attn_args(
+        "gqa_decode_attn_fp8kv", q, k_pool, v_pool, pool_types, block_table, context_lens,
+        softmax_scale, out)
+    need = gqa_decode_attn_fp8kv_workspace_bytes(B, W, Hq, Hkv, D, int(max_context))
+    if ws is None:
+        ws = workspace(need, q.device, stream)
+    _check(_lib.gqa_decode_attn_fp8kv(_ptr(q), _ptr(k_pool), _ptr(v_pool), nblk, _ptr(block_table),
+                                      block_table.shape[1], _ptr(context_lens), int(max_context), B,
+                                      W, Hq, Hkv, D, scale, float(k_scale), float(v_scale), _ptr(out),
+                                      _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                      _stream(stream)),
+           "gqa_decode_attn_fp8kv")
     return out

@@ -68,11 +68,18 @@ def check_attn(dqd, dev, case, seed, max_groups=None):
     ctx = np.asarray(case.context, np.int32)
     table, nblk = synth.block_table(seed, case.name + ".table", ctx, case.shuffle)
     shape = (nblk, hkv, 16, 128)
-    kp = synth.normal_bf16(seed, case.name + ".k", shape, 1.0, device=dev)
-    vp = synth.normal_bf16(seed, case.name + ".v", shape, 1.0, device=dev)
+    if case.kv_fp8:
+        kp = synth.e4m3_codes(seed, case.name + ".k", shape, device=dev)
+        vp = synth.e4m3_codes(seed, case.name + ".v", shape, device=dev)
+    else:
+        kp = synth.normal_bf16(seed, case.name + ".k", shape, 1.0, device=dev)
+        vp = synth.normal_bf16(seed, case.name + ".v", shape, 1.0, device=dev)
     q = synth.normal_bf16(seed, case.name + ".q", (B, W, hq, 128), device=dev)
-    out = dqd.gqa_decode_attn(q, kp, vp, torch.from_numpy(table).to(dev), torch.from_numpy(ctx).to(dev),
-                              int(ctx.max()))
+    args = (q, kp, vp, torch.from_numpy(table).to(dev), torch.from_numpy(ctx).to(dev), int(ctx.max()))
+    if case.kv_fp8:
+        out = dqd.gqa_decode_attn_fp8kv(*args, case.k_scale, case.v_scale)
+    else:
+        out = dqd.gqa_decode_attn(*args)
     groups = [(b, g) for b in range(B) for g in range(hkv)]
     if max_groups is not None and len(groups) > max_groups:
         pick = np.random.default_rng(seed).choice(len(groups), max_groups, replace=False)
@@ -81,11 +88,17 @@ def check_attn(dqd, dev, case, seed, max_groups=None):
     for b, g in groups:
         nb = (int(ctx[b]) + 15) // 16
         blocks = tab_dev[b, :nb].long()
-        ksub = bits(kp[blocks, g].unsqueeze(1).contiguous())     # [nb, 1, 16, 128]
-        vsub = bits(vp[blocks, g].unsqueeze(1).contiguous())
         qsub = bits(q[b:b + 1, :, g * G:(g + 1) * G].contiguous())  # [1, W, G, 128]
-        ref = oracle.gqa_decode_attn(qsub, ksub, vsub, np.arange(nb, dtype=np.int32)[None, :],
-                                     ctx[b:b + 1], 1, 1 / math.sqrt(128))
+        local = np.arange(nb, dtype=np.int32)[None, :]
+        if case.kv_fp8:
+            ksub = kp[blocks, g].unsqueeze(1).contiguous().cpu().numpy()   # [nb, 1, 16, 128]
+            vsub = vp[blocks, g].unsqueeze(1).contiguous().cpu().numpy()
+            ref = oracle.gqa_decode_attn_fp8kv(qsub, ksub, vsub, local, ctx[b:b + 1], 1, 1 / math.sqrt(128),
+                                               case.k_scale, case.v_scale)
+        else:
+            ksub = bits(kp[blocks, g].unsqueeze(1).contiguous())
+            vsub = bits(vp[blocks, g].unsqueeze(1).contiguous())
+            ref = oracle.gqa_decode_attn(qsub, ksub, vsub, local, ctx[b:b + 1], 1, 1 / math.sqrt(128))
         got = f64(out[b:b + 1, :, g * G:(g + 1) * G])
         assert_close(got, ref, what=f"{case.name} b={b} g={g}")
 
@@ -141,3 +154,18 @@ def test_longctx_gemm(dev, dqd, case):
 @pytest.mark.parametrize("case", WORKLOADS["longctx_70b_b8"].attns, ids=lambda c: c.name)
 def test_longctx_attn(dev, dqd, case):
     check_attn(dqd, dev, case, WORKLOADS["longctx_70b_b8"].seed, max_groups=3)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["int4_70b_b32_fp8kv"].gemms, ids=lambda c: c.name)
+def test_int4_70b_fp8kv_gemm(dev, dqd, case):
+    check_gemm(dqd, dev, case, WORKLOADS["int4_70b_b32_fp8kv"].seed)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["int4_70b_b32_fp8kv"].attns, ids=lambda c: c.name)
+def test_int4_70b_fp8kv_attn(dev, dqd, case):
+    check_attn(dqd, dev, case, WORKLOADS["int4_70b_b32_fp8kv"].seed, max_groups=24)
+
+
+@pytest.mark.parametrize("case", WORKLOADS["longctx_70b_b8_fp8kv"].attns, ids=lambda c: c.name)
+def test_longctx_fp8kv_attn(dev, dqd, case):
+    check_attn(dqd, dev, case, WORKLOADS["longctx_70b_b8_fp8kv"].seed, max_groups=3)
