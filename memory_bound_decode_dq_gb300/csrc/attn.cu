@@ -94,12 +94,32 @@ __device__ __forceinline__ uint32_t kv_unit(uint32_t half_base, int row, int uni
   return half_base + row * 128 + ((unit ^ (row & 7)) << 4);
 }
 
-// Two E4M3 codes -> one bf16x2: prmt picks the low-half code and its
-// sign-replicated byte from (lo, hi) and likewise the high-half code; the
-// shift, mask and exact multiply by 2^120 are those of fp8_pair_to_bf16x2.
-__device__ __forceinline__ uint32_t fp8_sel_to_bf16x2(uint32_t lo, uint32_t hi, uint32_t sel) {
-  const uint32_t h = prmt(lo, hi, sel);
-  return bf16x2_mul((h << 4) & 0x87F087F0u, 0x7B807B80u);
+// Four E4M3 codes (bytes 0..3 of u) -> two f16x2 (codes 0,1 and 2,3), exact:
+// every E4M3 value is an f16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t u, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(u));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// bf16x2 -> f16x2 (exact for magnitudes in [2^-14, 65504]).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
 template <int QT, bool F8>
@@ -208,8 +228,12 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int d = (F8 ? 32 * t + 16 * dh : 64 * dh + 16 * t) + 8 * u;
-        const uint4 vl = okl ? *reinterpret_cast<const uint4*>(a.q + ql + d) : z;
-        const uint4 vh = okh ? *reinterpret_cast<const uint4*>(a.q + qh + d) : z;
+        uint4 vl = okl ? *reinterpret_cast<const uint4*>(a.q + ql + d) : z;
+        uint4 vh = okh ? *reinterpret_cast<const uint4*>(a.q + qh + d) : z;
+        if constexpr (F8) {  // the FP8 path multiplies in f16
+          vl = make_uint4(bf16x2_to_f16x2(vl.x), bf16x2_to_f16x2(vl.y), bf16x2_to_f16x2(vl.z), bf16x2_to_f16x2(vl.w));
+          vh = make_uint4(bf16x2_to_f16x2(vh.x), bf16x2_to_f16x2(vh.y), bf16x2_to_f16x2(vh.z), bf16x2_to_f16x2(vh.w));
+        }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int i = 2 * u + e;
@@ -255,9 +279,9 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
           const uint4 c = lds128(kv_unit(kb, r, 2 * t + dh));
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint32_t u = word(c, i);
-            mma_bf16(acc, qf[dh][i][0], qf[dh][i][1], qf[dh][i][2], qf[dh][i][3], fp8_lo_to_bf16x2(u),
-                     fp8_hi_to_bf16x2(u));
+            uint32_t b0, b1;
+            e4m3x4_to_f16x2(word(c, i), b0, b1);
+            mma_f16(acc, qf[dh][i][0], qf[dh][i][1], qf[dh][i][2], qf[dh][i][3], b0, b1);
           }
         } else {
           const uint4 k0 = lds128(kv_unit(kb + 2048 * dh, r, 2 * t));
@@ -315,8 +339,18 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
       o[j][2] *= al_hi;
       o[j][3] *= al_hi;
     }
-    const uint32_t pa0 = pack_bf16x2(p[0][0], p[0][1]), pa1 = pack_bf16x2(p[0][2], p[0][3]);
-    const uint32_t pa2 = pack_bf16x2(p[1][0], p[1][1]), pa3 = pack_bf16x2(p[1][2], p[1][3]);
+    uint32_t pa0, pa1, pa2, pa3;
+    if constexpr (F8) {
+      pa0 = pack_f16x2(p[0][0], p[0][1]);
+      pa1 = pack_f16x2(p[0][2], p[0][3]);
+      pa2 = pack_f16x2(p[1][0], p[1][1]);
+      pa3 = pack_f16x2(p[1][2], p[1][3]);
+    } else {
+      pa0 = pack_bf16x2(p[0][0], p[0][1]);
+      pa1 = pack_bf16x2(p[0][2], p[0][3]);
+      pa2 = pack_bf16x2(p[1][0], p[1][1]);
+      pa3 = pack_bf16x2(p[1][2], p[1][3]);
+    }
 
     // ---- O += P V ----
     const int k0 = 2 * t, k1 = 2 * t + 1, k2 = 2 * t + 8, k3 = 2 * t + 9;
@@ -336,12 +370,16 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
         if (k3 >= ntok) vd = z;
       }
 #pragma unroll
-      for (int jt = 0; jt < 16; ++jt) {
-        // bytes: code jt&3 of the first word, its sign, the same of the second
-        const uint32_t sel = 0xC480u + 0x1111u * (jt & 3);
-        const uint32_t b0 = fp8_sel_to_bf16x2(word(va, jt >> 2), word(vv, jt >> 2), sel);
-        const uint32_t b1 = fp8_sel_to_bf16x2(word(vc, jt >> 2), word(vd, jt >> 2), sel);
-        mma_bf16(o[jt], pa0, pa1, pa2, pa3, b0, b1);
+      for (int w = 0; w < 4; ++w) {
+        // interleave codes 4w.. of keys 2t and 2t+1 (and 2t+8, 2t+9):
+        // [a0 b0 a1 b1] and [a2 b2 a3 b3], then widen pairs to f16x2
+        uint32_t x[4], y[4];
+        e4m3x4_to_f16x2(prmt(word(va, w), word(vv, w), 0x5140u), x[0], x[1]);
+        e4m3x4_to_f16x2(prmt(word(va, w), word(vv, w), 0x7362u), x[2], x[3]);
+        e4m3x4_to_f16x2(prmt(word(vc, w), word(vd, w), 0x5140u), y[0], y[1]);
+        e4m3x4_to_f16x2(prmt(word(vc, w), word(vd, w), 0x7362u), y[2], y[3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma_f16(o[4 * w + j], pa0, pa1, pa2, pa3, x[j], y[j]);
       }
     } else {
     // n8 tile (h, jj), column s <-> d = 64h + 8s + jj
