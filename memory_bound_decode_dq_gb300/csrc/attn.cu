@@ -675,6 +675,9 @@ AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms, 
   const int cb_min = std::max(4 * ks, std::min((13 * qr + 9) / 10, cb_wave));
   int64_t nch = std::max<int64_t>(1, (4 * slots + items - 1) / items);
   int cb = std::max<int>((int)((maxblk + nch - 1) / nch), cb_min);
+  // An FP8 block holds half the bytes of a bf16 block: twice the blocks keep
+  // a chunk's bytes, and the per-CTA start-up cost they amortise, the same.
+  if (kv_fp8) cb *= 2;
   // Test hook: DQD_ATTN_CHUNK_BLOCKS forces the split-KV chunk size.
   if (const char* env = std::getenv("DQD_ATTN_CHUNK_BLOCKS")) {
     const long v = std::strtol(env, nullptr, 10);
