@@ -445,9 +445,9 @@ __global__ void __launch_bounds__(Cfg<WT, MT>::THREADS) dq_gemm_kernel(const Arg
 // producer. Zero points travel with the stage when their 8-byte blocks form
 // 16-byte-aligned runs (an even number of groups in k and per stage);
 // otherwise they are read with ordinary loads one stage ahead.
-template <int MT>
+template <int MT, int W>
 struct Int4Cfg {
-  static constexpr int WARPS = MT <= 2 ? 8 : 4;
+  static constexpr int WARPS = W;  // consumer warps: 8 or 4 for m <= 16, 4 beyond
   static constexpr int THREADS = (WARPS + 1) * 32;
   static constexpr int ROWS = 8 * MT;
   static constexpr int KC = cmin(512, 8192 / ROWS);
@@ -460,9 +460,9 @@ struct Int4Cfg {
   static constexpr int XSTR = KC * 2 + 64;                    // padded activation row
 };
 
-template <int MT>
-__global__ void __launch_bounds__(Int4Cfg<MT>::THREADS) dq_gemm_int4_kernel(const Args a) {
-  using C = Int4Cfg<MT>;
+template <int MT, int W>
+__global__ void __launch_bounds__(Int4Cfg<MT, W>::THREADS) dq_gemm_int4_kernel(const Args a) {
+  using C = Int4Cfg<MT, W>;
   constexpr int NS = C::NS;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[2 * NS];
@@ -627,10 +627,10 @@ struct KernelInfo {
   int warps, kc, wstage, mstage, xrowb, rows, stages;
 };
 
-template <int WT, int MT>
+template <int WT, int MT, int W = (MT <= 2 ? 8 : 4)>
 KernelInfo info_t() {
   if constexpr (WT == kINT4) {
-    using C = Int4Cfg<MT>;
+    using C = Int4Cfg<MT, W>;
     return {C::WARPS, C::KC, C::CODES, C::META, C::XSTR, C::ROWS, C::NS};
   } else {
     using C = Cfg<WT, MT>;
@@ -638,7 +638,8 @@ KernelInfo info_t() {
   }
 }
 
-KernelInfo info_of(int wt, int mt) {
+// warps: INT4 consumer warps per CTA (8 or 4 for mt <= 2); ignored otherwise.
+KernelInfo info_of(int wt, int mt, int warps) {
 #define DQD_INFO(W)                          \
   switch (mt) {                              \
     case 1: return info_t<W, 1>();           \
@@ -648,18 +649,20 @@ KernelInfo info_of(int wt, int mt) {
   }
   if (wt == kBF16) { DQD_INFO(kBF16) }
   if (wt == kFP8) { DQD_INFO(kFP8) }
+  if (mt == 1 && warps == 4) return info_t<kINT4, 1, 4>();
+  if (mt == 2 && warps == 4) return info_t<kINT4, 2, 4>();
   DQD_INFO(kINT4)
 #undef DQD_INFO
 }
 
-template <int WT, int MT>
+template <int WT, int MT, int W = (MT <= 2 ? 8 : 4)>
 cudaError_t launch_t(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   using C = Cfg<WT, MT>;
   static std::atomic<int> configured[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || configured[dev].load(std::memory_order_relaxed) < p.smem_bytes) {
-    cudaError_t e = WT == kINT4 ? cudaFuncSetAttribute(dq_gemm_int4_kernel<MT>,
+    cudaError_t e = WT == kINT4 ? cudaFuncSetAttribute(dq_gemm_int4_kernel<MT, W>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes)
                                 : cudaFuncSetAttribute(dq_gemm_kernel<WT, MT>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
@@ -686,9 +689,9 @@ cudaError_t launch_t(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   dim3 grid(p.grid_x, p.splits, p.m_chunks);
   if constexpr (WT == kINT4) {
     if (p.cluster)
-      return launch_pdl_cluster(dq_gemm_int4_kernel<MT>, grid, dim3(Int4Cfg<MT>::THREADS), p.smem_bytes, s,
+      return launch_pdl_cluster(dq_gemm_int4_kernel<MT, W>, grid, dim3(Int4Cfg<MT, W>::THREADS), p.smem_bytes, s,
                                 (unsigned)p.splits, a);
-    return launch_pdl(dq_gemm_int4_kernel<MT>, grid, dim3(Int4Cfg<MT>::THREADS), p.smem_bytes, s, a);
+    return launch_pdl(dq_gemm_int4_kernel<MT, W>, grid, dim3(Int4Cfg<MT, W>::THREADS), p.smem_bytes, s, a);
   } else {
     if (p.cluster)
       return launch_pdl_cluster(dq_gemm_kernel<WT, MT>, grid, dim3(C::THREADS), p.smem_bytes, s, (unsigned)p.splits,
@@ -699,6 +702,10 @@ cudaError_t launch_t(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
 
 template <int WT>
 cudaError_t launch_wt(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
+  if constexpr (WT == kINT4) {
+    if (p.mt == 1 && p.warps == 4) return launch_t<WT, 1, 4>(l, p, s);
+    if (p.mt == 2 && p.warps == 4) return launch_t<WT, 2, 4>(l, p, s);
+  }
   switch (p.mt) {
     case 1: return launch_t<WT, 1>(l, p, s);
     case 2: return launch_t<WT, 2>(l, p, s);
@@ -709,13 +716,13 @@ cudaError_t launch_wt(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
 
 }  // namespace
 
-GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
-  // Test hook: DQD_GEMM_TC=0 keeps wide-m shapes on the warp-MMA kernels.
-  const char* tc_env = std::getenv("DQD_GEMM_TC");
-  if (tc_supported(wtype, m, n, k) && !(tc_env && tc_env[0] == '0')) return plan_dq_gemm_tc(wtype, m, n, k, num_sms);
+namespace {
+
+GemmPlan plan_warp_mma(int wtype, int64_t m, int64_t n, int64_t k, int num_sms, int warps) {
   GemmPlan p{};
   p.mt = m <= 8 ? 1 : (m <= 16 ? 2 : (m <= 32 ? 4 : 8));
-  const KernelInfo ki = info_of(wtype, p.mt);
+  const KernelInfo ki = info_of(wtype, p.mt, warps);
+  p.warps = ki.warps;
   const int64_t rows = ki.rows;
   p.m_chunks = (int)((m + rows - 1) / rows);
   const int64_t ntiles = (n + 15) / 16;
@@ -783,6 +790,33 @@ GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
   if (cl_env && cl_env[0] == '0') p.cluster = 0;
   if (cl_env && cl_env[0] == '1') p.cluster = p.splits > 1 && p.splits <= 8;
   p.ws_bytes = p.splits > 1 && !p.cluster ? kCounterBytes + sizeof(float) * (size_t)p.splits * m * n : 0;
+  return p;
+}
+
+// Time model for choosing the INT4 CTA width: CTAs are dealt to SMs evenly,
+// and an SM's time is its consumer warps' k stages, one tile per warp.
+double warp_mma_cost(const GemmPlan& p, int num_sms) {
+  const int64_t ctas = (int64_t)p.grid_x * p.splits * p.m_chunks;
+  const int64_t per_sm = (ctas + num_sms - 1) / std::max(num_sms, 1);
+  return (double)per_sm * p.warps * (double)((p.k_per_split + p.kc - 1) / p.kc);
+}
+
+}  // namespace
+
+GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
+  // Test hook: DQD_GEMM_TC=0 keeps wide-m shapes on the warp-MMA kernels.
+  const char* tc_env = std::getenv("DQD_GEMM_TC");
+  if (tc_supported(wtype, m, n, k) && !(tc_env && tc_env[0] == '0')) return plan_dq_gemm_tc(wtype, m, n, k, num_sms);
+  GemmPlan p = plan_warp_mma(wtype, m, n, k, num_sms, 8);
+  if (wtype == kINT4 && m <= 16) {
+    // INT4 at m <= 16: 8 or 4 consumer warps per CTA, whichever spreads the
+    // 16-row tiles more evenly over the SMs (fewer warps on ties). Test hook:
+    // DQD_GEMM_WARPS=4 / 8 forces the width.
+    const GemmPlan p4 = plan_warp_mma(wtype, m, n, k, num_sms, 4);
+    const char* w_env = std::getenv("DQD_GEMM_WARPS");
+    if (w_env && w_env[0] == '4') return p4;
+    if (!(w_env && w_env[0] == '8') && warp_mma_cost(p4, num_sms) <= warp_mma_cost(p, num_sms)) return p4;
+  }
   return p;
 }
 

@@ -68,6 +68,7 @@ constexpr size_t kCounterBytes = 65536;  // = DQD_WS_COUNTER_BYTES
 struct GemmPlan {
   int tc;            // 1: tensor-core (tcgen05) kernel for wide m
   int mt;            // m8 tiles per CTA pass (1, 2, 4, 8)
+  int warps;         // warp-MMA kernels: compute warps per CTA (one 16-row tile each)
   int m_chunks;      // ceil(m / (8*mt))
   int grid_x;        // CTAs along n (one 16-row tile per warp)
   int splits;        // CTAs along k

@@ -138,6 +138,20 @@ def test_deterministic_with_split_k(dev, dqd, splits, cluster, wtype, on):
     assert dqd.device_errors() == 0
 
 
+@pytest.mark.parametrize("warps", ["4", "8"])
+@pytest.mark.parametrize("split", [None, 1, 3])
+@pytest.mark.parametrize("m,n,k", [(1, 1024, 1024), (5, 200, 640), (9, 72, 384), (16, 500, 1536)])
+def test_int4_cta_widths(dev, dqd, splits, monkeypatch, warps, split, m, n, k):
+    """INT4 at m <= 16 runs 8 or 4 tile warps per CTA (the planner picks the
+    width that spreads the tiles more evenly); both agree with the oracle,
+    with and without split-K, on ragged tile counts."""
+    monkeypatch.setenv("DQD_GEMM_WARPS", warps)
+    splits(split)
+    c = Case(dqd, dev, oracle.W_INT4_G128, n, k, seed=m + n)
+    x = synth.normal_bf16(m, "x", (m, k))
+    assert_close(f64(dqd.dq_gemm(c.weight, bf(x, dev))), c.ref(x), what=f"int4 warps={warps} split={split}")
+
+
 def _one_hot(m_rows, k, cols):
     x = np.zeros((m_rows, k), np.uint16)
     x[np.arange(len(cols)), cols] = 0x3F80
