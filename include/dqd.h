@@ -247,6 +247,9 @@ DQD_API dqd_status gqa_decode_attn(const uint16_t* q, const uint16_t* k_pool,
  *               NaN codes 0x7F and 0xFF must not occur (the kernel reads
  *               them as +-480)
  * k_scale, v_scale: finite host floats (0 allowed)
+ * The products are taken in f16 (every E4M3 value is an f16 value): q is
+ * converted to f16, so |q| <= 65504 is required (entries below 2^-14 keep an
+ * absolute error <= 2^-25), and the softmax weights enter P V as f16.
  * Every other argument, the layouts, requirements and results are those of
  * gqa_decode_attn; the workspace size comes from
  * gqa_decode_attn_fp8kv_workspace_bytes.
