@@ -165,6 +165,56 @@ ORC_EXPORT void orc_int4_dequant(const uint8_t* codes, const uint16_t* scales,
                                 scales[r * groups + j / 128]);
 }
 
+/* INT4 asymmetric min/max quantiser [CS10 §5.2: a scale and a zero point map
+ * x to an integer grid, x ~ (q - z) * s; "粒度" (granularity): how many values
+ * share one scale, finer groups are more accurate at the cost of storing more
+ * scales; MTC "格式": INT4 with one scale per group of 128]. The pages' worked
+ * example is garbled; the plain min/max reading, per group of gsize weights of
+ * one row:
+ *   lo = min(0, min w), hi = max(0, max w)     (0 stays on the grid)
+ *   s  = bf16_RNE(fp32(fp32(hi - lo) / 15)); a group of zeros takes s = 1;
+ *        an s that rounds to 0 becomes the smallest bf16 subnormal
+ *   z  = clamp(rint(fp32(-lo / s)), 0, 15)
+ *   q  = clamp(rint(fp32(w / s)) + z, 0, 15)   (rint: ties to even)
+ * Every step that decides an integer is taken in IEEE binary32, the
+ * precision of the kernel. w: bf16 [n][k]; k % gsize == 0. */
+ORC_EXPORT void orc_int4_quant(const uint16_t* w, int64_t n, int64_t k, int64_t gsize,
+                               uint8_t* codes, uint16_t* scales, uint8_t* zeros) {
+  const int64_t G = k / gsize;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t g = 0; g < G; ++g) {
+      const uint16_t* wg = w + r * k + g * gsize;
+      float lo = 0.0f, hi = 0.0f;
+      for (int64_t j = 0; j < gsize; ++j) {
+        const float v = (float)bf16_to_double(wg[j]);
+        if (v < lo) lo = v;
+        if (v > hi) hi = v;
+      }
+      const float d = hi - lo;
+      uint16_t sb = 0x3F80; /* 1.0 */
+      if (d > 0.0f) {
+        const float s32 = d / 15.0f;
+        sb = orc_bf16_round((double)s32);
+        if ((sb & 0x7FFF) == 0) sb = 0x0001;
+      }
+      const float sf = (float)bf16_to_double(sb);
+      float zf = rintf(-lo / sf);
+      if (zf < 0.0f) zf = 0.0f;
+      if (zf > 15.0f) zf = 15.0f;
+      for (int64_t j = 0; j < gsize; ++j) {
+        const float v = (float)bf16_to_double(wg[j]);
+        float q = rintf(v / sf) + zf;
+        if (q < 0.0f) q = 0.0f;
+        if (q > 15.0f) q = 15.0f;
+        codes[r * k + g * gsize + j] = (uint8_t)q;
+      }
+      scales[r * G + g] = sb;
+      zeros[r * G + g] = (uint8_t)zf;
+    }
+  }
+}
+
 /* The packed INT4 g128 layout, as documented in include/dqd.h:
  *   NT = ceil(n/16) row tiles, G = k/128 groups, block b = T*G + g.
  *   Codes: 1024-byte blocks of 256 little-endian 32-bit words. Word

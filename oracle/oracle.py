@@ -64,6 +64,8 @@ def _L():
         lib.orc_quant_fp8_rowwise.argtypes = [P, I64, I64, P, P]
         lib.orc_int4_dequant.restype = None
         lib.orc_int4_dequant.argtypes = [P, P, P, I64, I64, P]
+        lib.orc_int4_quant.restype = None
+        lib.orc_int4_quant.argtypes = [P, I64, I64, I64, P, P, P]
         lib.orc_int4_pack.restype = None
         lib.orc_int4_pack.argtypes = [P, P, P, I64, I64, P, P, P]
         lib.orc_int4_unpack.restype = I64
@@ -149,6 +151,20 @@ def int4_dequant(codes, scales_bf16, zeros) -> np.ndarray:
     out = np.empty((n, k), np.uint16)
     _L().orc_int4_dequant(_p(c), _p(s), _p(z), n, k, _p(out))
     return out
+
+
+def int4_quant(w_bf16, group: int = 128):
+    """Asymmetric min/max INT4 quantiser (see orc_int4_quant): bf16 bit
+    patterns [n, k] -> (codes u8 [n, k], scales bf16 bits [n, k/group],
+    zeros u8 [n, k/group])."""
+    w = _c(w_bf16, np.uint16)
+    n, k = w.shape
+    assert group >= 1 and k % group == 0
+    codes = np.empty((n, k), np.uint8)
+    scales = np.empty((n, k // group), np.uint16)
+    zeros = np.empty((n, k // group), np.uint8)
+    _L().orc_int4_quant(_p(w), n, k, group, _p(codes), _p(scales), _p(zeros))
+    return codes, scales, zeros
 
 
 def int4_packed_sizes(n: int, k: int) -> tuple[int, int, int]:
