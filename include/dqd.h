@@ -2,7 +2,7 @@
  * dqd — memory-bound LLM decode kernels for GB300 (sm_103a), C ABI.
  *
  * Two operations make up the hot path of one decode (or speculative-verify)
- * step, and two offline operations prepare weights for it:
+ * step, and offline operations prepare weights for it:
  *
  *   dq_gemm          y = x * deq(W)^T, a weight-only quantised skinny GEMM.
  *   gqa_decode_attn  GQA attention of the new tokens' queries over a paged
@@ -10,6 +10,7 @@
  *                    (gqa_decode_attn_fp8kv: the same over an FP8-E4M3 cache).
  *   pack_int4_g128   re-lay INT4 g128 codes/scales/zeros for dq_gemm.
  *   quant_fp8_rowwise  BF16 W -> FP8 E4M3 codes + per-output-row fp32 scales.
+ *   quant_int4_g128  BF16 W -> INT4 codes + per-group bf16 scales and zeros.
  *
  * Sources (web pages):
  *   [MTC]  "降低每個 Token 的生成成本" (Making each token cheaper), optiverse-tech.com
@@ -158,6 +159,31 @@ DQD_API dqd_status pack_int4_g128(const uint8_t* codes, const uint16_t* scales_b
  * ---------------------------------------------------------------------- */
 DQD_API dqd_status quant_fp8_rowwise(const uint16_t* w_bf16, int64_t n, int64_t k,
                              uint8_t* codes, float* scales, dqd_stream stream);
+
+/* ------------------------------------------------------------------------
+ * quant_int4_g128 — BF16 W [n][k] -> INT4 g128 codes, bf16 scales, zero points
+ * (the logical inputs of pack_int4_g128), asymmetric min/max per group.
+ *
+ * Source: [CS10 §5.2] a scale and a zero point map values onto the integer
+ * grid, x ~ (q - z) * s; the granularity demo there: an outlier widens its
+ * own group's scale, finer groups are more accurate; [MTC, "格式"] INT4 with
+ * one scale per group of 128. The notes' worked example is garbled; reading,
+ * for row n and group j (weights W[n][128j .. 128j+127]):
+ *   lo = min(0, min W), hi = max(0, max W)          (0 stays on the grid)
+ *   s  = bf16_RNE(fp32(fp32(hi - lo) / 15)); all-zero group: s = 1; an s that
+ *        rounds to 0 becomes the smallest positive bf16
+ *   z  = clamp(rint(fp32(-lo / s)), 0, 15)
+ *   q  = clamp(rint(fp32(W / s)) + z, 0, 15)       (rint: ties to even)
+ * with IEEE binary32 division; dequantisation is (q - z) * s.
+ *
+ * w_bf16: [n][k] (device); codes: u8 [n][k], 0..15 (device);
+ * scales_bf16: [n][k/128] (device); zeros: u8 [n][k/128] (device).
+ * Requirements: n >= 1, k >= 128, k % 128 == 0, W finite, pointers 16-byte
+ * aligned.
+ * ---------------------------------------------------------------------- */
+DQD_API dqd_status quant_int4_g128(const uint16_t* w_bf16, int64_t n, int64_t k,
+                           uint8_t* codes, uint16_t* scales_bf16, uint8_t* zeros,
+                           dqd_stream stream);
 
 /* ------------------------------------------------------------------------
  * dq_gemm — y[m][n] = sum_k x[m][k] * deq(W)[n][k], bf16 in/out, fp32 accumulate.

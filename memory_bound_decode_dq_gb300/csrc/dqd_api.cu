@@ -154,6 +154,22 @@ dqd_status quant_fp8_rowwise(const uint16_t* w_bf16, int64_t n, int64_t k, uint8
                       "quant_fp8_rowwise launch");
 }
 
+dqd_status quant_int4_g128(const uint16_t* w_bf16, int64_t n, int64_t k, uint8_t* codes,
+                           uint16_t* scales_bf16, uint8_t* zeros, dqd_stream stream) {
+  g_last_error.clear();
+  if (n < 1 || k < 128 || k % 128)
+    return fail(DQD_ERR_INVALID_ARG, "quant_int4_g128 needs n >= 1, k >= 128, k %% 128 == 0 (n=%lld k=%lld)",
+                (long long)n, (long long)k);
+  if (n > ((int64_t)1 << 31) - 1 || k > ((int64_t)1 << 31) || n * (k / 128) > ((int64_t)1 << 36))
+    return fail(DQD_ERR_UNSUPPORTED, "quant_int4_g128: dimension too large");
+  if (!w_bf16 || !codes || !scales_bf16 || !zeros || !aligned16(w_bf16) || !aligned16(codes) ||
+      !aligned16(scales_bf16) || !aligned16(zeros))
+    return fail(DQD_ERR_INVALID_ARG, "quant_int4_g128: NULL or misaligned pointer");
+  return check_launch(dqd::launch_quant_int4(w_bf16, n, k, codes, scales_bf16, zeros,
+                                             reinterpret_cast<cudaStream_t>(stream)),
+                      "quant_int4_g128 launch");
+}
+
 dqd_status dq_gemm_workspace_bytes(const dqd_weight* w, int64_t m, size_t* bytes) {
   g_last_error.clear();
   if (!bytes) return fail(DQD_ERR_INVALID_ARG, "bytes is NULL");

@@ -155,4 +155,7 @@ cudaError_t launch_pack_int4(const uint8_t* codes, const uint16_t* scales, const
 cudaError_t launch_quant_fp8(const uint16_t* w, int64_t n, int64_t k, uint8_t* codes,
                              float* scales, cudaStream_t s);
 
+cudaError_t launch_quant_int4(const uint16_t* w, int64_t n, int64_t k, uint8_t* codes, uint16_t* scales,
+                              uint8_t* zeros, cudaStream_t s);
+
 }  // namespace dqd

@@ -1,4 +1,5 @@
-// Offline weight preparation: pack_int4_g128 and quant_fp8_rowwise.
+// Offline weight preparation: pack_int4_g128, quant_fp8_rowwise and
+// quant_int4_g128.
 //
 // Source: "降低每個 Token 的生成成本" (Making each token cheaper), section "格式"
 // (Formats): weight-only INT4 keeps 4-bit integers with one scale per group
@@ -132,6 +133,70 @@ cudaError_t launch_pack_int4(const uint8_t* codes, const uint16_t* scales, const
 cudaError_t launch_quant_fp8(const uint16_t* w, int64_t n, int64_t k, uint8_t* codes, float* scales,
                              cudaStream_t s) {
   quant_fp8_kernel<<<(unsigned)n, kQuantThreads, 0, s>>>(w, n, k, codes, scales);
+  return cudaGetLastError();
+}
+
+namespace {
+
+// INT4 asymmetric min/max quantiser: one warp per (row, 128-group), 8 groups
+// per CTA. Lane l holds weights 4l .. 4l+3 of the group. Every step that
+// decides an integer is IEEE binary32 with round-to-nearest-even, so codes,
+// scales and zeros are reproducible bit for bit.
+constexpr int kInt4QuantWarps = 8;
+
+__global__ void __launch_bounds__(kInt4QuantWarps * 32)
+quant_int4_kernel(const uint16_t* __restrict__ w, int64_t n, int64_t k, uint8_t* __restrict__ codes,
+                  uint16_t* __restrict__ scales, uint8_t* __restrict__ zeros) {
+  const int lane = threadIdx.x & 31;
+  const int64_t G = k / 128;
+  const int64_t unit = (int64_t)blockIdx.x * kInt4QuantWarps + (threadIdx.x >> 5);
+  if (unit >= n * G) return;
+  const int64_t row = unit / G, g = unit % G;
+  const int64_t off = row * k + g * 128 + 4 * lane;
+  const uint2 raw = *reinterpret_cast<const uint2*>(w + off);
+  const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+  // the range always holds 0, so 0 stays exactly on the grid
+  float lo = 0.f, hi = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    lo = fminf(lo, v[i]);
+    hi = fmaxf(hi, v[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  const float d = hi - lo;
+  uint16_t sb = 0x3F80u;  // a group of zeros takes scale 1
+  if (d > 0.f) {
+    sb = f32_to_bf16(__fdiv_rn(d, 15.0f));
+    if ((sb & 0x7FFFu) == 0) sb = 0x0001u;  // keep the scale positive
+  }
+  const float sf = __uint_as_float((uint32_t)sb << 16);
+  const float zf = fminf(fmaxf(rintf(__fdiv_rn(-lo, sf)), 0.f), 15.f);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float q = fminf(fmaxf(rintf(__fdiv_rn(v[i], sf)) + zf, 0.f), 15.f);
+    packed |= (uint32_t)q << (8 * i);
+  }
+  *reinterpret_cast<uint32_t*>(codes + off) = packed;
+  if (lane == 0) {
+    scales[row * G + g] = sb;
+    zeros[row * G + g] = (uint8_t)zf;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_int4(const uint16_t* w, int64_t n, int64_t k, uint8_t* codes, uint16_t* scales,
+                              uint8_t* zeros, cudaStream_t s) {
+  const int64_t units = n * (k / 128);
+  if (units == 0) return cudaSuccess;
+  const int64_t blocks = (units + kInt4QuantWarps - 1) / kInt4QuantWarps;
+  quant_int4_kernel<<<(unsigned)blocks, kInt4QuantWarps * 32, 0, s>>>(w, n, k, codes, scales, zeros);
   return cudaGetLastError();
 }
 

@@ -48,6 +48,7 @@ _SIGS = {
     "pack_int4_g128_bytes": (_SZ, [_I64, _I64, ctypes.c_int]),
     "pack_int4_g128": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _P, _P, _P]),
     "quant_fp8_rowwise": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
+    "quant_int4_g128": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P]),
     "dq_gemm_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(_WeightDesc), _I64, ctypes.POINTER(_SZ)]),
     "dq_gemm": (ctypes.c_int, [ctypes.POINTER(_WeightDesc), _P, _I64, _P, _P, _SZ, _P]),
     "gqa_decode_attn_workspace_bytes": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32,
@@ -227,6 +228,19 @@ def quant_fp8_rowwise(w: torch.Tensor, stream=None):
     _check(_lib.quant_fp8_rowwise(_ptr(w), n, k, _ptr(codes), _ptr(scales), _stream(stream)),
            "quant_fp8_rowwise")
     return codes, scales
+
+
+def quant_int4_g128(w: torch.Tensor, stream=None):
+    """bf16 W [n, k] -> (codes u8 [n, k] in 0..15, bf16 scales [n, k/128],
+    zero points u8 [n, k/128]): asymmetric min/max per 128-group."""
+    _need(w, "w", _B16)
+    n, k = w.shape
+    codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((n, k // 128), dtype=torch.bfloat16, device=w.device)
+    zeros = torch.empty((n, k // 128), dtype=torch.uint8, device=w.device)
+    _check(_lib.quant_int4_g128(_ptr(w), n, k, _ptr(codes), _ptr(scales), _ptr(zeros), _stream(stream)),
+           "quant_int4_g128")
+    return codes, scales, zeros
 
 
 def dq_gemm_workspace_bytes(weight: Weight, m: int) -> int:

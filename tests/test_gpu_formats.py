@@ -69,3 +69,51 @@ def test_pack_rejects_bad_shapes(dev, dqd):
         dqd.pack_int4_g128(torch.zeros((16, 100), dtype=torch.uint8, device=dev),
                            torch.zeros((16, 1), dtype=torch.bfloat16, device=dev),
                            torch.zeros((16, 1), dtype=torch.uint8, device=dev))
+
+
+def _int4_cases():
+    rng = np.random.default_rng(11)
+    w = rng.standard_normal((48, 1024)).astype(np.float32) * 0.02
+    w[3, :128] = 0.0                                   # all-zero group
+    w[4, 128:256] = 0.37                               # constant positive group
+    w[5, 256:384] = -0.37                              # constant negative group
+    w[6, :] = np.abs(w[6, :])                          # all-positive row
+    w[7, :] = -np.abs(w[7, :])                         # all-negative row
+    w[8, 384:512] = rng.standard_normal(128).astype(np.float32) * 1e-39   # bf16 subnormals
+    w[9, 512:640] *= 1e4                               # wide range
+    w[10, 700] = 3.0                                   # one outlier
+    w[11, 0:128] = np.linspace(-1, 1, 128)             # many exact ties
+    return synth.f32_to_bf16_bits(w)
+
+
+@pytest.mark.parametrize("n,k,kind", [(48, 1024, "special"), (96, 4096, "normal"), (1, 128, "normal"),
+                                      (257, 2048, "outliers")])
+def test_quant_int4_bit_exact(dev, dqd, n, k, kind):
+    if kind == "special":
+        w = _int4_cases()
+    else:
+        w = synth.bf16_weight(n + k, "q4", n, k, std=0.02, outlier_channels=6 if kind == "outliers" else 0)
+    codes, scales, zeros = dqd.quant_int4_g128(bf(w, dev))
+    rc, rs, rz = oracle.int4_quant(w)
+    assert np.array_equal(bits(scales), rs)
+    assert np.array_equal(zeros.cpu().numpy(), rz)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+def test_quant_int4_then_gemm(dev, dqd):
+    """bf16 W -> quant_int4_g128 -> pack_int4_g128 -> dq_gemm agrees with the
+    oracle's GEMM on the oracle's own quantisation of W."""
+    n, k = 200, 2048
+    w = synth.bf16_weight(5, "q4g", n, k, std=0.02, outlier_channels=4)
+    codes, scales, zeros = dqd.quant_int4_g128(bf(w, dev))
+    weight = dqd.Weight.int4(dqd.pack_int4_g128(codes, scales, zeros))
+    x = synth.normal_bf16(5, "x", (3, k))
+    from gpu_util import assert_close, f64
+    y = dqd.dq_gemm(weight, bf(x, dev))
+    rc, rs, rz = oracle.int4_quant(w)
+    assert_close(f64(y), oracle.dq_gemm(oracle.W_INT4_G128, rc, rs, rz, x), what="quantise -> pack -> gemm")
+
+
+def test_quant_int4_rejects_bad_shapes(dev, dqd):
+    with pytest.raises(dqd.DqdError):
+        dqd.quant_int4_g128(bf(np.zeros((4, 100), np.uint16), dev))
