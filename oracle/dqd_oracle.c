@@ -479,6 +479,97 @@ ORC_EXPORT int orc_gqa_decode_attn_fp8kv(const uint16_t* q, const uint8_t* k_poo
                    num_blocks, B, W, Hq, Hkv, D, scale, rows, nrows, out);
 }
 
+/* ------------------------------------------------------------------------ */
+/* Speculative verify: the step after the target's verify forward.            */
+/* ------------------------------------------------------------------------ */
+
+/* Greedy verify and KV-tail invalidation [ATC, Algorithm 1 "贪心验证及状态回退"]:
+ * per request, position 0 of the verify block is the round's input token and
+ * positions 1..k = w-1 hold the drafts d_1..d_k. t_i = argmax logits[i] (ties:
+ * the smallest token id). Compare d_{i+1} with t_i from i = 0, stop at the
+ * first mismatch: a = number of leading matches. The round emits the a matched
+ * drafts and then the target's token t_a (the correction, or the extra token
+ * when every draft matched): out = t_0 .. t_a, count = a + 1. The cache holds
+ * the w verify tokens at its end; the k - a rejected drafts' KV becomes
+ * invalid: context_lens -= k - a. A draft id outside [0, vocab) never matches.
+ * logits: bf16 [b][w][vocab]; draft: int32 [b][w-1]; out: int32 [b][w] gets
+ * t_0 .. t_{w-1}, of which the first count are the round's output; count:
+ * int32 [b]; ctx: int32 [b] or NULL. */
+ORC_EXPORT void orc_spec_verify_greedy(const uint16_t* logits, int64_t B, int64_t W, int64_t V,
+                                       const int32_t* draft, int32_t* out, int32_t* count,
+                                       int32_t* ctx) {
+  for (int64_t b = 0; b < B; ++b) {
+    int64_t a = 0;
+    for (int64_t i = 0; i < W; ++i) {
+      const uint16_t* row = logits + (b * W + i) * V;
+      int64_t best = 0;
+      double bv = bf16_to_double(row[0]);
+      for (int64_t v = 1; v < V; ++v) {
+        const double x = bf16_to_double(row[v]);
+        if (x > bv) { bv = x; best = v; }
+      }
+      out[b * W + i] = (int32_t)best;   /* t_i */
+      if (i == a && i < W - 1 && draft[b * (W - 1) + i] == best) a = i + 1;
+    }
+    count[b] = (int32_t)(a + 1);
+    if (ctx) ctx[b] -= (int32_t)((W - 1) - a);
+  }
+}
+
+/* Speculative sampling [CS336 lecture notes §6 "推测采样": draft x accepted with
+ * probability min(1, q(x)/p(x)); on the first rejection, one token from
+ * norm(max(q - p, 0)) and the rest of the draft is dropped; if all k are
+ * accepted, one extra token from the target's position k+1]. The random
+ * numbers are inputs: u_accept[b][i] in [0,1) decides draft i (accept iff
+ * u * p(x) < q(x), the same test without a division, in binary32 like the
+ * kernel), u_sample[b] in [0,1) draws the one sampled token by inverse CDF:
+ * the smallest y with sum_{z<=y} r(z) > u * sum_z r(z) (sums in double),
+ * r = max(q - p, 0) (binary32 difference) on a rejection, r = q for the extra
+ * token. A residual that sums to 0 (possible only through rounding) falls back
+ * to q. out = accepted drafts, then the sampled token; count = j + 1 with j
+ * the number accepted; ctx -= k - j.
+ * p: f32 [b][k][vocab]; q: f32 [b][k+1][vocab]; draft: int32 [b][k]. */
+static int64_t orc_inverse_cdf(const float* q, const float* p, int64_t V, double u) {
+  double total = 0.0;
+  for (int64_t y = 0; y < V; ++y) {
+    const float r = p ? fmaxf(q[y] - p[y], 0.0f) : q[y];
+    total += (double)r;
+  }
+  if (p && total <= 0.0) return orc_inverse_cdf(q, NULL, V, u);
+  const double thr = u * total;
+  double acc = 0.0;
+  int64_t last = 0;
+  for (int64_t y = 0; y < V; ++y) {
+    const float r = p ? fmaxf(q[y] - p[y], 0.0f) : q[y];
+    if (r > 0.0f) last = y;
+    acc += (double)r;
+    if (acc > thr) return y;
+  }
+  return last; /* u * total rounded up to the total: the last token with mass */
+}
+
+ORC_EXPORT void orc_spec_verify_sample(const float* p, const float* q, const int32_t* draft,
+                                       const float* u_accept, const float* u_sample,
+                                       int64_t B, int64_t K, int64_t V, int32_t* out,
+                                       int32_t* count, int32_t* ctx) {
+  for (int64_t b = 0; b < B; ++b) {
+    int64_t j = 0;
+    while (j < K) {
+      const int32_t x = draft[b * K + j];
+      if (x < 0 || x >= V) break;
+      const float px = p[(b * K + j) * V + x], qx = q[(b * (K + 1) + j) * V + x];
+      if (!(u_accept[b * K + j] * px < qx)) break;
+      out[b * (K + 1) + j] = x;
+      ++j;
+    }
+    const float* qrow = q + (b * (K + 1) + j) * V;
+    const float* prow = j < K ? p + (b * K + j) * V : NULL;
+    out[b * (K + 1) + j] = (int32_t)orc_inverse_cdf(qrow, prow, V, (double)u_sample[b]);
+    count[b] = (int32_t)(j + 1);
+    if (ctx) ctx[b] -= (int32_t)(K - j);
+  }
+}
+
 ORC_EXPORT int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -79,6 +79,10 @@ def _L():
         lib.orc_gqa_decode_attn_fp8kv.argtypes = [P, P, P, ctypes.c_double, ctypes.c_double, P,
                                                   I64, P, I64, I64, I64, I64, I64, I64,
                                                   ctypes.c_double, P, I64, P]
+        lib.orc_spec_verify_greedy.restype = None
+        lib.orc_spec_verify_greedy.argtypes = [P, I64, I64, I64, P, P, P, P]
+        lib.orc_spec_verify_sample.restype = None
+        lib.orc_spec_verify_sample.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, P]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -290,3 +294,39 @@ def gqa_decode_attn_fp8kv(q_bf16, k_codes, v_codes, block_table, context_lens, h
     if rc != 0:
         raise ValueError("orc_gqa_decode_attn_fp8kv rejected its arguments")
     return out.reshape(B, W, Hq, D) if r is None else out
+
+
+# ------------------------------------------------------------ verify ----
+
+def spec_verify_greedy(logits_bf16, draft, context_lens=None):
+    """Greedy verify (orc_spec_verify_greedy). logits bf16 bits [b, w, vocab];
+    draft int32 [b, w-1]. Returns (out int32 [b, w] with -1 past count,
+    count int32 [b], new context_lens or None)."""
+    lg = _c(logits_bf16, np.uint16)
+    B, W, V = lg.shape
+    d = _c(draft, np.int32).reshape(B, W - 1)
+    out = np.full((B, W), -1, np.int32)
+    cnt = np.zeros(B, np.int32)
+    ctx = None if context_lens is None else _c(context_lens, np.int32).copy()
+    _L().orc_spec_verify_greedy(_p(lg), B, W, V, _p(d), _p(out), _p(cnt), _p(ctx))
+    out[np.arange(W)[None, :] >= cnt[:, None]] = -1
+    return out, cnt, ctx
+
+
+def spec_verify_sample(p, q, draft, u_accept, u_sample, context_lens=None):
+    """Speculative sampling (orc_spec_verify_sample). p f32 [b, k, vocab];
+    q f32 [b, k+1, vocab]; draft int32 [b, k]; u_accept f32 [b, k]; u_sample
+    f32 [b]. Returns (out int32 [b, k+1] with -1 past count, count, ctx)."""
+    pp = _c(p, np.float32)
+    qq = _c(q, np.float32)
+    B, K, V = pp.shape
+    assert qq.shape == (B, K + 1, V)
+    d = _c(draft, np.int32).reshape(B, K)
+    ua = _c(u_accept, np.float32).reshape(B, K)
+    us = _c(u_sample, np.float32).reshape(B)
+    out = np.full((B, K + 1), -1, np.int32)
+    cnt = np.zeros(B, np.int32)
+    ctx = None if context_lens is None else _c(context_lens, np.int32).copy()
+    _L().orc_spec_verify_sample(_p(pp), _p(qq), _p(d), _p(ua), _p(us), B, K, V, _p(out), _p(cnt), _p(ctx))
+    out[np.arange(K + 1)[None, :] >= cnt[:, None]] = -1
+    return out, cnt, ctx
