@@ -12,6 +12,11 @@
  *   quant_fp8_rowwise  BF16 W -> FP8 E4M3 codes + per-output-row fp32 scales.
  *   quant_int4_g128  BF16 W -> INT4 codes + per-group bf16 scales and zeros.
  *
+ * and the step after the verify forward:
+ *
+ *   spec_verify_greedy / spec_verify_sample  accept a speculative draft
+ *                    block and invalidate the rejected KV tail.
+ *
  * Sources (web pages):
  *   [MTC]  "降低每個 Token 的生成成本" (Making each token cheaper), optiverse-tech.com
  *   [LIF]  "LLM 推理是怎么变快的" (How LLM inference gets fast), random.sdx88.com
@@ -327,6 +332,67 @@ DQD_API dqd_status gqa_decode_attn_static_ws(const uint16_t* q, const uint16_t* 
                                      const int32_t* context_lens, int32_t max_context,
                                      int32_t b, int32_t w, int32_t hq, int32_t hkv, int32_t d,
                                      float softmax_scale, uint16_t* out, dqd_stream stream);
+
+/* ------------------------------------------------------------------------
+ * spec_verify_greedy — greedy verify of a speculative draft block, with
+ * KV-tail invalidation (the step right after the target's verify forward).
+ *
+ * Source: [ATC, Algorithm 1 "贪心验证及状态回退" (greedy verify and state
+ * rollback)]: compare each draft with the target's greedy prediction from
+ * the first position, stop at the first mismatch, keep the matched prefix,
+ * add the target's token (the correction, or the extra token when every
+ * draft matched), invalidate the KV behind the accepted boundary; the
+ * correction token is the next round's input.
+ * Per request r, with verify width w = k + 1 (position 0 is the round's input
+ * token, positions 1..k the drafts d_1..d_k):
+ *   t_i       = argmax_v logits[r][i][v]   (ties: the smallest token id)
+ *   a         = number of leading i with d_{i+1} == t_i   (0 <= a <= k)
+ *   out[r][i] = t_i for every i; the round emits out[r][0 .. a]
+ *   count[r]  = a + 1
+ *   context_lens[r] -= k - a     (when context_lens is not NULL: the w verify
+ *                                 tokens sit at the end of the cache; the
+ *                                 rejected drafts' KV becomes invalid)
+ * A draft id outside [0, vocab) never matches.
+ *
+ * logits_bf16: [b][w][vocab] (device), not NaN; draft: int32 [b][w-1]
+ * (device; may be NULL when w == 1); out_tokens: int32 [b][w] (device);
+ * out_count: int32 [b] (device); context_lens: int32 [b] (device, in/out)
+ * or NULL.
+ * Requirements: b >= 1, 1 <= w <= 1024, 1 <= vocab < 2^31, logits 16-byte
+ * aligned, int32 buffers 4-byte aligned.
+ * ---------------------------------------------------------------------- */
+DQD_API dqd_status spec_verify_greedy(const uint16_t* logits_bf16, int32_t b, int32_t w,
+                              int64_t vocab, const int32_t* draft, int32_t* out_tokens,
+                              int32_t* out_count, int32_t* context_lens, dqd_stream stream);
+
+/* ------------------------------------------------------------------------
+ * spec_verify_sample — speculative sampling accept / resample.
+ *
+ * Source: [CS10 §6 "推测采样" (speculative sampling)]: draft token x is
+ * accepted with probability min(1, q(x)/p(x)); at the first rejection one
+ * token is drawn from norm(max(q - p, 0)) and the rest of the draft is
+ * dropped; when all k drafts are accepted one more token is drawn from the
+ * target's distribution at position k+1. The output is then distributed
+ * exactly as the target's q.
+ * The random numbers are inputs: draft i is accepted iff
+ * u_accept[r][i] * p(x) < q(x) (binary32); the one drawn token is the smallest
+ * y with sum_{z<=y} r(z) > u_sample[r] * sum_z r(z) (sums in double), with
+ * r = max(q - p, 0) (binary32 difference) after a rejection and r = q for the
+ * extra token; a residual that sums to 0 (through rounding only) falls back
+ * to q. out_tokens[r][0 .. j-1] = accepted drafts, out_tokens[r][j] = drawn
+ * token, count[r] = j + 1, context_lens[r] -= k - j.
+ *
+ * p_draft: f32 [b][k][vocab]; q_target: f32 [b][k+1][vocab]; draft: int32
+ * [b][k]; u_accept: f32 [b][k] in [0, 1); u_sample: f32 [b] in [0, 1) (all
+ * device). out_tokens: int32 [b][k+1]; out_count: int32 [b]; context_lens as
+ * above. Requirements: b >= 1, 0 <= k <= 1023, 1 <= vocab < 2^31; p, q
+ * non-negative and finite; 4-byte aligned pointers.
+ * ---------------------------------------------------------------------- */
+DQD_API dqd_status spec_verify_sample(const float* p_draft, const float* q_target,
+                              const int32_t* draft, const float* u_accept,
+                              const float* u_sample, int32_t b, int32_t k, int64_t vocab,
+                              int32_t* out_tokens, int32_t* out_count,
+                              int32_t* context_lens, dqd_stream stream);
 
 #ifdef __cplusplus
 }

@@ -170,6 +170,46 @@ dqd_status quant_int4_g128(const uint16_t* w_bf16, int64_t n, int64_t k, uint8_t
                       "quant_int4_g128 launch");
 }
 
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+dqd_status spec_verify_greedy(const uint16_t* logits_bf16, int32_t b, int32_t w, int64_t vocab,
+                              const int32_t* draft, int32_t* out_tokens, int32_t* out_count,
+                              int32_t* context_lens, dqd_stream stream) {
+  g_last_error.clear();
+  if (b < 1 || w < 1 || w > 1024 || vocab < 1 || vocab > INT32_MAX)
+    return fail(DQD_ERR_INVALID_ARG, "spec_verify_greedy needs b >= 1, 1 <= w <= 1024, 1 <= vocab < 2^31");
+  if ((int64_t)b * w > INT32_MAX) return fail(DQD_ERR_UNSUPPORTED, "spec_verify_greedy: b * w too large");
+  if (!logits_bf16 || !aligned16(logits_bf16) || !out_tokens || !aligned4(out_tokens) || !out_count ||
+      !aligned4(out_count) || (w > 1 && (!draft || !aligned4(draft))) || (context_lens && !aligned4(context_lens)))
+    return fail(DQD_ERR_INVALID_ARG, "spec_verify_greedy: NULL or misaligned pointer");
+  return check_launch(dqd::launch_spec_verify_greedy(logits_bf16, b, w, vocab, draft, out_tokens, out_count,
+                                                     context_lens, reinterpret_cast<cudaStream_t>(stream)),
+                      "spec_verify_greedy launch");
+}
+
+dqd_status spec_verify_sample(const float* p_draft, const float* q_target, const int32_t* draft,
+                              const float* u_accept, const float* u_sample, int32_t b, int32_t k, int64_t vocab,
+                              int32_t* out_tokens, int32_t* out_count, int32_t* context_lens,
+                              dqd_stream stream) {
+  g_last_error.clear();
+  if (b < 1 || k < 0 || k > 1023 || vocab < 1 || vocab > INT32_MAX)
+    return fail(DQD_ERR_INVALID_ARG, "spec_verify_sample needs b >= 1, 0 <= k <= 1023, 1 <= vocab < 2^31");
+  const void* always[] = {q_target, u_sample, out_tokens, out_count};
+  for (const void* p : always)
+    if (!p || !aligned4(p)) return fail(DQD_ERR_INVALID_ARG, "spec_verify_sample: NULL or misaligned pointer");
+  if (k > 0) {
+    const void* drafts[] = {p_draft, draft, u_accept};
+    for (const void* p : drafts)
+      if (!p || !aligned4(p)) return fail(DQD_ERR_INVALID_ARG, "spec_verify_sample: NULL or misaligned pointer");
+  }
+  if (context_lens && !aligned4(context_lens))
+    return fail(DQD_ERR_INVALID_ARG, "spec_verify_sample: misaligned context_lens");
+  return check_launch(dqd::launch_spec_verify_sample(p_draft, q_target, draft, u_accept, u_sample, b, k, vocab,
+                                                     out_tokens, out_count, context_lens,
+                                                     reinterpret_cast<cudaStream_t>(stream)),
+                      "spec_verify_sample launch");
+}
+
 dqd_status dq_gemm_workspace_bytes(const dqd_weight* w, int64_t m, size_t* bytes) {
   g_last_error.clear();
   if (!bytes) return fail(DQD_ERR_INVALID_ARG, "bytes is NULL");

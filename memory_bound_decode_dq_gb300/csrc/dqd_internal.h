@@ -158,4 +158,13 @@ cudaError_t launch_quant_fp8(const uint16_t* w, int64_t n, int64_t k, uint8_t* c
 cudaError_t launch_quant_int4(const uint16_t* w, int64_t n, int64_t k, uint8_t* codes, uint16_t* scales,
                               uint8_t* zeros, cudaStream_t s);
 
+// --------------------------------------------------------------- verify --
+
+cudaError_t launch_spec_verify_greedy(const uint16_t* logits, int b, int w, int64_t vocab, const int32_t* draft,
+                                      int32_t* out, int32_t* count, int32_t* ctx, cudaStream_t s);
+
+cudaError_t launch_spec_verify_sample(const float* p, const float* q, const int32_t* draft, const float* u_accept,
+                                      const float* u_sample, int b, int k, int64_t vocab, int32_t* out,
+                                      int32_t* count, int32_t* ctx, cudaStream_t s);
+
 }  // namespace dqd

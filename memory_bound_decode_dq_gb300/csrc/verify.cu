@@ -1,0 +1,247 @@
+// Speculative verify: the step right after the target's verify forward.
+//
+// Sources: "AcceptedTokens 阅读笔记", Algorithm 1 (greedy verify and state
+// rollback): compare each draft with the target's greedy prediction from the
+// first position, stop at the first mismatch, emit the matched prefix plus
+// the target's own token, invalidate the rejected tail of the KV cache;
+// "第 10 讲：推理" §6 (speculative sampling): accept draft x with probability
+// min(1, q(x)/p(x)); on the first rejection draw from norm(max(q - p, 0));
+// when every draft is accepted draw one more token from the target.
+//
+// Greedy: spec_argmax_kernel (one CTA per verify position, vocabulary
+// streamed with 16-byte loads, ties to the smallest token id) writes the
+// target's predictions t_i; spec_accept_kernel (one thread per request,
+// launched as a programmatic dependent) counts the leading matches a. The
+// round's output is t_0 .. t_a: accepted drafts equal the predictions they
+// were compared with.
+//
+// Sampling: spec_sample_kernel, one CTA per request. Thread 0 walks the
+// drafts (the test u * p(x) < q(x) in binary32); the CTA then draws the one
+// sampled token by inverse CDF over the vocabulary, with fp64 partial sums
+// per thread, a block-wide scan, and a sequential walk inside the thread
+// whose range holds the crossing.
+#include "dqd_device.cuh"
+#include "dqd_internal.h"
+
+#include <cmath>
+
+namespace dqd {
+namespace {
+
+constexpr int kArgmaxThreads = 512;
+constexpr int kSampleThreads = 512;
+
+// (value, index) with the larger value, the smaller index on ties.
+__device__ __forceinline__ void arg_better(float& v, int& i, float ov, int oi) {
+  if (ov > v || (ov == v && oi < i)) {
+    v = ov;
+    i = oi;
+  }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__global__ void __launch_bounds__(kArgmaxThreads)
+spec_argmax_kernel(const uint16_t* __restrict__ logits, int64_t vocab, int32_t* __restrict__ out) {
+  grid_dependency_wait();  // the logits come from the previous kernel
+  allow_dependent_launch();
+  const int64_t row = blockIdx.x;
+  const uint16_t* lr = logits + row * vocab;
+  float bv = -INFINITY;
+  int bi = 0x7FFFFFFF;
+  if ((vocab & 7) == 0) {
+    // 16-byte loads, four in flight per thread
+    const uint4* v4 = reinterpret_cast<const uint4*>(lr);
+    const int64_t n4 = vocab / 8;
+    int64_t u = threadIdx.x;
+    for (; u + 3 * kArgmaxThreads < n4; u += 4 * kArgmaxThreads) {
+      uint4 x[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[j] = ldg_stream(v4 + u + j * kArgmaxThreads);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int base = (int)(8 * (u + j * kArgmaxThreads));
+        const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          arg_better(bv, bi, bf16_lo(w[e]), base + 2 * e);
+          arg_better(bv, bi, bf16_hi(w[e]), base + 2 * e + 1);
+        }
+      }
+    }
+    for (; u < n4; u += kArgmaxThreads) {
+      const uint4 x = ldg_stream(v4 + u);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        arg_better(bv, bi, bf16_lo(w[e]), (int)(8 * u) + 2 * e);
+        arg_better(bv, bi, bf16_hi(w[e]), (int)(8 * u) + 2 * e + 1);
+      }
+    }
+  } else {
+    for (int64_t j = threadIdx.x; j < vocab; j += kArgmaxThreads)
+      arg_better(bv, bi, __uint_as_float((uint32_t)lr[j] << 16), (int)j);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    arg_better(bv, bi, ov, oi);
+  }
+  __shared__ float sv[kArgmaxThreads / 32];
+  __shared__ int si[kArgmaxThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sv[warp] = bv;
+    si[warp] = bi;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    bv = lane < kArgmaxThreads / 32 ? sv[lane] : -INFINITY;
+    bi = lane < kArgmaxThreads / 32 ? si[lane] : 0x7FFFFFFF;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      arg_better(bv, bi, ov, oi);
+    }
+    // a row of -inf only: the first token
+    if (lane == 0) out[row] = bi == 0x7FFFFFFF ? 0 : bi;
+  }
+}
+
+__global__ void spec_accept_kernel(const int32_t* __restrict__ draft, int32_t* __restrict__ out,
+                                   int32_t* __restrict__ count, int32_t* __restrict__ ctx, int b, int w) {
+  grid_dependency_wait();  // the predictions come from spec_argmax_kernel
+  allow_dependent_launch();
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= b) return;
+  int a = 0;
+  while (a < w - 1 && draft[(int64_t)r * (w - 1) + a] == out[(int64_t)r * w + a]) ++a;
+  count[r] = a + 1;
+  if (ctx) ctx[r] -= (w - 1) - a;
+}
+
+// Residual mass of token y: max(q - p, 0) in binary32, or q itself.
+__device__ __forceinline__ float residual(const float* q, const float* p, int64_t y) {
+  return p ? fmaxf(q[y] - p[y], 0.f) : q[y];
+}
+
+// Inverse CDF over one vocabulary row, by the whole CTA: the smallest y with
+// sum_{z<=y} r(z) > u * sum_z r(z), sums in fp64. Thread t owns a contiguous
+// range of the vocabulary; a scan of the thread sums gives every range its
+// bounds [lo, hi), built so that hi of one thread is bitwise lo of the next,
+// hence exactly one thread holds the threshold and walks its range. Returns
+// -1 when the total is not positive.
+__device__ int64_t inverse_cdf(const float* q, const float* p, int64_t vocab, double u, double* sred,
+                               long long* spick) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = kSampleThreads / 32;
+  const int64_t chunk = (vocab + kSampleThreads - 1) / kSampleThreads;
+  const int64_t y0 = min(vocab, tid * chunk), y1 = min(vocab, y0 + chunk);
+  double part = 0.0;
+  for (int64_t y = y0; y < y1; ++y) part += (double)residual(q, p, y);
+  double incl = part;  // inclusive scan inside the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  double excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.0;
+  if (lane == 31) sred[warp] = incl;
+  if (tid == 0) *spick = -1;
+  __syncthreads();
+  if (warp == 0) {
+    double wv = lane < NW ? sred[lane] : 0.0;  // inclusive scan of the warp totals
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double v = __shfl_up_sync(0xffffffffu, wv, o);
+      if (lane >= o) wv += v;
+    }
+    if (lane < NW) sred[NW + lane] = wv;
+  }
+  __syncthreads();
+  const double total = sred[2 * NW - 1];
+  const double wo = warp > 0 ? sred[NW + warp - 1] : 0.0;
+  const double lo = wo + excl;
+  const double hi = lane == 31 ? sred[NW + warp] : wo + incl;
+  if (total > 0.0) {
+    const double thr = u * total;
+    if (lo <= thr && thr < hi) {
+      double acc = lo;
+      int64_t pick = -1, last = -1;
+      for (int64_t y = y0; y < y1; ++y) {
+        const float r = residual(q, p, y);
+        if (r > 0.f) last = y;
+        acc += (double)r;
+        if (acc > thr) {
+          pick = y;
+          break;
+        }
+      }
+      *spick = pick >= 0 ? pick : last;  // last: the walk's rounding stayed below thr
+    }
+  }
+  __syncthreads();
+  const long long pick = *spick;
+  __syncthreads();
+  return total > 0.0 ? (int64_t)pick : -1;
+}
+
+__global__ void __launch_bounds__(kSampleThreads)
+spec_sample_kernel(const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ draft,
+                   const float* __restrict__ u_accept, const float* __restrict__ u_sample, int K, int64_t vocab,
+                   int32_t* __restrict__ out, int32_t* __restrict__ count, int32_t* __restrict__ ctx) {
+  grid_dependency_wait();
+  allow_dependent_launch();
+  const int64_t b = blockIdx.x;
+  __shared__ int s_j;
+  __shared__ double sred[2 * (kSampleThreads / 32)];
+  __shared__ long long spick;
+  if (threadIdx.x == 0) {
+    int j = 0;
+    while (j < K) {
+      const int32_t x = draft[b * K + j];
+      if (x < 0 || x >= vocab) break;
+      const float px = p[(b * K + j) * vocab + x], qx = q[(b * (K + 1) + j) * vocab + x];
+      if (!(u_accept[b * K + j] * px < qx)) break;
+      out[b * (K + 1) + j] = x;
+      ++j;
+    }
+    s_j = j;
+  }
+  __syncthreads();
+  const int j = s_j;
+  const float* qrow = q + (b * (K + 1) + j) * vocab;
+  const float* prow = j < K ? p + (b * K + j) * vocab : nullptr;
+  const double u = (double)u_sample[b];
+  int64_t y = inverse_cdf(qrow, prow, vocab, u, sred, &spick);
+  if (y < 0 && prow) y = inverse_cdf(qrow, nullptr, vocab, u, sred, &spick);  // residual lost to rounding
+  if (threadIdx.x == 0) {
+    out[b * (K + 1) + j] = (int32_t)(y < 0 ? 0 : y);
+    count[b] = j + 1;
+    if (ctx) ctx[b] -= K - j;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_spec_verify_greedy(const uint16_t* logits, int b, int w, int64_t vocab, const int32_t* draft,
+                                      int32_t* out, int32_t* count, int32_t* ctx, cudaStream_t s) {
+  cudaError_t e = launch_pdl(spec_argmax_kernel, dim3((unsigned)((int64_t)b * w)), dim3(kArgmaxThreads), 0, s,
+                             logits, vocab, out);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(spec_accept_kernel, dim3((unsigned)((b + 127) / 128)), dim3(128), 0, s, draft, out, count, ctx,
+                    b, w);
+}
+
+cudaError_t launch_spec_verify_sample(const float* p, const float* q, const int32_t* draft, const float* u_accept,
+                                      const float* u_sample, int b, int k, int64_t vocab, int32_t* out,
+                                      int32_t* count, int32_t* ctx, cudaStream_t s) {
+  return launch_pdl(spec_sample_kernel, dim3((unsigned)b), dim3(kSampleThreads), 0, s, p, q, draft, u_accept,
+                    u_sample, k, vocab, out, count, ctx);
+}
+
+}  // namespace dqd

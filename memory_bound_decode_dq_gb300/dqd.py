@@ -49,6 +49,8 @@ _SIGS = {
     "pack_int4_g128": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _P, _P, _P]),
     "quant_fp8_rowwise": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
     "quant_int4_g128": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "spec_verify_greedy": (ctypes.c_int, [_P, _I32, _I32, _I64, _P, _P, _P, _P, _P]),
+    "spec_verify_sample": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _P, _P, _P, _P]),
     "dq_gemm_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(_WeightDesc), _I64, ctypes.POINTER(_SZ)]),
     "dq_gemm": (ctypes.c_int, [ctypes.POINTER(_WeightDesc), _P, _I64, _P, _P, _SZ, _P]),
     "gqa_decode_attn_workspace_bytes": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32,
@@ -358,3 +360,55 @@ def gqa_decode_attn_fp8kv(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.T
                                       _stream(stream)),
            "gqa_decode_attn_fp8kv")
     return out
+
+
+# ---------------------------------------------------------------- verify ----
+
+def spec_verify_greedy(logits: torch.Tensor, draft: torch.Tensor | None,
+                       context_lens: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                       count: torch.Tensor | None = None, stream=None):
+    """Greedy verify. logits bf16 [b, w, vocab]; draft int32 [b, w-1];
+    context_lens int32 [b] updated in place (None: left alone). Returns
+    (out int32 [b, w] = the target's predictions, count int32 [b]): the
+    round emits out[r, :count[r]]."""
+    _need(logits, "logits", _B16)
+    dev = logits.device
+    b, w, vocab = logits.shape
+    if w > 1:
+        _need(draft, "draft", _I32T, dev)
+        if tuple(draft.shape) != (b, w - 1):
+            raise ValueError("spec_verify_greedy: draft must be [b, w-1]")
+    if context_lens is not None:
+        _need(context_lens, "context_lens", _I32T, dev)
+    out = torch.empty((b, w), dtype=torch.int32, device=dev) if out is None else out
+    count = torch.empty((b,), dtype=torch.int32, device=dev) if count is None else count
+    _need(out, "out", _I32T, dev)
+    _need(count, "count", _I32T, dev)
+    _check(_lib.spec_verify_greedy(_ptr(logits), b, w, vocab, _ptr(draft) if w > 1 else None, _ptr(out),
+                                   _ptr(count), _ptr(context_lens), _stream(stream)), "spec_verify_greedy")
+    return out, count
+
+
+def spec_verify_sample(p: torch.Tensor, q: torch.Tensor, draft: torch.Tensor, u_accept: torch.Tensor,
+                       u_sample: torch.Tensor, context_lens: torch.Tensor | None = None, stream=None):
+    """Speculative sampling. p f32 [b, k, vocab]; q f32 [b, k+1, vocab];
+    draft int32 [b, k]; u_accept f32 [b, k]; u_sample f32 [b]. Returns
+    (out int32 [b, k+1], count int32 [b]); context_lens updated in place."""
+    _need(q, "q", _F32)
+    dev = q.device
+    b, k1, vocab = q.shape
+    k = k1 - 1
+    for t, name in ((p, "p"), (u_accept, "u_accept"), (u_sample, "u_sample")):
+        _need(t, name, _F32, dev)
+    _need(draft, "draft", _I32T, dev)
+    if tuple(p.shape) != (b, k, vocab) or tuple(draft.shape) != (b, k) or tuple(u_accept.shape) != (b, k) \
+            or tuple(u_sample.shape) != (b,):
+        raise ValueError("spec_verify_sample: shapes must be p [b,k,V], draft/u_accept [b,k], u_sample [b]")
+    if context_lens is not None:
+        _need(context_lens, "context_lens", _I32T, dev)
+    out = torch.full((b, k + 1), -1, dtype=torch.int32, device=dev)
+    count = torch.empty((b,), dtype=torch.int32, device=dev)
+    _check(_lib.spec_verify_sample(_ptr(p), _ptr(q), _ptr(draft), _ptr(u_accept), _ptr(u_sample), b, k, vocab,
+                                   _ptr(out), _ptr(count), _ptr(context_lens), _stream(stream)),
+           "spec_verify_sample")
+    return out, count
