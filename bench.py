@@ -227,6 +227,23 @@ def build_calls(wl, dev, dqd):
                                             kv_bytes_per_element=1 if a.kv_fp8 else 2),
                           bounds.attn_flops(ctx, a.width, a.hq, a.d), attn_call(kp, vp), 2 if need else 1, clone))
         io.append((a.name, [q, table_t, ctx_t], [out]))
+    for v in getattr(wl, "verifies", ()):
+        import numpy as np
+        logits = synth.normal_bf16(wl.seed, v.name + ".logits", (v.batch, v.width, v.vocab), device=dev)
+        draft = torch.from_numpy(synth.rng(wl.seed, v.name + ".draft").integers(
+            0, v.vocab, (v.batch, v.width - 1)).astype(np.int32)).to(dev)
+        ctx_v = torch.full((v.batch,), 1 << 30, dtype=torch.int32, device=dev)  # updated in place
+        vout = torch.empty((v.batch, v.width), dtype=torch.int32, device=dev)
+        vcnt = torch.empty((v.batch,), dtype=torch.int32, device=dev)
+
+        def verify_call(lg, draft=draft, ctx_v=ctx_v, vout=vout, vcnt=vcnt):
+            return lambda: dqd.spec_verify_greedy(lg, draft, ctx_v, out=vout, count=vcnt)
+
+        def vclone(lg=logits, verify_call=verify_call):
+            return verify_call(lg.clone())
+        calls.append(Call(v.name, "spec_verify_greedy", bounds.verify_bytes(v.batch, v.width, v.vocab), 0.0,
+                          verify_call(logits), 2, vclone))
+        io.append((v.name, [logits, draft], [vout, vcnt]))
     return calls, io
 
 
@@ -462,7 +479,8 @@ class OracleSample:
         self.oracle = oracle
         rng = np.random.default_rng(seed)
         costs = [c.m * c.n * c.k for c in wl.gemms] + \
-                [sum(a.context) * a.width * a.hq * a.d * 2 for a in wl.attns]
+                [sum(a.context) * a.width * a.hq * a.d * 2 for a in wl.attns] + \
+                [v.batch * v.width * v.vocab for v in getattr(wl, "verifies", ())]
         rate = 1.5e8 * max(1, oracle.num_threads())  # oracle multiply-adds per second, roughly
         self.frac = frac = min(1.0, budget_s * rate / float(sum(costs)))
         self.jobs, self.covered = [], 0.0
@@ -504,6 +522,13 @@ class OracleSample:
             per_row = bounds.attn_bytes(a.context, a.width, a.hq, a.hkv, a.d,
                                         kv_bytes_per_element=1 if a.kv_fp8 else 2) / rows_all
             self.covered += per_row * rel * nrows
+        for v in getattr(wl, "verifies", ()):
+            # one request's verify block (its w logit rows), one in ``reqs``
+            reqs = max(1, int(round(v.batch * frac)))
+            lg = synth.normal_bf16(seed, v.name + ".cpu", (reqs, v.width, v.vocab))
+            dr = rng.integers(0, v.vocab, (reqs, v.width - 1)).astype(np.int32)
+            self.jobs.append(lambda lg=lg, dr=dr: oracle.spec_verify_greedy(lg, dr))
+            self.covered += bounds.verify_bytes(v.batch, v.width, v.vocab) * reqs / v.batch
         self.threads = oracle.num_threads()
         self.desc = (f"oracle on a random {frac:.4g} of every projection's output rows and on "
                      f"sampled query rows of one (sequence, kv head) per attention call; "

@@ -68,6 +68,12 @@ def attn_bytes(context_lens, w: int, hq: int, hkv: int, d: int = 128, block: int
     return float(kv + qo + table)
 
 
+def verify_bytes(batch: int, width: int, vocab: int) -> float:
+    """Greedy verify: the target's bf16 logits, the drafts, the predictions,
+    the counts and the context lengths (read and written)."""
+    return float(2 * batch * width * vocab + 4 * batch * (width - 1) + 4 * batch * width + 12 * batch)
+
+
 def attn_flops(context_lens, w: int, hq: int, d: int = 128) -> float:
     """QK^T and PV over the visible keys (causal inside the verify block)."""
     total = 0

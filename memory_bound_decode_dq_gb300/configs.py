@@ -44,11 +44,21 @@ class AttnCase:
 
 
 @dataclass(frozen=True)
+class VerifyCase:
+    """Greedy verify of a draft block: target logits [batch, width, vocab] bf16."""
+    name: str
+    batch: int
+    width: int
+    vocab: int
+
+
+@dataclass(frozen=True)
 class Workload:
     name: str
     seed: int
     gemms: tuple = field(default_factory=tuple)
     attns: tuple = field(default_factory=tuple)
+    verifies: tuple = field(default_factory=tuple)
 
 
 def _ctx_uniform(seed: int, batch: int, lo: int, hi: int) -> tuple:
@@ -87,11 +97,15 @@ def dense70b_b32() -> Workload:
                     attns=(AttnCase("attn_64_8_b32_ctx2048", 32, 1, 64, 8, (2048,) * 32),))
 
 
+LLAMA3_8B_VOCAB = 128256
+
+
 def verify_8b() -> Workload:
     """Speculative verify on the 8B shapes: INT4 g128 projections at
-    M = batch x (drafts + 1) for drafts in {5, 15} and batch in {1, 64}, and
-    verify attention of width drafts + 1 over contexts uniform on [512, 4096]."""
-    g, a = [], []
+    M = batch x (drafts + 1) for drafts in {5, 15} and batch in {1, 64},
+    verify attention of width drafts + 1 over contexts uniform on [512, 4096],
+    and the greedy accept step over the target's logits (vocabulary 128256)."""
+    g, a, v = [], [], []
     for batch in (1, 64):
         for width in (6, 16):
             m = batch * width
@@ -99,7 +113,8 @@ def verify_8b() -> Workload:
                 g.append(GemmCase(f"{name}_int4_m{m}", W_INT4_G128, m, n, k))
             a.append(AttnCase(f"attn_verify_b{batch}_w{width}", batch, width, 32, 8,
                               _ctx_uniform(3, batch, 512, 4096)))
-    return Workload("verify_8b_int4", 3, gemms=tuple(g), attns=tuple(a))
+            v.append(VerifyCase(f"accept_greedy_b{batch}_w{width}", batch, width, LLAMA3_8B_VOCAB))
+    return Workload("verify_8b_int4", 3, gemms=tuple(g), attns=tuple(a), verifies=tuple(v))
 
 
 def longctx_70b_b8() -> Workload:

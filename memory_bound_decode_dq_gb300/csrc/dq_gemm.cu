@@ -258,20 +258,6 @@ __device__ __forceinline__ void compute_stage(float (&acc)[MT][4], uint32_t slot
   }
 }
 
-// Cluster-wide barrier over every thread of every CTA of the cluster, with
-// release/acquire ordering of shared-memory writes.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-// fp32 load from the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t saddr, uint32_t rank) {
-  uint32_t remote;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
-
 // Epilogue shared by the dq_gemm kernels (every thread of the CTA calls it):
 // bf16 output, or fp32 split-K partials reduced by the last-arriving CTA.
 template <int WT, int MT, int WARPS, int THREADS>

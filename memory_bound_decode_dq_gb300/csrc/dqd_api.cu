@@ -182,8 +182,11 @@ dqd_status spec_verify_greedy(const uint16_t* logits_bf16, int32_t b, int32_t w,
   if (!logits_bf16 || !aligned16(logits_bf16) || !out_tokens || !aligned4(out_tokens) || !out_count ||
       !aligned4(out_count) || (w > 1 && (!draft || !aligned4(draft))) || (context_lens && !aligned4(context_lens)))
     return fail(DQD_ERR_INVALID_ARG, "spec_verify_greedy: NULL or misaligned pointer");
+  int sms = 0;
+  dqd_status st = sm_count(&sms);
+  if (st != DQD_OK) return st;
   return check_launch(dqd::launch_spec_verify_greedy(logits_bf16, b, w, vocab, draft, out_tokens, out_count,
-                                                     context_lens, reinterpret_cast<cudaStream_t>(stream)),
+                                                     context_lens, sms, reinterpret_cast<cudaStream_t>(stream)),
                       "spec_verify_greedy launch");
 }
 

@@ -194,6 +194,28 @@ __device__ __forceinline__ uint32_t fp8_hi_to_bf16x2(uint32_t u) {
   return fp8_pair_to_bf16x2(u, 0xB3A2u);
 }
 
+// ------------------------------------------------- thread-block clusters ----
+
+// Cluster-wide barrier over every thread of every CTA of the cluster, with
+// release/acquire ordering of shared-memory writes.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Loads from the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t saddr, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t saddr, uint32_t rank) {
+  uint32_t remote, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 // ------------------------------------------- programmatic dependent launch ----
 // Kernels are launched so that the next kernel on the stream may start while
 // this one drains. Every kernel waits (griddepcontrol.wait, a hardware wait

@@ -52,6 +52,28 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// As launch_pdl, with CTAs grouped in thread-block clusters of cluster_x CTAs
+// along x (grid.x must be a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster_x(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 enum WType { kBF16 = 0, kFP8 = 1, kINT4 = 2 };
 
 // Tiled TMA tensor map over `base` (rank <= 5; dims innermost first; strides
@@ -161,7 +183,7 @@ cudaError_t launch_quant_int4(const uint16_t* w, int64_t n, int64_t k, uint8_t* 
 // --------------------------------------------------------------- verify --
 
 cudaError_t launch_spec_verify_greedy(const uint16_t* logits, int b, int w, int64_t vocab, const int32_t* draft,
-                                      int32_t* out, int32_t* count, int32_t* ctx, cudaStream_t s);
+                                      int32_t* out, int32_t* count, int32_t* ctx, int num_sms, cudaStream_t s);
 
 cudaError_t launch_spec_verify_sample(const float* p, const float* q, const int32_t* draft, const float* u_accept,
                                       const float* u_sample, int b, int k, int64_t vocab, int32_t* out,

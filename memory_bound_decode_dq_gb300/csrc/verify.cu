@@ -8,9 +8,12 @@
 // min(1, q(x)/p(x)); on the first rejection draw from norm(max(q - p, 0));
 // when every draft is accepted draw one more token from the target.
 //
-// Greedy: spec_argmax_kernel (one CTA per verify position, vocabulary
-// streamed with 16-byte loads, ties to the smallest token id) writes the
-// target's predictions t_i; spec_accept_kernel (one thread per request,
+// Greedy: spec_argmax_kernel (a cluster of S CTAs per verify position, each
+// streaming a contiguous share of the vocabulary with 16-byte loads; the
+// shares' (value, index) pairs meet in rank 0 through distributed shared
+// memory; ties go to the smallest token id) writes the target's predictions
+// t_i; S grows when there are few positions, so that small batches still
+// spread over the SMs; spec_accept_kernel (one thread per request,
 // launched as a programmatic dependent) counts the leading matches a. The
 // round's output is t_0 .. t_a: accepted drafts equal the predictions they
 // were compared with.
@@ -46,15 +49,18 @@ __global__ void __launch_bounds__(kArgmaxThreads)
 spec_argmax_kernel(const uint16_t* __restrict__ logits, int64_t vocab, int32_t* __restrict__ out) {
   grid_dependency_wait();  // the logits come from the previous kernel
   allow_dependent_launch();
-  const int64_t row = blockIdx.x;
+  const int64_t row = blockIdx.y;
+  const int S = gridDim.x, rank = blockIdx.x;  // the CTAs of one row form a cluster along x
   const uint16_t* lr = logits + row * vocab;
   float bv = -INFINITY;
   int bi = 0x7FFFFFFF;
   if ((vocab & 7) == 0) {
-    // 16-byte loads, four in flight per thread
+    // 16-byte loads, four in flight per thread, over this CTA's share
     const uint4* v4 = reinterpret_cast<const uint4*>(lr);
-    const int64_t n4 = vocab / 8;
-    int64_t u = threadIdx.x;
+    const int64_t units = vocab / 8;
+    const int64_t per = (units + S - 1) / S;
+    const int64_t n4 = min(units, (rank + 1) * per);
+    int64_t u = rank * per + threadIdx.x;
     for (; u + 3 * kArgmaxThreads < n4; u += 4 * kArgmaxThreads) {
       uint4 x[4];
 #pragma unroll
@@ -80,7 +86,9 @@ spec_argmax_kernel(const uint16_t* __restrict__ logits, int64_t vocab, int32_t* 
       }
     }
   } else {
-    for (int64_t j = threadIdx.x; j < vocab; j += kArgmaxThreads)
+    const int64_t per = (vocab + S - 1) / S;
+    const int64_t end = min(vocab, (rank + 1) * per);
+    for (int64_t j = rank * per + threadIdx.x; j < end; j += kArgmaxThreads)
       arg_better(bv, bi, __uint_as_float((uint32_t)lr[j] << 16), (int)j);
   }
 #pragma unroll
@@ -106,9 +114,23 @@ spec_argmax_kernel(const uint16_t* __restrict__ logits, int64_t vocab, int32_t* 
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       arg_better(bv, bi, ov, oi);
     }
-    // a row of -inf only: the first token
-    if (lane == 0) out[row] = bi == 0x7FFFFFFF ? 0 : bi;
+    if (lane == 0) {
+      sv[0] = bv;
+      si[0] = bi;
+    }
   }
+  if (S > 1) {
+    // rank 0 takes the best of the cluster's shares, in rank order
+    cluster_sync_all();
+    if (rank == 0 && threadIdx.x == 0) {
+      const uint32_t av = smem_addr(&sv[0]), ai = smem_addr(&si[0]);
+      for (int r = 1; r < S; ++r)
+        arg_better(bv, bi, ld_dsmem_f32(av, (uint32_t)r), (int)ld_dsmem_u32(ai, (uint32_t)r));
+    }
+    cluster_sync_all();  // peers stay alive until their shares have been read
+  }
+  // a row of -inf only: the first token
+  if (rank == 0 && threadIdx.x == 0) out[row] = bi == 0x7FFFFFFF ? 0 : bi;
 }
 
 __global__ void spec_accept_kernel(const int32_t* __restrict__ draft, int32_t* __restrict__ out,
@@ -228,10 +250,22 @@ spec_sample_kernel(const float* __restrict__ p, const float* __restrict__ q, con
 
 }  // namespace
 
+static int verify_argmax_split(int64_t rows, int64_t vocab, int num_sms) {
+  // up to 8 CTAs per row while the rows alone fill fewer than 2 CTAs per SM,
+  // each keeping at least 4096 logits
+  int S = 1;
+  while (S < 8 && rows * S < 2 * (int64_t)num_sms && vocab / (2 * S) >= 4096) S *= 2;
+  return S;
+}
+
 cudaError_t launch_spec_verify_greedy(const uint16_t* logits, int b, int w, int64_t vocab, const int32_t* draft,
-                                      int32_t* out, int32_t* count, int32_t* ctx, cudaStream_t s) {
-  cudaError_t e = launch_pdl(spec_argmax_kernel, dim3((unsigned)((int64_t)b * w)), dim3(kArgmaxThreads), 0, s,
-                             logits, vocab, out);
+                                      int32_t* out, int32_t* count, int32_t* ctx, int num_sms, cudaStream_t s) {
+  const int64_t rows = (int64_t)b * w;
+  const int S = verify_argmax_split(rows, vocab, num_sms);
+  cudaError_t e = S > 1 ? launch_pdl_cluster_x(spec_argmax_kernel, dim3((unsigned)S, (unsigned)rows),
+                                                dim3(kArgmaxThreads), 0, s, (unsigned)S, logits, vocab, out)
+                        : launch_pdl(spec_argmax_kernel, dim3(1, (unsigned)rows), dim3(kArgmaxThreads), 0, s,
+                                     logits, vocab, out);
   if (e != cudaSuccess) return e;
   return launch_pdl(spec_accept_kernel, dim3((unsigned)((b + 127) / 128)), dim3(128), 0, s, draft, out, count, ctx,
                     b, w);

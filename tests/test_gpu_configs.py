@@ -169,3 +169,32 @@ def test_int4_70b_fp8kv_attn(dev, dqd, case):
 @pytest.mark.parametrize("case", WORKLOADS["longctx_70b_b8_fp8kv"].attns, ids=lambda c: c.name)
 def test_longctx_fp8kv_attn(dev, dqd, case):
     check_attn(dqd, dev, case, WORKLOADS["longctx_70b_b8_fp8kv"].seed, max_groups=3)
+
+
+def check_verify(dqd, dev, case, seed, max_reqs=8):
+    """The bench's greedy verify call at full size: the logits are drawn on the
+    device, sampled requests are copied back for the oracle."""
+    import numpy as np
+    logits = synth.normal_bf16(seed, case.name + ".logits", (case.batch, case.width, case.vocab), device=dev)
+    draft_np = synth.rng(seed, case.name + ".draft").integers(0, case.vocab, (case.batch, case.width - 1))
+    draft_np = draft_np.astype(np.int32)
+    # make some drafts right: the first j_r follow the target's own predictions
+    t = logits.float().argmax(dim=2).cpu().numpy().astype(np.int32)
+    keep = np.random.default_rng(seed).integers(0, case.width, case.batch)
+    for r in range(case.batch):
+        draft_np[r, :keep[r]] = t[r, :keep[r]]
+    ctx = torch.full((case.batch,), 100000, dtype=torch.int32, device=dev)
+    out, cnt = dqd.spec_verify_greedy(logits, torch.from_numpy(draft_np).to(dev), ctx)
+    reqs = sample_rows(case.batch, max_reqs, seed)
+    lg = bits(logits[torch.as_tensor(reqs, device=dev)].contiguous())
+    rout, rcnt, rctx = oracle.spec_verify_greedy(lg, draft_np[reqs], np.full(len(reqs), 100000, np.int32))
+    assert np.array_equal(cnt.cpu().numpy()[reqs], rcnt)
+    assert np.array_equal(ctx.cpu().numpy()[reqs], rctx)
+    o = out.cpu().numpy()[reqs]
+    k = np.arange(case.width)[None, :] < rcnt[:, None]
+    assert np.array_equal(o[k], rout[k])
+
+
+@pytest.mark.parametrize("case", WORKLOADS["verify_8b"].verifies, ids=lambda c: c.name)
+def test_verify_accept(dev, dqd, case):
+    check_verify(dqd, dev, case, WORKLOADS["verify_8b"].seed)
