@@ -480,6 +480,66 @@ ORC_EXPORT int orc_gqa_decode_attn_fp8kv(const uint16_t* q, const uint8_t* k_poo
 }
 
 /* ------------------------------------------------------------------------ */
+/* RoPE and KV append [CS10 §2.2-2.3: for each new token compute q, k, v,     */
+/* rotate q and k at the token's global position (start .. end-1, not from    */
+/* 0), append k and v to the cache, then attend]. Rotary embedding in the     */
+/* pairwise form: dims (2i, 2i+1) of a head rotate by angle pos * theta_i,    */
+/* theta_i = base^(-2i/d), i.e. [x0', x1'] = [x0 c - x1 s, x0 s + x1 c].      */
+/* ------------------------------------------------------------------------ */
+
+/* Rotates one head vector x[d] (double) in place at position pos. */
+static void rope_head(double* x, int64_t d, double pos, double base) {
+  for (int64_t i = 0; i < d / 2; ++i) {
+    const double theta = pow(base, -2.0 * (double)i / (double)d);
+    const double a = pos * theta, c = cos(a), s = sin(a);
+    const double x0 = x[2 * i], x1 = x[2 * i + 1];
+    x[2 * i] = x0 * c - x1 * s;
+    x[2 * i + 1] = x0 * s + x1 * c;
+  }
+}
+
+ORC_EXPORT void orc_rope(double* x, int64_t rows, int64_t d, const double* pos, double base) {
+  for (int64_t r = 0; r < rows; ++r) rope_head(x + r * d, d, pos[r], base);
+}
+
+/* qkv: bf16 [B*W][(Hq + 2*Hkv) * D], token (b, i) in row b*W + i, heads in the
+ * order q_0..q_{Hq-1}, k_0..k_{Hkv-1}, v_0..v_{Hkv-1}. Token (b, i) sits at
+ * position ctx[b] - W + i. Outputs (double): q_out [B*W][Hq][D] rotated,
+ * k_out, v_out [B*W][Hkv][D] (k rotated, v as is), and slot [B*W]: the pool
+ * row (phys * Hkv * 16 + pos % 16, to be offset by head * 16) the token's k
+ * and v are appended to, or -1 for a position below 0. */
+ORC_EXPORT int orc_rope_kv_append(const uint16_t* qkv, int64_t B, int64_t W, int64_t Hq,
+                                  int64_t Hkv, int64_t D, double base, const int32_t* ctx,
+                                  const int32_t* block_table, int64_t max_blocks,
+                                  int64_t num_blocks, double* q_out, double* k_out,
+                                  double* v_out, int64_t* slot) {
+  if (D % 2 || B < 1 || W < 1) return -1;
+  const int64_t width = (Hq + 2 * Hkv) * D;
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t i = 0; i < W; ++i) {
+      const int64_t row = b * W + i;
+      const int64_t pos = (int64_t)ctx[b] - W + i;
+      const uint16_t* src = qkv + row * width;
+      for (int64_t e = 0; e < Hq * D; ++e) q_out[row * Hq * D + e] = bf16_to_double(src[e]);
+      for (int64_t e = 0; e < Hkv * D; ++e) {
+        k_out[row * Hkv * D + e] = bf16_to_double(src[Hq * D + e]);
+        v_out[row * Hkv * D + e] = bf16_to_double(src[(Hq + Hkv) * D + e]);
+      }
+      for (int64_t h = 0; h < Hq; ++h) rope_head(q_out + (row * Hq + h) * D, D, (double)pos, base);
+      for (int64_t h = 0; h < Hkv; ++h) rope_head(k_out + (row * Hkv + h) * D, D, (double)pos, base);
+      if (pos < 0 || pos / 16 >= max_blocks) {
+        slot[row] = -1;
+      } else {
+        int64_t phys = block_table[b * max_blocks + pos / 16];
+        if (phys < 0) phys = 0;
+        if (phys >= num_blocks) phys = num_blocks - 1;
+        slot[row] = phys * Hkv * 16 + pos % 16;
+      }
+    }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Speculative verify: the step after the target's verify forward.            */
 /* ------------------------------------------------------------------------ */
 

@@ -83,6 +83,11 @@ def _L():
         lib.orc_spec_verify_greedy.argtypes = [P, I64, I64, I64, P, P, P, P]
         lib.orc_spec_verify_sample.restype = None
         lib.orc_spec_verify_sample.argtypes = [P, P, P, P, P, I64, I64, I64, P, P, P]
+        lib.orc_rope.restype = None
+        lib.orc_rope.argtypes = [P, I64, I64, P, ctypes.c_double]
+        lib.orc_rope_kv_append.restype = ctypes.c_int
+        lib.orc_rope_kv_append.argtypes = [P, I64, I64, I64, I64, I64, ctypes.c_double, P, P, I64, I64,
+                                           P, P, P, P]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
         _lib = lib
@@ -330,3 +335,35 @@ def spec_verify_sample(p, q, draft, u_accept, u_sample, context_lens=None):
     _L().orc_spec_verify_sample(_p(pp), _p(qq), _p(d), _p(ua), _p(us), B, K, V, _p(out), _p(cnt), _p(ctx))
     out[np.arange(K + 1)[None, :] >= cnt[:, None]] = -1
     return out, cnt, ctx
+
+
+# -------------------------------------------------------- RoPE / append ----
+
+def rope(x, pos, base: float = 10000.0) -> np.ndarray:
+    """Rotary embedding of head vectors x [rows, d] (float64) at positions
+    pos [rows]: dims (2i, 2i+1) rotate by pos * base^(-2i/d)."""
+    v = _c(x, np.float64).copy()
+    rows, d = v.shape
+    ps = _c(pos, np.float64).reshape(rows)
+    _L().orc_rope(_p(v), rows, d, _p(ps), float(base))
+    return v
+
+
+def rope_kv_append(qkv_bf16, B: int, W: int, hq: int, hkv: int, base: float, context_lens, block_table,
+                   num_blocks: int):
+    """orc_rope_kv_append: returns (q [B, W, hq, d], k [B, W, hkv, d],
+    v [B, W, hkv, d] as float64, slot int64 [B, W]: pool row
+    phys * hkv * 16 + pos % 16 (add head * 16), -1 for no append)."""
+    x = _c(qkv_bf16, np.uint16)
+    d = x.shape[-1] // (hq + 2 * hkv)
+    bt = _c(block_table, np.int32)
+    ctx = _c(context_lens, np.int32)
+    q = np.empty((B, W, hq, d))
+    k = np.empty((B, W, hkv, d))
+    v = np.empty((B, W, hkv, d))
+    slot = np.empty((B, W), np.int64)
+    rc = _L().orc_rope_kv_append(_p(x), B, W, hq, hkv, d, float(base), _p(ctx), _p(bt), bt.shape[1],
+                                 num_blocks, _p(q), _p(k), _p(v), _p(slot))
+    if rc != 0:
+        raise ValueError("orc_rope_kv_append rejected its arguments")
+    return q, k, v, slot
