@@ -12,6 +12,10 @@
  *   quant_fp8_rowwise  BF16 W -> FP8 E4M3 codes + per-output-row fp32 scales.
  *   quant_int4_g128  BF16 W -> INT4 codes + per-group bf16 scales and zeros.
  *
+ * the step between the QKV projection and the attention:
+ *
+ *   rope_kv_append   rotate the new tokens' q and k, append k and v to the cache,
+ *
  * and the step after the verify forward:
  *
  *   spec_verify_greedy / spec_verify_sample  accept a speculative draft
@@ -332,6 +336,44 @@ DQD_API dqd_status gqa_decode_attn_static_ws(const uint16_t* q, const uint16_t* 
                                      const int32_t* context_lens, int32_t max_context,
                                      int32_t b, int32_t w, int32_t hq, int32_t hkv, int32_t d,
                                      float softmax_scale, uint16_t* out, dqd_stream stream);
+
+/* ------------------------------------------------------------------------
+ * rope_kv_append — rotary embedding of the new tokens' q and k, and the
+ * append of their k and v to the paged KV cache (the step between the QKV
+ * projection and the attention).
+ *
+ * Source: [CS10 §2.2-2.3] for each new token compute q, k, v; rotate q and k
+ * at the token's global position (not from 0); write k and v into the cache
+ * at those positions; then attend. Rotary form (the pages do not fix one;
+ * reading: the pairwise form): dims (2i, 2i+1) of every q and k head turn by
+ * angle pos * base^(-2i/d):
+ *   [x_2i', x_2i+1'] = [x_2i cos - x_2i+1 sin, x_2i sin + x_2i+1 cos].
+ * (A checkpoint in the half-split form is brought to it by permuting the
+ * rows of its q and k projections.)
+ * Token (r, i), r < b, i < w, reads row r*w + i of qkv and sits at position
+ * pos = context_lens[r] - w + i (the cache already counts the w new tokens,
+ * as gqa_decode_attn expects). q_out[r][i][h] = rotated q head h (bf16 RNE of
+ * the binary32 rotation); k head g (rotated) and v head g (unchanged) go to
+ * row pos % 16 of kv head g of block block_table[r][pos / 16]. A position
+ * below 0 or past the table appends nothing; table entries outside
+ * [0, num_blocks) are clamped into range.
+ * kv_fp8 = 0: bf16 pools (v is copied bit for bit). kv_fp8 = 1: E4M3 pools as
+ * in gqa_decode_attn_fp8kv: code = e4m3_RNE_satfinite(binary32(x / scale)).
+ * The angle and its reduction to [-pi, pi] are taken in double, sin and cos
+ * in binary32.
+ *
+ * qkv: bf16 [b*w][(hq + 2*hkv) * d], heads ordered q_0.., k_0.., v_0..
+ * (device); q_out: bf16 [b][w][hq][d] (device); pools: [num_blocks][hkv][16][d]
+ * bf16 or u8 (device); block_table, context_lens as in gqa_decode_attn.
+ * Requirements: b, w, hq, hkv >= 1; d even, 2 <= d <= 512; rope_base > 1;
+ * qkv, q_out and pools 16-byte aligned; int32 arrays 4-byte aligned.
+ * ---------------------------------------------------------------------- */
+DQD_API dqd_status rope_kv_append(const uint16_t* qkv, int32_t b, int32_t w, int32_t hq,
+                          int32_t hkv, int32_t d, float rope_base,
+                          const int32_t* block_table, int32_t max_blocks_per_seq,
+                          const int32_t* context_lens, int64_t num_blocks, void* k_pool,
+                          void* v_pool, int32_t kv_fp8, float k_scale, float v_scale,
+                          uint16_t* q_out, dqd_stream stream);
 
 /* ------------------------------------------------------------------------
  * spec_verify_greedy — greedy verify of a speculative draft block, with

@@ -172,6 +172,31 @@ dqd_status quant_int4_g128(const uint16_t* w_bf16, int64_t n, int64_t k, uint8_t
 
 static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
+dqd_status rope_kv_append(const uint16_t* qkv, int32_t b, int32_t w, int32_t hq, int32_t hkv, int32_t d,
+                          float rope_base, const int32_t* block_table, int32_t max_blocks_per_seq,
+                          const int32_t* context_lens, int64_t num_blocks, void* k_pool, void* v_pool,
+                          int32_t kv_fp8, float k_scale, float v_scale, uint16_t* q_out, dqd_stream stream) {
+  g_last_error.clear();
+  if (b < 1 || w < 1 || hq < 1 || hkv < 1 || d < 2 || d > 512 || d % 2 || num_blocks < 1 ||
+      max_blocks_per_seq < 1)
+    return fail(DQD_ERR_INVALID_ARG, "rope_kv_append needs b, w, hq, hkv >= 1, even d in [2, 512], "
+                                     "num_blocks >= 1, max_blocks_per_seq >= 1");
+  if ((int64_t)b * w > INT32_MAX) return fail(DQD_ERR_UNSUPPORTED, "rope_kv_append: b * w too large");
+  if (!(rope_base > 1.f) || rope_base == INFINITY) return fail(DQD_ERR_INVALID_ARG, "rope_base must be finite and > 1");
+  if (kv_fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY))
+    return fail(DQD_ERR_INVALID_ARG, "an FP8 cache needs finite positive k_scale and v_scale");
+  const void* p16[] = {qkv, q_out, k_pool, v_pool};
+  for (const void* p : p16)
+    if (!p || !aligned16(p)) return fail(DQD_ERR_INVALID_ARG, "rope_kv_append: NULL or misaligned pointer");
+  if (!block_table || !context_lens || !aligned4(block_table) || !aligned4(context_lens))
+    return fail(DQD_ERR_INVALID_ARG, "rope_kv_append: NULL or misaligned table or context_lens");
+  return check_launch(dqd::launch_rope_kv_append(qkv, b, w, hq, hkv, d, (double)rope_base, block_table,
+                                                 max_blocks_per_seq, context_lens, num_blocks, k_pool, v_pool,
+                                                 kv_fp8 != 0, k_scale, v_scale, q_out,
+                                                 reinterpret_cast<cudaStream_t>(stream)),
+                      "rope_kv_append launch");
+}
+
 dqd_status spec_verify_greedy(const uint16_t* logits_bf16, int32_t b, int32_t w, int64_t vocab,
                               const int32_t* draft, int32_t* out_tokens, int32_t* out_count,
                               int32_t* context_lens, dqd_stream stream) {

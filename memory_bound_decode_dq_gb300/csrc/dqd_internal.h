@@ -180,6 +180,13 @@ cudaError_t launch_quant_fp8(const uint16_t* w, int64_t n, int64_t k, uint8_t* c
 cudaError_t launch_quant_int4(const uint16_t* w, int64_t n, int64_t k, uint8_t* codes, uint16_t* scales,
                               uint8_t* zeros, cudaStream_t s);
 
+// ------------------------------------------------------ RoPE and append --
+
+cudaError_t launch_rope_kv_append(const uint16_t* qkv, int b, int w, int hq, int hkv, int d, double rope_base,
+                                  const int32_t* table, int max_blocks, const int32_t* ctx, int64_t num_blocks,
+                                  void* k_pool, void* v_pool, bool kv_fp8, float k_scale, float v_scale,
+                                  uint16_t* q_out, cudaStream_t s);
+
 // --------------------------------------------------------------- verify --
 
 cudaError_t launch_spec_verify_greedy(const uint16_t* logits, int b, int w, int64_t vocab, const int32_t* draft,

@@ -50,6 +50,8 @@ _SIGS = {
     "quant_fp8_rowwise": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
     "quant_int4_g128": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P]),
     "spec_verify_greedy": (ctypes.c_int, [_P, _I32, _I32, _I64, _P, _P, _P, _P, _P]),
+    "rope_kv_append": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _I32, ctypes.c_float, _P, _I32, _P, _I64,
+                                      _P, _P, _I32, ctypes.c_float, ctypes.c_float, _P, _P]),
     "spec_verify_sample": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _P, _P, _P, _P]),
     "dq_gemm_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(_WeightDesc), _I64, ctypes.POINTER(_SZ)]),
     "dq_gemm": (ctypes.c_int, [ctypes.POINTER(_WeightDesc), _P, _I64, _P, _P, _SZ, _P]),
@@ -412,3 +414,36 @@ def spec_verify_sample(p: torch.Tensor, q: torch.Tensor, draft: torch.Tensor, u_
                                    _ptr(out), _ptr(count), _ptr(context_lens), _stream(stream)),
            "spec_verify_sample")
     return out, count
+
+
+# ------------------------------------------------------ RoPE and append ----
+
+def rope_kv_append(qkv: torch.Tensor, b: int, w: int, hq: int, hkv: int, k_pool: torch.Tensor,
+                   v_pool: torch.Tensor, block_table: torch.Tensor, context_lens: torch.Tensor,
+                   rope_base: float = 10000.0, k_scale: float = 1.0, v_scale: float = 1.0,
+                   q_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Rotate the new tokens' q and k, append k and v to the paged cache.
+    qkv bf16 [b*w, (hq + 2*hkv) * d]; pools [num_blocks, hkv, 16, d], bf16
+    or uint8 / float8_e4m3fn (FP8 cache with k_scale, v_scale). Returns
+    q_out bf16 [b, w, hq, d]."""
+    _need(qkv, "qkv", _B16)
+    dev = qkv.device
+    f8_types = _U8 + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+    fp8 = k_pool.dtype in f8_types
+    _need(k_pool, "k_pool", f8_types if fp8 else _B16, dev)
+    _need(v_pool, "v_pool", f8_types if fp8 else _B16, dev)
+    _need(block_table, "block_table", _I32T, dev)
+    _need(context_lens, "context_lens", _I32T, dev)
+    rows, width = qkv.shape
+    d = width // (hq + 2 * hkv)
+    if rows != b * w or width != (hq + 2 * hkv) * d or tuple(k_pool.shape[1:]) != (hkv, 16, d) \
+            or v_pool.shape != k_pool.shape:
+        raise ValueError("rope_kv_append: qkv must be [b*w, (hq+2*hkv)*d], pools [num_blocks, hkv, 16, d]")
+    if q_out is None:
+        q_out = torch.empty((b, w, hq, d), dtype=torch.bfloat16, device=dev)
+    _need(q_out, "q_out", _B16, dev)
+    _check(_lib.rope_kv_append(_ptr(qkv), b, w, hq, hkv, d, float(rope_base), _ptr(block_table),
+                               block_table.shape[1], _ptr(context_lens), k_pool.shape[0], _ptr(k_pool),
+                               _ptr(v_pool), 1 if fp8 else 0, float(k_scale), float(v_scale), _ptr(q_out),
+                               _stream(stream)), "rope_kv_append")
+    return q_out
