@@ -227,6 +227,26 @@ def build_calls(wl, dev, dqd):
                                             kv_bytes_per_element=1 if a.kv_fp8 else 2),
                           bounds.attn_flops(ctx, a.width, a.hq, a.d), attn_call(kp, vp), 2 if need else 1, clone))
         io.append((a.name, [q, table_t, ctx_t], [out]))
+    for rc in getattr(wl, "ropes", ()):
+        ctx = list(rc.context)
+        table, nblk = synth.block_table(wl.seed, rc.name + ".table", ctx, True)
+        rows = rc.batch * rc.width
+        qkv = synth.normal_bf16(wl.seed, rc.name + ".qkv", (rows, (rc.hq + 2 * rc.hkv) * rc.d), device=dev)
+        kp = torch.zeros((nblk, rc.hkv, 16, rc.d), dtype=torch.bfloat16, device=dev)
+        vp = torch.zeros_like(kp)
+        table_t = torch.from_numpy(table).to(dev)
+        ctx_t = torch.tensor(ctx, dtype=torch.int32, device=dev)
+        q_out = torch.empty((rc.batch, rc.width, rc.hq, rc.d), dtype=torch.bfloat16, device=dev)
+
+        def rope_call(x, kp=kp, vp=vp, table_t=table_t, ctx_t=ctx_t, q_out=q_out, rc=rc):
+            return lambda: dqd.rope_kv_append(x, rc.batch, rc.width, rc.hq, rc.hkv, kp, vp, table_t, ctx_t,
+                                              rope_base=rc.rope_base, q_out=q_out)
+
+        def rclone(x=qkv, rope_call=rope_call):
+            return rope_call(x.clone())
+        calls.append(Call(rc.name, "rope_kv_append", bounds.rope_append_bytes(rows, rc.hq, rc.hkv, rc.d), 0.0,
+                          rope_call(qkv), 1, rclone))
+        io.append((rc.name, [qkv, table_t, ctx_t], [q_out]))
     for v in getattr(wl, "verifies", ()):
         import numpy as np
         logits = synth.normal_bf16(wl.seed, v.name + ".logits", (v.batch, v.width, v.vocab), device=dev)
@@ -480,7 +500,8 @@ class OracleSample:
         rng = np.random.default_rng(seed)
         costs = [c.m * c.n * c.k for c in wl.gemms] + \
                 [sum(a.context) * a.width * a.hq * a.d * 2 for a in wl.attns] + \
-                [v.batch * v.width * v.vocab for v in getattr(wl, "verifies", ())]
+                [v.batch * v.width * v.vocab for v in getattr(wl, "verifies", ())] + \
+                [200 * r.batch * r.width * (r.hq + 2 * r.hkv) * r.d for r in getattr(wl, "ropes", ())]
         rate = 1.5e8 * max(1, oracle.num_threads())  # oracle multiply-adds per second, roughly
         self.frac = frac = min(1.0, budget_s * rate / float(sum(costs)))
         self.jobs, self.covered = [], 0.0
@@ -522,6 +543,14 @@ class OracleSample:
             per_row = bounds.attn_bytes(a.context, a.width, a.hq, a.hkv, a.d,
                                         kv_bytes_per_element=1 if a.kv_fp8 else 2) / rows_all
             self.covered += per_row * rel * nrows
+        for rc in getattr(wl, "ropes", ()):
+            ntok = max(1, int(round(rc.batch * rc.width * frac)))
+            ctx_s = np.asarray(rc.context[:1], np.int32)
+            tbl, nb = synth.block_table(seed, rc.name + ".cpu.table", ctx_s)
+            qkv = synth.normal_bf16(seed, rc.name + ".cpu", (ntok, (rc.hq + 2 * rc.hkv) * rc.d))
+            self.jobs.append(lambda qkv=qkv, ntok=ntok, rc=rc, ctx_s=ctx_s, tbl=tbl, nb=nb: oracle.rope_kv_append(
+                qkv, 1, ntok, rc.hq, rc.hkv, rc.rope_base, np.maximum(ctx_s, ntok), tbl, nb))
+            self.covered += bounds.rope_append_bytes(ntok, rc.hq, rc.hkv, rc.d)
         for v in getattr(wl, "verifies", ()):
             # one request's verify block (its w logit rows), one in ``reqs``
             reqs = max(1, int(round(v.batch * frac)))

@@ -68,6 +68,13 @@ def attn_bytes(context_lens, w: int, hq: int, hkv: int, d: int = 128, block: int
     return float(kv + qo + table)
 
 
+def rope_append_bytes(tokens: int, hq: int, hkv: int, d: int = 128, kv_bytes_per_element: int = 2) -> float:
+    """RoPE + KV append: read each new token's qkv row (bf16), write its
+    rotated q (bf16) and its k and v into the cache, plus the token's
+    context length and block-table entry."""
+    return float(tokens * ((hq + 2 * hkv) * d * 2 + hq * d * 2 + 2 * hkv * d * kv_bytes_per_element + 8))
+
+
 def verify_bytes(batch: int, width: int, vocab: int) -> float:
     """Greedy verify: the target's bf16 logits, the drafts, the predictions,
     the counts and the context lengths (read and written)."""

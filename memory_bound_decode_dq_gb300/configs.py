@@ -53,12 +53,27 @@ class VerifyCase:
 
 
 @dataclass(frozen=True)
+class RopeCase:
+    """Rotary embedding of the new tokens' q, k and the append of k, v:
+    qkv rows [batch * width, (hq + 2 hkv) * 128] bf16, bf16 paged cache."""
+    name: str
+    batch: int
+    width: int
+    hq: int
+    hkv: int
+    context: tuple
+    rope_base: float = 500000.0
+    d: int = 128
+
+
+@dataclass(frozen=True)
 class Workload:
     name: str
     seed: int
     gemms: tuple = field(default_factory=tuple)
     attns: tuple = field(default_factory=tuple)
     verifies: tuple = field(default_factory=tuple)
+    ropes: tuple = field(default_factory=tuple)
 
 
 def _ctx_uniform(seed: int, batch: int, lo: int, hi: int) -> tuple:
@@ -76,13 +91,15 @@ def tiny() -> Workload:
 
 def llama3_8b_b1() -> Workload:
     """Llama-3-8B-shaped decode layer at batch 1: four projections in BF16 and
-    INT4 g128, attention 32/8 heads over 8192 paged tokens."""
+    INT4 g128, the rotary embedding and KV append of the new token, attention
+    32/8 heads over 8192 paged tokens."""
     g = []
     for wt in (W_BF16, W_INT4_G128):
         for name, n, k in LLAMA3_8B_PROJ:
             g.append(GemmCase(f"{name}_{WTYPE_NAMES[wt]}", wt, 1, n, k))
     return Workload("llama3_8b_decode_b1_ctx8192", 1, gemms=tuple(g),
-                    attns=(AttnCase("attn_32_8_ctx8192", 1, 1, 32, 8, (8192,)),))
+                    attns=(AttnCase("attn_32_8_ctx8192", 1, 1, 32, 8, (8192,)),),
+                    ropes=(RopeCase("rope_append_32_8", 1, 1, 32, 8, (8192,)),))
 
 
 def dense70b_b32() -> Workload:
@@ -114,7 +131,8 @@ def verify_8b() -> Workload:
             a.append(AttnCase(f"attn_verify_b{batch}_w{width}", batch, width, 32, 8,
                               _ctx_uniform(3, batch, 512, 4096)))
             v.append(VerifyCase(f"accept_greedy_b{batch}_w{width}", batch, width, LLAMA3_8B_VOCAB))
-    return Workload("verify_8b_int4", 3, gemms=tuple(g), attns=tuple(a), verifies=tuple(v))
+    r = (RopeCase("rope_append_b64_w16", 64, 16, 32, 8, _ctx_uniform(3, 64, 512, 4096)),)
+    return Workload("verify_8b_int4", 3, gemms=tuple(g), attns=tuple(a), verifies=tuple(v), ropes=r)
 
 
 def longctx_70b_b8() -> Workload:

@@ -181,7 +181,8 @@ dqd_status rope_kv_append(const uint16_t* qkv, int32_t b, int32_t w, int32_t hq,
       max_blocks_per_seq < 1)
     return fail(DQD_ERR_INVALID_ARG, "rope_kv_append needs b, w, hq, hkv >= 1, even d in [2, 512], "
                                      "num_blocks >= 1, max_blocks_per_seq >= 1");
-  if ((int64_t)b * w > INT32_MAX) return fail(DQD_ERR_UNSUPPORTED, "rope_kv_append: b * w too large");
+  if ((int64_t)b * w > INT32_MAX || (int64_t)(hq + 2 * (int64_t)hkv) * (d / 2) > ((int64_t)1 << 24))
+    return fail(DQD_ERR_UNSUPPORTED, "rope_kv_append: b * w or the head count too large");
   if (!(rope_base > 1.f) || rope_base == INFINITY) return fail(DQD_ERR_INVALID_ARG, "rope_base must be finite and > 1");
   if (kv_fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY))
     return fail(DQD_ERR_INVALID_ARG, "an FP8 cache needs finite positive k_scale and v_scale");

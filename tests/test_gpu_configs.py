@@ -198,3 +198,36 @@ def check_verify(dqd, dev, case, seed, max_reqs=8):
 @pytest.mark.parametrize("case", WORKLOADS["verify_8b"].verifies, ids=lambda c: c.name)
 def test_verify_accept(dev, dqd, case):
     check_verify(dqd, dev, case, WORKLOADS["verify_8b"].seed)
+
+
+def check_rope(dqd, dev, case, seed, max_tokens=16):
+    """The bench's RoPE + append call at full size: sampled tokens' rotated q
+    and appended k, v against the oracle."""
+    import numpy as np
+    ctx = np.asarray(case.context, np.int32)
+    table, nblk = synth.block_table(seed, case.name + ".table", ctx, True)
+    rows = case.batch * case.width
+    qkv = synth.normal_bf16(seed, case.name + ".qkv", (rows, (case.hq + 2 * case.hkv) * case.d), device=dev)
+    kp = torch.zeros((nblk, case.hkv, 16, case.d), dtype=torch.bfloat16, device=dev)
+    vp = torch.zeros_like(kp)
+    q = dqd.rope_kv_append(qkv, case.batch, case.width, case.hq, case.hkv, kp, vp,
+                           torch.from_numpy(table).to(dev), torch.from_numpy(ctx).to(dev), rope_base=case.rope_base)
+    toks = sample_rows(rows, max_tokens, seed)
+    kr = kp.view(-1, case.d)
+    vr = vp.view(-1, case.d)
+    for t in toks:
+        b, i = divmod(int(t), case.width)
+        one = bits(qkv[t:t + 1])
+        rq, rk, rv, slot = oracle.rope_kv_append(one, 1, 1, case.hq, case.hkv, case.rope_base,
+                                                 ctx[b:b + 1] - (case.width - 1 - i), table[b:b + 1], nblk)
+        assert_close(f64(q[b, i]), rq[0, 0], what=f"{case.name} q token {t}")
+        for g in range(case.hkv):
+            row = int(slot[0, 0]) + 16 * g
+            assert_close(f64(kr[row]), rk[0, 0, g], what=f"{case.name} k token {t}")
+            assert np.array_equal(bits(vr[row]), one[0, (case.hq + case.hkv + g) * case.d:(case.hq + case.hkv + g + 1) * case.d])
+
+
+@pytest.mark.parametrize("wl", ["llama3_8b_b1", "verify_8b"])
+def test_rope_append(dev, dqd, wl):
+    for case in WORKLOADS[wl].ropes:
+        check_rope(dqd, dev, case, WORKLOADS[wl].seed)
