@@ -45,6 +45,30 @@ __device__ __forceinline__ void arg_better(float& v, int& i, float ov, int oi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Eight logits (16 bytes) starting at token id `base`: the running (value,
+// index) moves only when the chunk's maximum is strictly larger, so chunks
+// visited in increasing id order keep the first maximum; three packed maxima
+// and one compare per chunk, the scan for the index only on a new maximum.
+__device__ __forceinline__ void arg_chunk(float& bv, int& bi, const uint4& x, int base) {
+  const uint32_t m = bf16x2_max(bf16x2_max(x.x, x.y), bf16x2_max(x.z, x.w));
+  const float mx = fmaxf(bf16_lo(m), bf16_hi(m));
+  if (mx > bv) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    int e = 0;
+#pragma unroll
+    for (int j = 7; j >= 0; --j)  // the first element equal to the maximum
+      if ((j & 1 ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1])) == mx) e = j;
+    bv = mx;
+    bi = base + e;
+  }
+}
+
 __global__ void __launch_bounds__(kArgmaxThreads)
 spec_argmax_kernel(const uint16_t* __restrict__ logits, int64_t vocab, int32_t* __restrict__ out) {
   grid_dependency_wait();  // the logits come from the previous kernel
@@ -66,25 +90,9 @@ spec_argmax_kernel(const uint16_t* __restrict__ logits, int64_t vocab, int32_t* 
 #pragma unroll
       for (int j = 0; j < 4; ++j) x[j] = ldg_stream(v4 + u + j * kArgmaxThreads);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int base = (int)(8 * (u + j * kArgmaxThreads));
-        const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          arg_better(bv, bi, bf16_lo(w[e]), base + 2 * e);
-          arg_better(bv, bi, bf16_hi(w[e]), base + 2 * e + 1);
-        }
-      }
+      for (int j = 0; j < 4; ++j) arg_chunk(bv, bi, x[j], (int)(8 * (u + j * kArgmaxThreads)));
     }
-    for (; u < n4; u += kArgmaxThreads) {
-      const uint4 x = ldg_stream(v4 + u);
-      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        arg_better(bv, bi, bf16_lo(w[e]), (int)(8 * u) + 2 * e);
-        arg_better(bv, bi, bf16_hi(w[e]), (int)(8 * u) + 2 * e + 1);
-      }
-    }
+    for (; u < n4; u += kArgmaxThreads) arg_chunk(bv, bi, ldg_stream(v4 + u), (int)(8 * u));
   } else {
     const int64_t per = (vocab + S - 1) / S;
     const int64_t end = min(vocab, (rank + 1) * per);
