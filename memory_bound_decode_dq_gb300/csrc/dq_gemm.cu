@@ -81,6 +81,7 @@ struct Args {
   int cluster;             // splits reduce through distributed shared memory
   int ra;                  // activation rows held per stage (<= ROWS)
   int slot;                // bytes per ring slot
+  int ns;                  // INT4: ring slots (2 or 3)
 };
 
 __device__ __forceinline__ void cp_async8(uint32_t saddr, const void* gptr, bool pred) {
@@ -438,7 +439,7 @@ struct Int4Cfg {
   static constexpr int ROWS = 8 * MT;
   static constexpr int KC = cmin(512, 8192 / ROWS);
   static constexpr int NG = KC / 128;
-  static constexpr int NS = 3;                               // ring slots
+  static constexpr int NS_MAX = 3;                           // ring slots: 2 or 3, set per call
   static constexpr int CODES = WARPS * NG * 1024;
   static constexpr int SCALES = WARPS * NG * 32;
   static constexpr int ZEROS = WARPS * NG * 8;               // staged when their copies align
@@ -449,9 +450,9 @@ struct Int4Cfg {
 template <int MT, int W>
 __global__ void __launch_bounds__(Int4Cfg<MT, W>::THREADS) dq_gemm_int4_kernel(const Args a) {
   using C = Int4Cfg<MT, W>;
-  constexpr int NS = C::NS;
+  const int NS = a.ns;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[2 * NS];
+  __shared__ __align__(8) uint64_t bars[2 * C::NS_MAX];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int64_t tile0 = (int64_t)blockIdx.x * C::WARPS;
@@ -469,7 +470,7 @@ __global__ void __launch_bounds__(Int4Cfg<MT, W>::THREADS) dq_gemm_int4_kernel(c
   // when G and the groups per stage are even (stages start at even groups).
   const bool zbulk = (G % 2 == 0) && (C::NG % 2 == 0);
   const uint32_t ring = smem_addr(smem);
-  const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[NS]);
+  const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[C::NS_MAX]);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -617,7 +618,7 @@ template <int WT, int MT, int W = (MT <= 2 ? 8 : 4)>
 KernelInfo info_t() {
   if constexpr (WT == kINT4) {
     using C = Int4Cfg<MT, W>;
-    return {C::WARPS, C::KC, C::CODES, C::META, C::XSTR, C::ROWS, C::NS};
+    return {C::WARPS, C::KC, C::CODES, C::META, C::XSTR, C::ROWS, C::NS_MAX};
   } else {
     using C = Cfg<WT, MT>;
     return {C::WARPS, C::KC, C::WSTAGE, C::MSTAGE, C::XROWB, C::ROWS, kStages};
@@ -672,6 +673,7 @@ cudaError_t launch_t(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   a.ra = p.ra;
   a.slot = p.slot_bytes;
   a.cluster = p.cluster;
+  a.ns = p.int4_slots;
   dim3 grid(p.grid_x, p.splits, p.m_chunks);
   if constexpr (WT == kINT4) {
     if (p.cluster)
@@ -704,7 +706,7 @@ cudaError_t launch_wt(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
 
 namespace {
 
-GemmPlan plan_warp_mma(int wtype, int64_t m, int64_t n, int64_t k, int num_sms, int warps) {
+GemmPlan plan_warp_mma(int wtype, int64_t m, int64_t n, int64_t k, int num_sms, int warps, int int4_slots) {
   GemmPlan p{};
   p.mt = m <= 8 ? 1 : (m <= 16 ? 2 : (m <= 32 ? 4 : 8));
   const KernelInfo ki = info_of(wtype, p.mt, warps);
@@ -716,7 +718,8 @@ GemmPlan plan_warp_mma(int wtype, int64_t m, int64_t n, int64_t k, int num_sms, 
   p.kc = ki.kc;
   p.ra = (int)std::min<int64_t>(rows, m);
   p.slot_bytes = (ki.wstage + ki.mstage + p.ra * ki.xrowb + 127) / 128 * 128;
-  p.smem_bytes = ki.stages * p.slot_bytes;
+  p.int4_slots = wtype == kINT4 ? std::max(2, std::min(ki.stages, int4_slots)) : 0;
+  p.smem_bytes = (wtype == kINT4 ? p.int4_slots : ki.stages) * p.slot_bytes;
   const int64_t stages = std::max<int64_t>(1, (k + p.kc - 1) / p.kc);
   const int64_t base = (int64_t)p.grid_x * p.m_chunks;
   const int cps = std::max(1, std::min((227 * 1024 - 1024) / std::max(p.smem_bytes, 1), 16 / ki.warps));
@@ -793,12 +796,19 @@ GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
   // Test hook: DQD_GEMM_TC=0 keeps wide-m shapes on the warp-MMA kernels.
   const char* tc_env = std::getenv("DQD_GEMM_TC");
   if (tc_supported(wtype, m, n, k) && !(tc_env && tc_env[0] == '0')) return plan_dq_gemm_tc(wtype, m, n, k, num_sms);
-  GemmPlan p = plan_warp_mma(wtype, m, n, k, num_sms, 8);
+  // INT4 ring depth: 2 slots from m = 5, 3 below. Measured on the 8B and 70B
+  // projections: 2 slots free shared memory for one more CTA per SM once the
+  // activation rows make slots large (m = 8: 70B gate+up 73.9 -> 61.3 us, 8B
+  // gate+up 22.4 -> 19.3 us; m = 16: 70B qkv 29.1 -> 22.4 us), and are mixed
+  // at m <= 4. Test hook: DQD_GEMM_INT4_NS=2 / 3 forces it.
+  int ns = m >= 5 ? 2 : 3;
+  if (const char* env = std::getenv("DQD_GEMM_INT4_NS")) ns = env[0] == '2' ? 2 : 3;
+  GemmPlan p = plan_warp_mma(wtype, m, n, k, num_sms, 8, ns);
   if (wtype == kINT4 && m <= 16) {
     // INT4 at m <= 16: 8 or 4 consumer warps per CTA, whichever spreads the
     // 16-row tiles more evenly over the SMs (fewer warps on ties). Test hook:
     // DQD_GEMM_WARPS=4 / 8 forces the width.
-    const GemmPlan p4 = plan_warp_mma(wtype, m, n, k, num_sms, 4);
+    const GemmPlan p4 = plan_warp_mma(wtype, m, n, k, num_sms, 4, ns);
     const char* w_env = std::getenv("DQD_GEMM_WARPS");
     if (w_env && w_env[0] == '4') return p4;
     if (!(w_env && w_env[0] == '8') && warp_mma_cost(p4, num_sms) <= warp_mma_cost(p, num_sms)) return p4;

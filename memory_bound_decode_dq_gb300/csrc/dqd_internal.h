@@ -91,6 +91,7 @@ struct GemmPlan {
   int tc;            // 1: tensor-core (tcgen05) kernel for wide m
   int mt;            // m8 tiles per CTA pass (1, 2, 4, 8)
   int warps;         // warp-MMA kernels: compute warps per CTA (one 16-row tile each)
+  int int4_slots;    // INT4 warp-MMA kernel: ring slots (2 or 3)
   int m_chunks;      // ceil(m / (8*mt))
   int grid_x;        // CTAs along n (one 16-row tile per warp)
   int splits;        // CTAs along k

@@ -138,14 +138,16 @@ def test_deterministic_with_split_k(dev, dqd, splits, cluster, wtype, on):
     assert dqd.device_errors() == 0
 
 
+@pytest.mark.parametrize("slots", ["2", "3"])
 @pytest.mark.parametrize("warps", ["4", "8"])
 @pytest.mark.parametrize("split", [None, 1, 3])
 @pytest.mark.parametrize("m,n,k", [(1, 1024, 1024), (5, 200, 640), (9, 72, 384), (16, 500, 1536)])
-def test_int4_cta_widths(dev, dqd, splits, monkeypatch, warps, split, m, n, k):
-    """INT4 at m <= 16 runs 8 or 4 tile warps per CTA (the planner picks the
-    width that spreads the tiles more evenly); both agree with the oracle,
-    with and without split-K, on ragged tile counts."""
+def test_int4_cta_widths(dev, dqd, splits, monkeypatch, slots, warps, split, m, n, k):
+    """INT4 at m <= 16 runs 8 or 4 tile warps per CTA over a 2- or 3-slot ring
+    (the planner picks both per shape); every combination agrees with the
+    oracle, with and without split-K, on ragged tile counts."""
     monkeypatch.setenv("DQD_GEMM_WARPS", warps)
+    monkeypatch.setenv("DQD_GEMM_INT4_NS", slots)
     splits(split)
     c = Case(dqd, dev, oracle.W_INT4_G128, n, k, seed=m + n)
     x = synth.normal_bf16(m, "x", (m, k))
