@@ -625,11 +625,12 @@ void* tc_kernel() {
 bool tc_supported(int wtype, int64_t m, int64_t n, int64_t k) {
   if (m > (int64_t)INT32_MAX || n <= 0 || (n + 127) / 128 > 65535 || k <= 0) return false;
   switch (wtype) {
-    // INT4 from m = 25. The tcgen05 kernel's INT4 time hardly depends on m
-    // (it is bound by its dequantisation warps), while the warp-MMA kernel's
-    // grows with its m-tiles: on a 6144 x 4096 weight, 15.6 vs 12.8 us at
-    // m = 17, 15.8 vs 11.9 us at m = 24, 16.1 vs 19.5 us at m = 32.
-    case kINT4: return m >= 25 && k % 128 == 0 && k / 128 <= 65535;
+    // INT4 from m = 33. The tcgen05 kernel's INT4 time hardly depends on m
+    // (a per-slab cost caps it), while the warp-MMA kernel's grows with its
+    // m-tiles: with its 2-slot ring it is faster up to m = 32 on every 8B and
+    // 70B projection (70B gate+up at m = 32: 148.7 vs 185.5 us) and falls
+    // far behind from m = 40, where it needs eight m-tiles.
+    case kINT4: return m >= 33 && k % 128 == 0 && k / 128 <= 65535;
     // FP8 at m = 32 stays on the warp-MMA kernel: on large matrices the
     // tcgen05 kernel's FP8 dequantisation pipeline tops out near 2.5 TB/s.
     case kFP8: return m >= 48 && k % 16 == 0;

@@ -33,8 +33,8 @@ def _weight(dqd, dev, n, k, seed):
 
 
 SHAPES = [(128, 128, 128), (129, 1000, 256), (256, 2048, 1024), (300, 48, 4096), (1024, 130, 512),
-          (500, 4112, 384), (200, 16, 128), (384, 6144, 4096), (17, 300, 1024), (32, 4096, 4096),
-          (64, 28672, 4096)]
+          (500, 4112, 384), (200, 16, 128), (384, 6144, 4096), (33, 300, 1024), (40, 4096, 4096),
+          (64, 28672, 4096), (17, 300, 1024), (32, 4096, 4096)]   # the last two: the warp-MMA side of the boundary
 
 
 @pytest.mark.parametrize("m,n,k", SHAPES)
