@@ -293,10 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < ncs; ++i) {
       mbar_init(cfull + 8 * i, 1);
       // INT4: one group of four warps per slot; FP8: both groups
-      mbar_init(cempty + 8 * i, WT == kFP8 ? kDeqWarps * 32 : kDeqWarps * 16);
+      // one arrival per dequantising warp (lane 0, after __syncwarp): an FP8
+      // code slot serves both groups, an INT4 one a single group
+      mbar_init(cempty + 8 * i, WT == kFP8 ? kDeqWarps : kDeqWarps / 2);
     }
     for (int i = 0; i < nas; ++i) {
-      mbar_init(afull + 8 * i, WT == kBF16 ? 1 : kDeqWarps * 16);
+      mbar_init(afull + 8 * i, WT == kBF16 ? 1 : kDeqWarps / 2);
       mbar_init(aempty + 8 * i, 1);
     }
     for (int i = 0; i < nbs; ++i) {
@@ -419,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           znext[q] = (live[q] && gr + 1 < G) ? ldg_u8(zp[q] + 8 * (gr + 1)) : 0u;
         }
         ++gr;
-        if (!mbar_wait(cfull + 8 * cs, cph)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(cfull + 8 * cs, cph))) {  // warp-uniform: one arrival per warp
           ok = false;
           break;
         }
@@ -431,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           u[q] = lds128(cring + cs * CSLOT + tt * 512 + lane * 16);
           sc[q] = lds32(cring + cs * CSLOT + kI4Codes + tt * 32 + g * 4);
         }
-        if (i >= nas && !mbar_wait(aempty + 8 * s, sph ^ 1u)) {
+        if (i >= nas && !__all_sync(0xffffffffu, mbar_wait(aempty + 8 * s, sph ^ 1u))) {
           ok = false;
           break;
         }
@@ -463,11 +465,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                    bf16x2_mul(f1.a3, shi));
           }
         }
-        fence_proxy_async_smem();  // make the generic-proxy stores visible to the tensor core
-        mbar_arrive(afull + 8 * s);
-        // Release the code slot only now: an arrive does not wait for shared
-        // loads still in flight, so it must follow the use of their values.
-        mbar_arrive(cempty + 8 * cs);
+        // Every lane makes its generic-proxy stores visible to the tensor core;
+        // after the warp has converged, lane 0 arrives for the warp (one
+        // arrival per warp: per-lane arrivals on one barrier word serialise).
+        // The code slot is released only now: an arrive does not wait for
+        // shared loads still in flight, so it must follow the use of their
+        // values, which every lane has made before the __syncwarp.
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(afull + 8 * s);
+          mbar_arrive(cempty + 8 * cs);
+        }
         advance();
       }
     } else if constexpr (WT == kFP8) {
@@ -483,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ks = 0;
       uint32_t kph = 0;  // code slot cursor: one slot per slab pair
       for (int i = grp; i < nl; i += 2) {
-        if (!mbar_wait(cfull + 8 * ks, kph)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(cfull + 8 * ks, kph))) {
           ok = false;
           break;
         }
@@ -493,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = 32 * pass + rbase;
           cw[pass] = lds128(cring + ks * CSLOT + r * 128 + (((4 * grp + c4) ^ (r & 7)) << 4));
         }
-        if (i >= nas && !mbar_wait(aempty + 8 * s, sph ^ 1u)) {
+        if (i >= nas && !__all_sync(0xffffffffu, mbar_wait(aempty + 8 * s, sph ^ 1u))) {
           ok = false;
           break;
         }
@@ -515,9 +524,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             sts128(e1, hi0, hi1, hi2, hi3);
           }
         }
-        fence_proxy_async_smem();  // make the generic-proxy stores visible to the tensor core
-        mbar_arrive(afull + 8 * s);
-        mbar_arrive(cempty + 8 * ks);  // after the loaded codes were used
+        fence_proxy_async_smem();  // as for INT4: per-lane fence, one arrival per warp
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(afull + 8 * s);
+          mbar_arrive(cempty + 8 * ks);  // after the loaded codes were used
+        }
         if (++ks == ncs) {
           ks = 0;
           kph ^= 1u;
