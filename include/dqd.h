@@ -110,6 +110,13 @@ DQD_API const char* dqd_version(void);
 #define DQD_DEVICE_ERR_WAIT_TIMEOUT 1u
 DQD_API dqd_status dqd_device_errors(uint32_t* flags);
 
+/* Diagnostic for failure detection: launches one kernel that waits, with the
+ * same bounded polling as every pipeline wait of the library but at most
+ * `polls` polls (1 <= polls <= 2^22), on a barrier that nothing completes.
+ * The wait gives up, sets DQD_DEVICE_ERR_WAIT_TIMEOUT (read and cleared by
+ * dqd_device_errors) and the kernel returns; the context stays usable. */
+DQD_API dqd_status dqd_selftest_wait_timeout(uint32_t polls, dqd_stream stream);
+
 /* ------------------------------------------------------------------------
  * pack_int4_g128 — re-lay W4A16 INT4 g128 weights for dq_gemm.
  *

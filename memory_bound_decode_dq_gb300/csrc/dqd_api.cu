@@ -109,8 +109,16 @@ dqd_status dqd_device_errors(uint32_t* flags) {
   *flags = 0;
   cudaError_t e = dqd::attn_take_device_error(flags);
   if (e == cudaSuccess) e = dqd::gemm_take_device_error(flags);
+  if (e == cudaSuccess) e = dqd::selftest_take_device_error(flags);
   if (e != cudaSuccess) return fail(DQD_ERR_CUDA, "reading the device error words: %s", cudaGetErrorString(e));
   return DQD_OK;
+}
+
+dqd_status dqd_selftest_wait_timeout(uint32_t polls, dqd_stream stream) {
+  g_last_error.clear();
+  if (polls < 1 || polls > (1u << 22)) return fail(DQD_ERR_INVALID_ARG, "polls must be in [1, 2^22]");
+  return check_launch(dqd::launch_selftest_wait(polls, reinterpret_cast<cudaStream_t>(stream)),
+                      "dqd_selftest_wait_timeout launch");
 }
 
 size_t pack_int4_g128_bytes(int64_t n, int64_t k, int which) {

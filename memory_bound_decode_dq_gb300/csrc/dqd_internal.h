@@ -197,4 +197,11 @@ cudaError_t launch_spec_verify_sample(const float* p, const float* q, const int3
                                       const float* u_sample, int b, int k, int64_t vocab, int32_t* out,
                                       int32_t* count, int32_t* ctx, cudaStream_t s);
 
+// ----------------------------------------------------------- diagnostics --
+
+// One bounded wait (polls polls) on an mbarrier nothing completes; it gives
+// up, sets the self-test error word and returns.
+cudaError_t launch_selftest_wait(uint32_t polls, cudaStream_t s);
+cudaError_t selftest_take_device_error(uint32_t* flags);
+
 }  // namespace dqd

@@ -45,6 +45,7 @@ _SIGS = {
     "dqd_last_error": (ctypes.c_char_p, []),
     "dqd_version": (ctypes.c_char_p, []),
     "dqd_device_errors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "dqd_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
     "pack_int4_g128_bytes": (_SZ, [_I64, _I64, ctypes.c_int]),
     "pack_int4_g128": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _P, _P, _P]),
     "quant_fp8_rowwise": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
@@ -94,6 +95,11 @@ def device_errors() -> int:
     v = ctypes.c_uint32(0)
     _check(_lib.dqd_device_errors(ctypes.byref(v)), "dqd_device_errors")
     return int(v.value)
+
+
+def selftest_wait_timeout(polls: int = 1 << 16, stream=None) -> None:
+    """Run one bounded wait that runs out (see dqd_selftest_wait_timeout)."""
+    _check(_lib.dqd_selftest_wait_timeout(int(polls), _stream(stream)), "dqd_selftest_wait_timeout")
 
 
 def library() -> ctypes.CDLL:
