@@ -165,3 +165,27 @@ def test_rejects_bad_arguments(dev, dqd):
 
 def test_no_device_error_flags(dev, dqd):
     assert dqd.device_errors() == 0
+
+
+def test_sample_at_full_vocabulary(dev, dqd):
+    """Speculative sampling at the 8B vocabulary (128256), batch 64, 5 drafts:
+    tokens, counts and contexts equal the oracle's for every request."""
+    b, k, vocab = 64, 5, 128256
+    rng = np.random.default_rng(77)
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    logits_q = torch.randn((b, k + 1, vocab), generator=g, device=dev) * 3.0
+    logits_p = logits_q[:, :k] + torch.randn((b, k, vocab), generator=g, device=dev)  # a draft close to the target
+    q = torch.softmax(logits_q, dim=2).contiguous()
+    p = torch.softmax(logits_p, dim=2).contiguous()
+    draft = torch.multinomial(p.view(-1, vocab), 1, generator=g).view(b, k).to(torch.int32)
+    ua = torch.from_numpy(rng.random((b, k)).astype(np.float32)).to(dev)
+    us = torch.from_numpy(rng.random(b).astype(np.float32)).to(dev)
+    ctx = torch.full((b,), 3000, dtype=torch.int32, device=dev)
+    out, cnt = dqd.spec_verify_sample(p, q, draft, ua, us, ctx)
+    rout, rcnt, rctx = oracle.spec_verify_sample(p.cpu().numpy(), q.cpu().numpy(), draft.cpu().numpy(),
+                                                 ua.cpu().numpy(), us.cpu().numpy(), np.full(b, 3000, np.int32))
+    assert np.array_equal(cnt.cpu().numpy(), rcnt)
+    assert np.array_equal(out.cpu().numpy(), rout)
+    assert np.array_equal(ctx.cpu().numpy(), rctx)
+    assert 1 < rcnt.mean() < k + 1          # the drafts are accepted some of the time
