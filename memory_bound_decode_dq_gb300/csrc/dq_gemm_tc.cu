@@ -58,8 +58,11 @@ constexpr int kI4Codes = 8 * 512;             // INT4: 8 tiles x half a group bl
 constexpr int kI4Scales = 8 * 32;             // INT4: group scales of the 8 tiles
 constexpr int kDeqWarps = 8;
 constexpr int kDeq0 = 2;                      // first dequantising warp
-constexpr int kMmaWarp = kDeq0 + kDeqWarps;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kMmaWarp = kDeq0 + kDeqWarps;  // first MMA-issuing warp
+constexpr int kMmaWarps = 2;                  // MMA issuers: even and odd slabs
+constexpr int kThreads = (kMmaWarp + kMmaWarps) * 32;
+constexpr int kTmemCols = 512;                // all of an SM's tensor memory: one CTA per SM
+constexpr int kAccCols = 256;                 // column offset of the odd slabs' accumulator
 constexpr int kRingBytes = 222 * 1024;        // all rings
 constexpr int kSmem = kRingBytes + 1024;      // + alignment slack
 static_assert(kSmem + 1024 <= 227 * 1024, "shared memory");
@@ -307,10 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bfull + 8 * i, 1);
       mbar_init(bempty + 8 * i, 1);
     }
-    mbar_init(done, 1);
+    mbar_init(done, nl >= 2 ? kMmaWarps : 1);  // one commit per issuer that has slabs
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) tmem_alloc(smem_addr(&tmem_base_sh), kMaxN);
+  if (warp == kMmaWarp) tmem_alloc(smem_addr(&tmem_base_sh), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -544,13 +547,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) atomicOr(&g_tc_error, kErrWaitTimeout);
   } else {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    // ---------------- MMA issuers ----------------
+    // One thread of each issuing warp: warp kMmaWarp takes the even slabs into
+    // the accumulator at column 0, the next warp the odd slabs into the one at
+    // column kAccCols; the epilogue adds the two. A single issuer spends some
+    // 800-950 cycles per slab on its barrier checks, MMA issues and commits
+    // (measured with per-slab clock stamps, with both operands long in place),
+    // which caps a slab below the time HBM needs for its dequantised weights;
+    // two issuers overlap those latencies.
+    const int e = warp - kMmaWarp;
+    if (lane == 0 && e < min(nl, kMmaWarps)) {
       const uint32_t idesc = idesc_bf16(kRows, a.ntok);
-      int sa = 0, sb = 0;
-      uint32_t pa = 0, pb = 0;
-      for (int i = 0; i < nl; ++i) {
-        if (!mbar_wait(afull + 8 * sa, pa) || !mbar_wait(bfull + 8 * sb, pb)) {
+      const uint32_t acc = tmem + (uint32_t)(e * kAccCols);
+      for (int i = e; i < nl; i += kMmaWarps) {
+        const int sa = i % nas, sb = i % nbs;
+        if (!mbar_wait(afull + 8 * sa, (uint32_t)(i / nas) & 1u) ||
+            !mbar_wait(bfull + 8 * sb, (uint32_t)(i / nbs) & 1u)) {
           atomicOr(&g_tc_error, kErrWaitTimeout);
           break;
         }
@@ -558,19 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t abase = aring + sa * kABytes, bbase = bring + sb * bslot_bytes;
 #pragma unroll
         for (int kk = 0; kk < kSlabK / 16; ++kk)
-          umma_bf16(tmem, sw128_desc(abase + kk * 32), sw128_desc(bbase + kk * 32), idesc,
-                    (i > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16(acc, sw128_desc(abase + kk * 32), sw128_desc(bbase + kk * 32), idesc,
+                    (i > e || kk > 0) ? 1u : 0u);
         // both slots are free once these MMAs have read them
         umma_commit(aempty + 8 * sa);
         umma_commit(bempty + 8 * sb);
-        if (++sa == nas) {
-          sa = 0;
-          pa ^= 1u;
-        }
-        if (++sb == nbs) {
-          sb = 0;
-          pb ^= 1u;
-        }
       }
       umma_commit(done);
     }
@@ -588,10 +592,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nchunks = (a.ntok + 31) / 32;
     float* part = a.splits > 1 ? a.part + (int64_t)blockIdx.z * a.m * a.n : nullptr;
     const float rscale = (WT == kFP8 && row < a.n) ? a.wscale[row] : 1.f;
+    const bool two = nl >= 2;  // the odd slabs' accumulator holds a sum
 #pragma unroll 1
     for (int cc = half; cc < nchunks; cc += 2) {
       uint32_t r[32];
-      tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + cc * 32, r);
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + cc * 32;
+      tmem_ld32(taddr, r);
+      if (two) {
+        uint32_t r2[32];
+        tmem_ld32(taddr + kAccCols, r2);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+      }
       if (good && row < a.n) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -625,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kMaxN);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
