@@ -679,8 +679,9 @@ GemmPlan plan_dq_gemm_tc(int wtype, int64_t m, int64_t n, int64_t k, int num_sms
   // equal chunks) and the k split from a cost model: CTAs run in waves of one
   // per SM; a 64-wide slab costs its shared-memory traffic (weights in,
   // dequantised tile out and back to the tensor core, activations in and
-  // back: about base + 2 N cycles; measured never below about 700 cycles, the
-  // latency of one slab's barrier, copy and MMA round trip) or, with every SM
+  // back: about base + 2 N cycles; measured never below about 700 cycles, what
+  // the two MMA issuers' barrier checks, MMA issues and commits take per slab
+  // between them) or, with every SM
   // streaming, its share of HBM (weight bytes at about 21 bytes per SM
   // cycle), whichever is larger;
   // plus a fixed 6 slabs of fill, drain and epilogue; a split adds its fp32
