@@ -81,16 +81,28 @@ __host__ __device__ constexpr int code_slot(int wt) {
 // (they stream from HBM, so they need the depth). Dequantised weights get up
 // to eight A slots (the dequantise -> MMA -> release round trip spans the A
 // ring), keeping room for a few code slots, and the code ring the rest.
+//
+// Both the A and the activation ring hold an even number of slots. The two
+// MMA issuers take alternate slabs, so with an even ring each slot is only
+// ever used by one issuer, which waits on its "full" barrier use after use.
+// With an odd ring a slot alternates between the issuers, and the one running
+// ahead can wait for use u + 1 of a slot whose use u has not landed yet: the
+// barrier is then two phases behind, its parity matches, and the wait passes
+// on stale data. It then commits early and the slot is refilled under copies
+// still in flight. (A randomised model of the protocol shows such passes for
+// every odd ring size and none for even ones.)
 struct Rings {
   int nas, nbs, ncs;
 };
 __host__ __device__ inline Rings rings(int wt, int ntok) {
   const int bslot = ntok * kSlabK * 2;
   Rings r;
-  r.nbs = min(kMaxBSlots, max(3, (64 * 1024) / bslot));
+  r.nbs = (min(kMaxBSlots, max(3, (64 * 1024) / bslot)) + 1) & ~1;
+  // keep room for four A slots and two code slots
+  if (r.nbs > 2 && r.nbs * bslot + 4 * kABytes + 2 * code_slot(wt) > kRingBytes) r.nbs -= 2;
   const int rest = kRingBytes - r.nbs * bslot;
   if (wt == kBF16) {
-    r.nas = min(kMaxASlots, rest / kABytes);
+    r.nas = min(kMaxASlots, rest / kABytes) & ~1;
     r.ncs = 0;
   } else {
     // INT4: even slot counts, so that slab i's slots (i % n) always serve the
@@ -559,10 +571,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && e < min(nl, kMmaWarps)) {
       const uint32_t idesc = idesc_bf16(kRows, a.ntok);
       const uint32_t acc = tmem + (uint32_t)(e * kAccCols);
+      int sa = e, sb = e;  // slab i's slots i % nas, i % nbs and their parities, kept
+      uint32_t pa = 0, pb = 0;  // incrementally (both rings hold at least 3 slots)
       for (int i = e; i < nl; i += kMmaWarps) {
-        const int sa = i % nas, sb = i % nbs;
-        if (!mbar_wait(afull + 8 * sa, (uint32_t)(i / nas) & 1u) ||
-            !mbar_wait(bfull + 8 * sb, (uint32_t)(i / nbs) & 1u)) {
+        if (!mbar_wait(afull + 8 * sa, pa) || !mbar_wait(bfull + 8 * sb, pb)) {
           atomicOr(&g_tc_error, kErrWaitTimeout);
           break;
         }
@@ -575,6 +587,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // both slots are free once these MMAs have read them
         umma_commit(aempty + 8 * sa);
         umma_commit(bempty + 8 * sb);
+        if ((sa += kMmaWarps) >= nas) {
+          sa -= nas;
+          pa ^= 1u;
+        }
+        if ((sb += kMmaWarps) >= nbs) {
+          sb -= nbs;
+          pb ^= 1u;
+        }
       }
       umma_commit(done);
     }
@@ -763,6 +783,10 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
     }
   }
   if (e != cudaSuccess) return e;
+  {  // the two MMA issuers need even rings (see Rings)
+    const Rings R = rings(l.wtype, (int)p.ra);
+    if ((R.nas | R.nbs) & 1) return cudaErrorInvalidValue;
+  }
   static std::atomic<int> configured[64][3];
   int dev = 0;
   cudaGetDevice(&dev);
