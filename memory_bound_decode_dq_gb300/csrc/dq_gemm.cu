@@ -793,9 +793,12 @@ double warp_mma_cost(const GemmPlan& p, int num_sms) {
 }  // namespace
 
 GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms) {
-  // Test hook: DQD_GEMM_TC=0 keeps wide-m shapes on the warp-MMA kernels.
+  // Test hooks: DQD_GEMM_TC=0 keeps wide-m shapes on the warp-MMA kernels;
+  // DQD_GEMM_TC=1 takes any m to the tcgen05 kernel where the shape allows it.
   const char* tc_env = std::getenv("DQD_GEMM_TC");
-  if (tc_supported(wtype, m, n, k) && !(tc_env && tc_env[0] == '0')) return plan_dq_gemm_tc(wtype, m, n, k, num_sms);
+  const bool tc_on = tc_env && tc_env[0] == '1' ? tc_supported(wtype, std::max<int64_t>(m, 1024), n, k)
+                                                 : tc_supported(wtype, m, n, k);
+  if (tc_on && !(tc_env && tc_env[0] == '0')) return plan_dq_gemm_tc(wtype, m, n, k, num_sms);
   // INT4 ring depth: 2 slots from m = 5, 3 below. Measured on the 8B and 70B
   // projections: 2 slots free shared memory for one more CTA per SM once the
   // activation rows make slots large (m = 8: 70B gate+up 73.9 -> 61.3 us, 8B

@@ -673,16 +673,21 @@ bool tc_supported(int wtype, int64_t m, int64_t n, int64_t k) {
   switch (wtype) {
     // INT4 from m = 33. The tcgen05 kernel's INT4 time hardly depends on m
     // (a per-slab cost caps it), while the warp-MMA kernel's grows with its
-    // m-tiles: with its 2-slot ring it is faster up to m = 32 on every 8B and
-    // 70B projection (70B gate+up at m = 32: 148.7 vs 185.5 us) and falls
-    // far behind from m = 40, where it needs eight m-tiles.
+    // m-tiles: with its 2-slot ring it is faster up to m = 32 on nearly every
+    // 8B and 70B projection (at m = 32, 70B down 78.6 vs 82.2 us, qkv 34.3 vs
+    // 38.9; the 70B gate+up, 149.0 vs 144.7, is the exception) and falls far
+    // behind from m = 40, where it needs eight m-tiles (gate+up 423 vs 142 us).
     case kINT4: return m >= 33 && k % 128 == 0 && k / 128 <= 65535;
-    // FP8 at m = 32 stays on the warp-MMA kernel: on large matrices the
-    // tcgen05 kernel's FP8 dequantisation pipeline tops out near 2.5 TB/s.
-    case kFP8: return m >= 48 && k % 16 == 0;
-    // BF16 from m = 9: from there the warp-MMA GEMV needs two m-tiles and
-    // falls behind (m = 16: 27 vs 15 us on a 6144 x 4096 weight).
-    case kBF16: return m >= 9 && k % 8 == 0;
+    // FP8 from m = 24 and BF16 from m = 17, measured on the 8B and 70B
+    // projections against the warp-MMA kernel with four m-tiles (m = 17..32),
+    // 70B gate+up / down / qkv / o at m = 24, FP8: 130 / 79 / 38 / 27 us against
+    // 147 / 89 / 49 / 29; BF16 at m = 17: 144 / 79 / 39 / 27 against
+    // 157 / 95 / 44 / 32. Below those the warp-MMA kernels win or tie on nearly
+    // every shape (BF16 at m = 16: 4096 x 14336 down 22.6 vs 24.7 us); the
+    // 8B gate+up (28672 x 4096, 224 CTAs: a second wave half full) stays
+    // faster on them throughout (BF16 at m = 32: 46 vs 53 us).
+    case kFP8: return m >= 24 && k % 16 == 0;
+    case kBF16: return m >= 17 && k % 8 == 0;
     default: return false;
   }
 }
@@ -713,9 +718,14 @@ GemmPlan plan_dq_gemm_tc(int wtype, int64_t m, int64_t n, int64_t k, int num_sms
   const double wslab = wtype == kINT4 ? 4352.0 : (wtype == kFP8 ? 8192.0 : 16384.0);
   const char* env = std::getenv("DQD_GEMM_SPLITS");
   const long forced = env ? std::strtol(env, nullptr, 10) : 0;
+  // Test hook: DQD_GEMM_TC_N caps the tokens per CTA (a multiple of 16), which
+  // fixes N and with it the ring layout.
+  const char* n_env = std::getenv("DQD_GEMM_TC_N");
+  const long forced_n = n_env ? std::strtol(n_env, nullptr, 10) : 0;
   double best = -1.0;
   int64_t best_n = kMaxN, best_sp = 1;
   for (int64_t cap = kMaxN; cap >= 16; cap -= 16) {
+    if (forced_n >= 16 && forced_n <= kMaxN && forced_n % 16 == 0 && cap != forced_n) continue;
     const int64_t chunks = (m + cap - 1) / cap;
     const int64_t ntok = ((m + chunks - 1) / chunks + 15) / 16 * 16;  // <= cap
     const int64_t ctas = chunks * p.grid_x;

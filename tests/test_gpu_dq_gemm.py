@@ -77,7 +77,10 @@ WT_IDS = ["bf16", "fp8", "int4"]
 @pytest.mark.parametrize("m,n,k", [(1, 1024, 1024), (1, 40, 384), (3, 17, 256), (8, 100, 512),
                                    (9, 64, 1024), (16, 33, 768), (32, 130, 512), (33, 48, 256),
                                    (64, 80, 384), (100, 50, 256), (1, 4096, 2048)])
-def test_against_oracle(dev, dqd, wtype, m, n, k):
+def test_against_oracle(dev, dqd, monkeypatch, wtype, m, n, k):
+    # the warp-MMA kernels at every m-tile count (wide m otherwise goes to tcgen05;
+    # the warp-MMA kernels still take it where tcgen05 cannot, e.g. k % 16 != 0)
+    monkeypatch.setenv("DQD_GEMM_TC", "0")
     c = Case(dqd, dev, wtype, n, k, seed=m * 31 + n, outliers=6 if wtype != oracle.W_INT4_G128 else 0)
     x = synth.normal_bf16(m + k, "x", (m, k))
     y = dqd.dq_gemm(c.weight, bf(x, dev))
@@ -112,9 +115,10 @@ def cluster(monkeypatch):
 @pytest.mark.parametrize("split", [1, 2, 3, 7, 8, 64])
 @pytest.mark.parametrize("m", [5, 20, 40])
 @pytest.mark.parametrize("on", [True, False], ids=["dsmem", "global"])
-def test_every_split_count(dev, dqd, splits, cluster, wtype, split, m, on):
+def test_every_split_count(dev, dqd, monkeypatch, splits, cluster, wtype, split, m, on):
     """Up to 8 splits reduce inside a thread-block cluster; more, or with the
     cluster path switched off, through global partials and a ticket."""
+    monkeypatch.setenv("DQD_GEMM_TC", "0")
     splits(split)
     cluster(on)
     c = Case(dqd, dev, wtype, 96, 2048, seed=split)

@@ -1,5 +1,5 @@
 """GPU parity of the tensor-core (tcgen05) dq_gemm path taken at wide m (INT4
-from 17 rows, FP8 from 48, BF16 from 9), against the float64 oracle and
+from 33 rows, FP8 from 24, BF16 from 17), against the float64 oracle and
 against the warp-MMA kernels on the same inputs.
 
 Shapes span several 128-row weight tiles and 128-token chunks with ragged n
@@ -121,7 +121,7 @@ DENSE = [oracle.W_BF16, oracle.W_FP8_E4M3]
                                    (300, 64, 1024), (48, 10240, 8192), (1024, 300, 128)])
 def test_dense_against_oracle(dev, dqd, wtype, m, n, k):
     """Ragged k (a partial last slab), ragged n and m, one-slab k, big shapes
-    (FP8 takes this path from 48 rows, BF16 from 9)."""
+    (FP8 takes this path from 24 rows, BF16 from 17)."""
     w, host = _dense(dqd, dev, wtype, n, k, seed=m + n + k)
     x = synth.normal_bf16(m + 2 * k, "x", (m, k))
     y = dqd.dq_gemm(w, bf(x, dev))
@@ -159,11 +159,39 @@ def test_dense_no_device_error_flags(dev, dqd):
 
 
 @pytest.mark.parametrize("m,n,k", [(9, 300, 1024), (16, 6144, 4096), (12, 17, 72)])
-def test_bf16_small_m_on_tensor_cores(dev, dqd, m, n, k):
-    """BF16 from 9 rows: N = 16 tokens per CTA, most of them zero padding."""
+def test_bf16_small_m_on_tensor_cores(dev, dqd, monkeypatch, m, n, k):
+    """BF16 below its threshold, forced onto the tensor cores: N = 16 tokens
+    per CTA, most of them zero padding."""
+    monkeypatch.setenv("DQD_GEMM_TC", "1")
     w, host = _dense(dqd, dev, oracle.W_BF16, n, k, seed=m + n)
     x = synth.normal_bf16(m + k, "x", (m, k))
     rows = None if n <= 1024 else np.unique(np.r_[0, n - 1, np.arange(0, n, 97)])
     got = f64(dqd.dq_gemm(w, bf(x, dev)))
     ref = oracle.dq_gemm(oracle.W_BF16, *host, x, rows=rows)
     assert_close(got if rows is None else got[:, rows], ref, what=f"tc bf16 m={m}")
+
+
+RING_N = [16, 32, 48, 96, 144, 192, 256]
+
+
+@pytest.mark.parametrize("ntok", RING_N)
+@pytest.mark.parametrize("wtype", [oracle.W_BF16, oracle.W_FP8_E4M3, oracle.W_INT4_G128], ids=["bf16", "fp8", "int4"])
+def test_every_ring_layout(dev, dqd, monkeypatch, wtype, ntok):
+    """Every ring layout the tokens per CTA select (N = 16 .. 256: weight, code
+    and activation rings of different depths) over 128 slabs in one CTA, so
+    that each slot is reused many times by the two MMA issuers: results agree
+    with the oracle and no bounded wait gives up."""
+    monkeypatch.setenv("DQD_GEMM_TC", "1")
+    monkeypatch.setenv("DQD_GEMM_TC_N", str(ntok))
+    monkeypatch.setenv("DQD_GEMM_SPLITS", "1")
+    m, n, k = ntok - 5, 256, 8192
+    x = synth.normal_bf16(ntok, "x", (m, k))
+    if wtype == oracle.W_INT4_G128:
+        wq, w = _weight(dqd, dev, n, k, seed=ntok)
+        ref = oracle.dq_gemm(wtype, wq.codes, wq.scales, wq.zeros, x)
+    else:
+        w, host = _dense(dqd, dev, wtype, n, k, seed=ntok)
+        ref = oracle.dq_gemm(wtype, *host, x)
+    assert dqd.dq_gemm_workspace_bytes(w, m) == 0  # one split: the whole k in each CTA
+    assert_close(f64(dqd.dq_gemm(w, bf(x, dev))), ref, what=f"tc {wtype} N={ntok}")
+    assert dqd.device_errors() == 0
