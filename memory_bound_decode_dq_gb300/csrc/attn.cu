@@ -555,6 +555,77 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const Args a) {
   *reinterpret_cast<uint2*>(a.out + row * kD + lane * 4) = o;
 }
 
+// The merge for many chunks per row (8 or more): one CTA per output row, its
+// four warps taking every fourth chunk with eight partial loads in flight per
+// lane, then warp 0 adds the four warps' sums in warp order (the result does
+// not depend on timing). A warp per row, as above, is bound by the latency of
+// its chunk loads at small batch, where few rows have to fill the GPU.
+__global__ void __launch_bounds__(128) attn_merge_wide_kernel(const Args a) {
+  grid_dependency_wait();  // the partials come from the split kernel
+  allow_dependent_launch();
+  __shared__ float4 s_acc[4][32];
+  __shared__ float s_l[4];
+  const int64_t row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = (int)(row / ((int64_t)a.W * a.Hq));
+  const int ctx = seq_ctx(a, b);
+  const int nblk = (ctx + kBlk - 1) / kBlk;
+  const int nch = min(a.nchunks, (nblk + a.chunk_blocks - 1) / a.chunk_blocks);
+  const float* ml = a.part_ml + row * a.nchunks * 2;
+  const float* po = a.part_o + row * a.nchunks * kD + lane * 4;
+  float mstar = kNegInf;
+  for (int c = lane; c < nch; c += 32) mstar = fmaxf(mstar, ml[2 * c]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
+  const float mbase = mstar == kNegInf ? 0.f : mstar;
+  float lpart = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = warp; c0 < nch; c0 += 32) {  // chunks c0 + 4 u, u < 8
+    const int cj = c0 + 4 * lane;
+    float wl = 0.f;
+    if (lane < 8 && cj < nch) {
+      wl = ex2(ml[2 * cj] - mbase);
+      lpart += wl * ml[2 * cj + 1];
+    }
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = c0 + 4 * u;
+      v[u] = c < nch ? __ldcg(reinterpret_cast<const float4*>(po + (int64_t)c * kD)) : zero;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float w = __shfl_sync(0xffffffffu, wl, u);
+      acc.x += w * v[u].x;
+      acc.y += w * v[u].y;
+      acc.z += w * v[u].z;
+      acc.w += w * v[u].w;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, off);
+  s_acc[warp][lane] = acc;
+  if (lane == 0) s_l[warp] = lpart;
+  __syncthreads();
+  if (warp != 0) return;
+  float4 t = s_acc[0][lane];
+#pragma unroll
+  for (int w = 1; w < 4; ++w) {
+    const float4 u = s_acc[w][lane];
+    t.x += u.x;
+    t.y += u.y;
+    t.z += u.z;
+    t.w += u.w;
+  }
+  const float l = ((s_l[0] + s_l[1]) + s_l[2]) + s_l[3];
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  uint2 o;
+  o.x = pack_bf16x2(t.x * inv, t.y * inv);
+  o.y = pack_bf16x2(t.z * inv, t.w * inv);
+  *reinterpret_cast<uint2*>(a.out + row * kD + lane * 4) = o;
+}
+
 // A 4-D tensor map over a KV pool [num_blocks][hkv][16][128] whose box is 16
 // tokens of one (block, kv head), 128 bytes wide (64 bf16 head dims or 128
 // FP8 codes), 128-byte swizzled.
@@ -684,6 +755,29 @@ AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms, 
       }
     }
     if (best < cur && best_cost < 0.87 * cur_cost) cb = (int)rounded((maxblk + best - 1) / best);
+    // Small problems (fewer items than SMs, at most about 2 MB of bf16 KV per
+    // SM): one wave of CTAs, with the chunk count that minimises the blocks
+    // the busiest SM streams (fewer chunks on ties). Measured at batch 1-4,
+    // each wave of CTAs on an SM costs about as much as 30 more blocks
+    // (start-up, first loads, the chunk's partial), so several waves of short
+    // chunks lose to one wave of long ones: batch 1 x 32768 tokens 37.3 ->
+    // about 27 us, batch 4 x 8192 34.5 -> about 28 us. Test hook:
+    // DQD_ATTN_PLAN=0 keeps the plan above.
+    const char* plan_env = std::getenv("DQD_ATTN_PLAN");
+    const bool small = items < num_sms && items * maxblk <= (int64_t)256 * std::max(num_sms, 1);
+    if (small && !(plan_env && plan_env[0] == '0')) {
+      const int64_t n_max = std::max<int64_t>(1, (int64_t)std::max(num_sms, 1) * cps / items);
+      int64_t best_load = -1;
+      for (int64_t n = 1; n <= std::min<int64_t>(n_max, maxblk); ++n) {
+        const int64_t c = std::max<int64_t>(rounded((maxblk + n - 1) / n), cb_min);
+        const int64_t n_eff = (maxblk + c - 1) / c;
+        const int64_t load = (items * n_eff + num_sms - 1) / std::max(num_sms, 1) * c;
+        if (best_load < 0 || load < best_load) {
+          best_load = load;
+          cb = (int)c;
+        }
+      }
+    }
   }
   // Test hook: DQD_ATTN_CHUNK_BLOCKS forces the split-KV chunk size.
   if (const char* env = std::getenv("DQD_ATTN_CHUNK_BLOCKS")) {
@@ -756,6 +850,7 @@ cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) 
     }
   }
   if (e != cudaSuccess || p.nchunks == 1) return e;
+  if (p.nchunks >= 8) return launch_pdl(attn_merge_wide_kernel, dim3((unsigned)rows), dim3(128), 0, s, a);
   const int64_t blocks = ((int64_t)rows + 3) / 4;
   return launch_pdl(attn_merge_kernel, dim3((unsigned)blocks), dim3(128), 0, s, a);
 }
