@@ -762,9 +762,11 @@ AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms, 
     // (start-up, first loads, the chunk's partial), so several waves of short
     // chunks lose to one wave of long ones: batch 1 x 32768 tokens 37.3 ->
     // about 27 us, batch 4 x 8192 34.5 -> about 28 us. Test hook:
-    // DQD_ATTN_PLAN=0 keeps the plan above.
+    // DQD_ATTN_PLAN=0 keeps the plan above; =1 takes this one whenever there
+    // are fewer items than SMs.
     const char* plan_env = std::getenv("DQD_ATTN_PLAN");
-    const bool small = items < num_sms && items * maxblk <= (int64_t)256 * std::max(num_sms, 1);
+    const bool small = items < num_sms && (items * maxblk <= (int64_t)256 * std::max(num_sms, 1) ||
+                                           (plan_env && plan_env[0] == '1'));
     if (small && !(plan_env && plan_env[0] == '0')) {
       const int64_t n_max = std::max<int64_t>(1, (int64_t)std::max(num_sms, 1) * cps / items);
       int64_t best_load = -1;
