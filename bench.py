@@ -438,7 +438,14 @@ def run_e2e(args, calls, io, dev, dqd, step_bytes, world):
     """Each step: copy the step's inputs (activations, queries, block table,
     context lengths) from pinned host memory, run every call through the
     binding, copy every output back, synchronise. Weights and KV stay
-    resident (they are model and cache state, not per-step inputs)."""
+    resident (they are model and cache state, not per-step inputs).
+
+    The step is captured once as a CUDA graph (the copies from and to the
+    pinned host buffers are nodes of it, so every replay moves that step's
+    bytes) and each timed step is a replay followed by a synchronise, timed on
+    the host clock: a decode loop as a serving engine runs it. The same step
+    issued eagerly from Python (host launch overhead included) is reported
+    beside it."""
     import torch
     import torch.distributed as dist
     host_in, host_out = [], []
@@ -451,9 +458,8 @@ def run_e2e(args, calls, io, dev, dqd, step_bytes, world):
         h2d += sum(t.numel() * t.element_size() for t in hi)
         d2h += sum(t.numel() * t.element_size() for t in ho)
     steps = args.e2e_steps or min(args.steps, 2000)
-    stream = torch.cuda.current_stream()
 
-    def one_step():
+    def issue():
         for (name, ins, outs), hi in zip(io, host_in):
             for d, h in zip(ins, hi):
                 d.copy_(h, non_blocking=True)
@@ -462,25 +468,52 @@ def run_e2e(args, calls, io, dev, dqd, step_bytes, world):
         for (name, ins, outs), ho in zip(io, host_out):
             for d, h in zip(outs, ho):
                 h.copy_(d, non_blocking=True)
-        stream.synchronize()
 
-    for _ in range(3):
-        one_step()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        one_step()
-    torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
-    t = torch.tensor([dt], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    dt = float(t.item())
+    def one_step_eager():
+        issue()
+        torch.cuda.current_stream().synchronize()
+
+    graph = None
+    try:
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            issue()
+        side.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            issue()
+    except Exception:
+        graph = None
+
+    def one_step_graph():
+        graph.replay()
+        torch.cuda.current_stream().synchronize()
+
+    def timed(step_fn, n):
+        for _ in range(3):
+            step_fn()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            step_fn()
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        t = torch.tensor([dt], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    dt = timed(one_step_graph if graph is not None else one_step_eager, steps)
+    eager_steps = max(1, min(steps, 200))
+    dt_eager = timed(one_step_eager, eager_steps)
     return {"value": round(step_bytes * steps * world / dt / 1e9, 3), "unit": "GB/s",
             "ms_per_step": round(1e3 * dt / steps, 4), "steps": steps,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "mode": "cuda graph of the step, copies included" if graph is not None else "eager",
+            "eager_ms_per_step": round(1e3 * dt_eager / eager_steps, 4)}
 
 
 # ------------------------------------------------------------ CPU oracle ----
