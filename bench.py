@@ -438,7 +438,9 @@ def run_e2e(args, calls, io, dev, dqd, step_bytes, world):
     """Each step: copy the step's inputs (activations, queries, block table,
     context lengths) from pinned host memory, run every call through the
     binding, copy every output back, synchronise. Weights and KV stay
-    resident (they are model and cache state, not per-step inputs).
+    resident (they are model and cache state, not per-step inputs). The
+    inputs and outputs live in one buffer per dtype, as an engine's step
+    buffers would, so each direction is one copy per dtype.
 
     The step is captured once as a CUDA graph (the copies from and to the
     pinned host buffers are nodes of it, so every replay moves that step's
@@ -448,26 +450,45 @@ def run_e2e(args, calls, io, dev, dqd, step_bytes, world):
     beside it."""
     import torch
     import torch.distributed as dist
-    host_in, host_out = [], []
-    h2d = d2h = 0
-    for _, ins, outs in io:
-        hi = [t.detach().cpu().pin_memory() for t in ins]
-        ho = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-        host_in.append(hi)
-        host_out.append(ho)
-        h2d += sum(t.numel() * t.element_size() for t in hi)
-        d2h += sum(t.numel() * t.element_size() for t in ho)
+    def arenas(tensors):
+        """Re-points the given device tensors (their contents kept) into one
+        contiguous device buffer per dtype; returns (device buffer, pinned host
+        twin holding the same bytes) pairs. A step then moves its inputs and
+        outputs with one copy per dtype and direction."""
+        by_dtype = {}
+        for t in tensors:
+            by_dtype.setdefault(t.dtype, []).append(t)
+        pairs = []
+        for dt, ts in by_dtype.items():
+            n = sum(t.numel() for t in ts)
+            dbuf = torch.empty(n, dtype=dt, device=dev)
+            hbuf = torch.empty(n, dtype=dt, pin_memory=True)
+            off = 0
+            for t in ts:
+                if not t.is_contiguous():
+                    raise ValueError("e2e inputs and outputs must be contiguous")
+                k = t.numel()
+                dbuf[off:off + k].copy_(t.reshape(-1))
+                t.set_(dbuf.untyped_storage(), off, t.shape, t.stride())
+                off += k
+            hbuf.copy_(dbuf)
+            pairs.append((dbuf, hbuf))
+        torch.cuda.synchronize()
+        return pairs
+
+    in_pairs = arenas([t for _, ins, _ in io for t in ins])
+    out_pairs = arenas([t for _, _, outs in io for t in outs])
+    h2d = sum(d.numel() * d.element_size() for d, _ in in_pairs)
+    d2h = sum(d.numel() * d.element_size() for d, _ in out_pairs)
     steps = args.e2e_steps or min(args.steps, 2000)
 
     def issue():
-        for (name, ins, outs), hi in zip(io, host_in):
-            for d, h in zip(ins, hi):
-                d.copy_(h, non_blocking=True)
+        for d, h in in_pairs:
+            d.copy_(h, non_blocking=True)
         for c in calls:
             c.fn()
-        for (name, ins, outs), ho in zip(io, host_out):
-            for d, h in zip(outs, ho):
-                h.copy_(d, non_blocking=True)
+        for d, h in out_pairs:
+            h.copy_(d, non_blocking=True)
 
     def one_step_eager():
         issue()
