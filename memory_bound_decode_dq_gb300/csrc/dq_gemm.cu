@@ -756,12 +756,6 @@ GemmPlan plan_warp_mma(int wtype, int64_t m, int64_t n, int64_t k, int num_sms, 
       if (eff >= 0.9) break;
     }
   }
-  // INT4 over a long k: at least 6 stages a split, so that each CTA's ring
-  // reaches its steady state (measured on the 8B down projection, 4096 x
-  // 14336: 7 cluster splits of 4 stages 12.8 us, 4 of 7 stages 11.3 us; the
-  // planner's pick is within 1% of a sweep of 4, 6 and 8 cluster or global
-  // splits on the other 8B and 70B projections at m = 1 and 8).
-  if (wtype == kINT4 && stages >= 24) splits = std::min<int64_t>(splits, std::max<int64_t>(2, stages / 6));
   // counters must fit their reserved region
   if ((size_t)base * 4 > kCounterBytes) splits = 1;
   // Test hook: DQD_GEMM_SPLITS forces the k split (results must not depend on it
