@@ -26,11 +26,12 @@
 //    multiply; zero points prefetched a group ahead); FP8 eight codes per
 //    16-byte row chunk, converted exactly to bf16 (the scale is applied to
 //    the fp32 result);
-//  * one thread of warp 10 issues tcgen05.mma (M 128, N, K 16, bf16 in, fp32
-//    accumulate in tensor memory) once both operands of a slab are in place,
+//  * one thread each of warps 10 and 11 issues tcgen05.mma (M 128, N, K 16,
+//    bf16 in, fp32 accumulate in tensor memory) for the even and the odd
+//    slabs, into two accumulators, once both operands of a slab are in place,
 //    and commits the slab's MMAs to the "empty" mbarriers of both slots;
-//  * warps 2-9 read the accumulator back with tcgen05.ld (two warps per
-//    32-lane quarter, splitting its columns) and write bf16 y, or with k
+//  * warps 2-9 read the accumulators back with tcgen05.ld (two warps per
+//    32-lane quarter, splitting its columns), add them and write bf16 y, or with k
 //    split, fp32 partials that the last-arriving CTA of the tile sums in
 //    split order (deterministic).
 // Every wait is bounded; tensor memory is released on every path.
@@ -572,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_bf16(kRows, a.ntok);
       const uint32_t acc = tmem + (uint32_t)(e * kAccCols);
       int sa = e, sb = e;  // slab i's slots i % nas, i % nbs and their parities, kept
-      uint32_t pa = 0, pb = 0;  // incrementally (both rings hold at least 3 slots)
+      uint32_t pa = 0, pb = 0;  // incrementally (every ring holds an even number >= 2)
       for (int i = e; i < nl; i += kMmaWarps) {
         if (!mbar_wait(afull + 8 * sa, pa) || !mbar_wait(bfull + 8 * sb, pb)) {
           atomicOr(&g_tc_error, kErrWaitTimeout);
