@@ -648,6 +648,8 @@ def run_reference(args, rank, world):
 
 
 METRIC = "effective HBM GB/s (% of GB300 peak) and us/call for dq_gemm + gqa_decode_attn"
+# Nominal HBM3e bandwidth of the part (the measured copy peak is the roofline's denominator).
+HBM_NOMINAL_GBS = 8000.0
 
 
 def cpu_model() -> str:
@@ -719,6 +721,7 @@ def main():
                 info["alone"] = {"us_median": round(med, 3), "us_min": round(pr["min"], 3),
                                  "GB/s": round(c.nbytes / (med * 1e-6) / 1e9, 1),
                                  "frac_hbm": round(c.nbytes / (med * 1e-6) / 1e9 / hbm, 4),
+                                 "frac_hbm_nominal": round(c.nbytes / (med * 1e-6) / 1e9 / HBM_NOMINAL_GBS, 4),
                                  "TFLOP/s": round(c.flops / (med * 1e-6) / 1e12, 2),
                                  "frac_tensor_bf16": round(c.flops / (med * 1e-6) / 1e12 / tf, 4),
                                  "copies": pr["copies"], "calls": pr["calls"],
@@ -758,6 +761,7 @@ def main():
                                   f"the last {max(1, min(args.graph_steps, r['K'] // 2))} steps carry per-call timing events"),
                        "parallelism": f"replicas x{world}"},
             "frac_of_peak": round(value / world / hbm, 4),
+            "frac_of_nominal": round(value / world / HBM_NOMINAL_GBS, 4),
             "per_call": calls_info,
             "roofline": roof,
             "cpu_baseline": cpu,
