@@ -625,6 +625,12 @@ class OracleSample:
 
 
 def run_reference(args, rank, world):
+    if world > 1:
+        # the other ranks do no work, so rank 0's oracle takes the host's cores
+        # (torchrun sets OMP_NUM_THREADS=1 for every process)
+        import oracle
+        oracle.build()
+        oracle.set_num_threads(len(os.sched_getaffinity(0)))
     wl = workload(args.workload)
     total_steps = args.steps + args.warmup
     # the whole reference run ends within a few minutes

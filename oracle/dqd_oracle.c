@@ -638,6 +638,15 @@ ORC_EXPORT int orc_num_threads(void) {
 #endif
 }
 
+/* Threads for the oracle's later parallel loops (n >= 1); a no-op without OpenMP. */
+ORC_EXPORT void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* Array forms of the scalar codecs, for the Python wrapper. */
 ORC_EXPORT void orc_e4m3_decode_n(const uint8_t* c, int64_t n, double* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_decode(c[i]);

@@ -90,6 +90,8 @@ def _L():
                                            P, P, P, P]
         lib.orc_num_threads.restype = ctypes.c_int
         lib.orc_num_threads.argtypes = []
+        lib.orc_set_num_threads.restype = None
+        lib.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -105,6 +107,11 @@ def _c(a, dtype) -> np.ndarray:
 def num_threads() -> int:
     """OpenMP threads the oracle's parallel loops use."""
     return int(_L().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the oracle's later parallel loops."""
+    _L().orc_set_num_threads(int(n))
 
 
 # ---------------------------------------------------------------- codecs ----

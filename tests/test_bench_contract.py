@@ -46,3 +46,20 @@ def test_gpu_arm_refuses_without_a_gpu():
     p = _run(["--steps", "1", "--warmup", "1", "--workload", "tiny"], timeout=120)
     assert p.returncode != 0
     assert not [l for l in p.stdout.splitlines() if l.strip().startswith("{")]
+
+
+def test_reference_arm_under_torchrun_prints_once_with_all_cores():
+    """Launched as the driver launches N > 1 runs: rank 0 alone prints the
+    line, the other rank exits 0, and the oracle uses the host's cores."""
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    env.pop("OMP_NUM_THREADS", None)
+    p = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", "29617", "bench.py", "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "1", "--workload", "tiny"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+    assert d["cpu_baseline"]["cores"] == len(os.sched_getaffinity(0))
