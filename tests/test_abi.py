@@ -161,3 +161,52 @@ def test_binding_refuses_to_run_without_library(tmp_path, monkeypatch):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "dqd.h"
+
+int main(void) {
+  /* host-only calls: no device is touched */
+  const char* v = dqd_version();
+  const char* s = dqd_status_string(DQD_ERR_WORKSPACE);
+  size_t codes = pack_int4_g128_bytes(256, 1024, 0);
+  dqd_weight w;
+  memset(&w, 0, sizeof w);
+  w.type = DQD_W_INT4_G128;
+  w.n = 64;
+  w.k = 100; /* not a multiple of 128: refused on the host */
+  size_t ws = 0;
+  dqd_status st = dq_gemm_workspace_bytes(&w, 1, &ws);
+  printf("%s|%s|%zu|%d\n", v ? v : "", s ? s : "", codes, (int)st);
+  return 0;
+}
+"""
+
+
+@pytest.mark.parametrize("std", ["c99", "c11"])
+def test_header_is_plain_c_and_links(lib, tmp_path, std):
+    """A C program includes the header under a strict C standard, links
+    against libdqd.so and makes host-only calls."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    from memory_bound_decode_dq_gb300 import build
+    libdir = os.path.dirname(build.build())
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    r = subprocess.run([gcc, f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", str(exe), f"-L{libdir}", "-ldqd", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    version, status, codes, st = out.stdout.strip().split("|")
+    assert version and status
+    assert int(codes) == 256 * 1024 // 2
+    assert int(st) == 1  # DQD_ERR_INVALID_ARG
