@@ -53,3 +53,15 @@ def test_algorithmic_bytes():
     # attention: 8192 tokens x 8 heads x 128 x 2 (K,V) x 2 B + q/out + table
     assert bounds.attn_bytes([8192], 1, 32, 8) == 8192 * 8 * 128 * 4 + 4 * 32 * 128 + 4 * 512
     assert bounds.attn_flops([10], 2, 1, 4) == 4.0 * (9 + 10) * 4
+
+
+def test_algorithmic_bytes_of_the_next_rows():
+    # FP8 cache: 8192 tokens x 8 heads x 128 x 2 (K, V) x 1 B, q and out in bf16, the table
+    assert bounds.attn_bytes([8192], 1, 32, 8, kv_bytes_per_element=1) == 16_777_216 + 16_384 + 2_048
+    # one new token, 32/8 heads: qkv row read (48 x 128 x 2), q written (32 x 128 x 2),
+    # k and v appended (2 x 8 x 128 x 2 in bf16, x 1 in FP8), context length + table entry
+    assert bounds.rope_append_bytes(1, 32, 8) == 12_288 + 8_192 + 4_096 + 8
+    assert bounds.rope_append_bytes(1, 32, 8, kv_bytes_per_element=1) == 12_288 + 8_192 + 2_048 + 8
+    # greedy verify, batch 64 x width 16 over 128256 logits: logits (bf16), drafts (64 x 15),
+    # predictions (64 x 16), counts and context lengths read and written (64 x 12 B)
+    assert bounds.verify_bytes(64, 16, 128256) == 262_668_288 + 3_840 + 4_096 + 768
