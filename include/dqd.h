@@ -102,12 +102,20 @@ DQD_API const char* dqd_last_error(void);
 /* Library version, e.g. "dqd 0.1 sm_103a". */
 DQD_API const char* dqd_version(void);
 
-/* Kernels never spin without bound: every wait on an asynchronous copy gives
- * up after a fixed number of polls (seconds), records a flag in a device error
- * word and ends the kernel (its output is then meaningless). This call
- * synchronises with the current device, returns the OR of those flags in
- * *flags (0: none; bit 0: a bounded wait gave up) and clears them. */
+/* Errors that only the device can see are recorded in device error words:
+ *  - bit 0 (DQD_DEVICE_ERR_WAIT_TIMEOUT): kernels never spin without bound;
+ *    every wait on an asynchronous copy gives up after a fixed number of polls
+ *    (seconds), records this flag and ends the kernel (its output is then
+ *    meaningless);
+ *  - bit 1 (DQD_DEVICE_ERR_BAD_INPUT): a kernel met an input outside its
+ *    documented range and clamped it, so that every access stays in bounds: a
+ *    block-table entry outside [0, num_blocks) (attention, RoPE + append), or
+ *    a context_lens[b] below the verify width w or above max_context
+ *    (attention). The output of that call is not meaningful.
+ * This call synchronises with the current device, returns the OR of the flags
+ * raised since the last call in *flags (0: none) and clears them. */
 #define DQD_DEVICE_ERR_WAIT_TIMEOUT 1u
+#define DQD_DEVICE_ERR_BAD_INPUT 2u
 DQD_API dqd_status dqd_device_errors(uint32_t* flags);
 
 /* Diagnostic for failure detection: launches one kernel that waits, with the
@@ -254,14 +262,17 @@ DQD_API dqd_status dq_gemm(const dqd_weight* w, const uint16_t* x_bf16, int64_t 
  * k_pool,v_pool:bf16 [num_blocks][hkv][16][d]   (device)
  * block_table:  int32 [b][max_blocks_per_seq]   (device)
  * context_lens: int32 [b]                        (device); includes the w new
- *               tokens, so context_lens[b] >= w is required
+ *               tokens, so w <= context_lens[b] <= max_context is required
  * max_context:  host upper bound of context_lens (plans the split)
  * out:          bf16 [b][w][hq][d]              (device)
  * Requirements: d == 128, 1 <= w <= 16, hq % hkv == 0, 1 <= b,
  * max_context <= 16 * max_blocks_per_seq, num_blocks >= 1.
- * Block-table entries outside [0, num_blocks) are clamped into range (the
- * output is then meaningless, but no memory outside the pool is read).
- * A query row that sees no key (context_lens[b] < w) is written as zeros.
+ * Inputs the host cannot check are clamped on the device, so that no memory
+ * outside the pool is read, and reported through DQD_DEVICE_ERR_BAD_INPUT
+ * (dqd_device_errors); the output of such a call is not meaningful:
+ *  - a block-table entry outside [0, num_blocks) is clamped into range;
+ *  - a context_lens[b] above max_context is taken as max_context;
+ *  - a query row that sees no key (context_lens[b] < w) is written as zeros.
  * ---------------------------------------------------------------------- */
 DQD_API dqd_status gqa_decode_attn_workspace_bytes(int32_t b, int32_t w, int32_t hq,
                                            int32_t hkv, int32_t d,
@@ -320,16 +331,22 @@ DQD_API dqd_status gqa_decode_attn_fp8kv(const uint16_t* q, const uint8_t* k_poo
  * the pools, the tables and out; only the split-KV scratch changes hands.
  *
  * Arguments, layouts and results are those of gqa_decode_attn. The scratch
- * is a fixed 32 MiB array inside the library (a static device variable that
- * every GPU loading the library holds until the process exits). A call that
- * needs more than that (b * w * hq * chunks * 520 bytes, plus 64 KiB) returns
- * DQD_ERR_WORKSPACE with a message and launches nothing; use gqa_decode_attn
- * with a caller workspace instead.
+ * is a fixed 32 MiB array inside the library (a static device variable). A
+ * call that needs more than that (b * w * hq * chunks * 520 bytes, plus
+ * 64 KiB) returns DQD_ERR_WORKSPACE with a message and launches nothing; use
+ * gqa_decode_attn with a caller workspace instead.
  *
- * The first call on each device looks up the array's device address (with
- * that device current) and caches it: make that first call before any CUDA
- * stream capture. The function itself allocates nothing and calls no
- * allocating routine.
+ * Set-up, once per device: the first call that needs scratch in a CUDA
+ * context looks up the array's device address there (with that device
+ * current) and caches it under the context's id. Because CUDA loads a
+ * library's kernels on a device lazily, that first call (like the first
+ * call of any entry point of the attention module) may load them, and
+ * loading reserves the 32 MiB array and the kernel code on the device: an
+ * allocation made by the driver, which can fail under memory pressure. Make
+ * that first call at start-up, before serving and before any CUDA stream
+ * capture; from then on the GPU holds the array until the process exits, and
+ * later calls allocate nothing and call no allocating routine. After a device
+ * reset the new context makes its own first call.
  *
  * All calls on a device share the one scratch array, which keeps whatever the
  * previous call left in it; each call writes the partial results it reads,
@@ -363,11 +380,14 @@ DQD_API dqd_status gqa_decode_attn_static_ws(const uint16_t* q, const uint16_t* 
  * the binary32 rotation); k head g (rotated) and v head g (unchanged) go to
  * row pos % 16 of kv head g of block block_table[r][pos / 16]. A position
  * below 0 or past the table appends nothing; table entries outside
- * [0, num_blocks) are clamped into range.
+ * [0, num_blocks) are clamped into range and reported through
+ * DQD_DEVICE_ERR_BAD_INPUT (dqd_device_errors).
  * kv_fp8 = 0: bf16 pools (v is copied bit for bit). kv_fp8 = 1: E4M3 pools as
  * in gqa_decode_attn_fp8kv: code = e4m3_RNE_satfinite(binary32(x / scale)).
- * The angle and its reduction to [-pi, pi] are taken in double, sin and cos
- * in binary32.
+ * The angle pos * base^(-2i/d) is reduced exactly in turns: each frequency
+ * over 2 pi is held as a 64-bit fixed-point fraction (computed in double on
+ * the host), pos times it modulo 2^64 is the angle's fraction of a turn; sin
+ * and cos of it, and the rotation, are taken in binary32.
  *
  * qkv: bf16 [b*w][(hq + 2*hkv) * d], heads ordered q_0.., k_0.., v_0..
  * (device); q_out: bf16 [b][w][hq][d] (device); pools: [num_blocks][hkv][16][d]
@@ -381,6 +401,43 @@ DQD_API dqd_status rope_kv_append(const uint16_t* qkv, int32_t b, int32_t w, int
                           const int32_t* context_lens, int64_t num_blocks, void* k_pool,
                           void* v_pool, int32_t kv_fp8, float k_scale, float v_scale,
                           uint16_t* q_out, dqd_stream stream);
+
+/* ------------------------------------------------------------------------
+ * dq_gemm_qkv_rope_append — the QKV projection of the new tokens fused with
+ * rope_kv_append: the step from a layer's input to the attention's q and
+ * cache in one launch.
+ *
+ * Source: [CS10 §2.2-2.3] for each new token compute q, k, v (the QKV
+ * projection), rotate q and k at the token's global position, write k and v
+ * into the cache, then attend; [MTC, section "量化省下什麼"] the projection is
+ * the dequantising GEMM (BF16, FP8-E4M3 or INT4 g128 weights).
+ *
+ * Result: exactly (bit for bit) what
+ *   dq_gemm(w, x, b*wv, qkv)  followed by
+ *   rope_kv_append(qkv, b, wv, hq, hkv, 128, rope_base, ...)
+ * produce, without qkv: each bf16 output of the projection's epilogue is
+ * rotated with its pair (columns 2i, 2i+1 of a q or k head) and stored into
+ * q_out, the K pool or the V pool (positions, slots, FP8 encoding and the
+ * handling of out-of-range table entries as in rope_kv_append).
+ *
+ * w:     the QKV weight [(hq + 2*hkv) * 128 out][k in], rows ordered
+ *        q_0.., k_0.., v_0.. (any dqd_wtype, layout as in dq_gemm)
+ * x_bf16:bf16 [b*wv][k] (device): row r*wv + i is token i of sequence r
+ * d:     head dimension, must be 128
+ * other arguments: as in rope_kv_append (w there is wv here)
+ * workspace: as dq_gemm's for (w, m = b*wv): dq_gemm_workspace_bytes gives
+ *        its size; counters left at zero, as dq_gemm leaves them.
+ * Requirements: those of dq_gemm and rope_kv_append, d == 128,
+ * b*wv <= 65536, x, q_out and the pools 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+DQD_API dqd_status dq_gemm_qkv_rope_append(const dqd_weight* w, const uint16_t* x_bf16, int32_t b,
+                                   int32_t wv, int32_t hq, int32_t hkv, int32_t d,
+                                   float rope_base, const int32_t* block_table,
+                                   int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                   int64_t num_blocks, void* k_pool, void* v_pool,
+                                   int32_t kv_fp8, float k_scale, float v_scale,
+                                   uint16_t* q_out, void* workspace, size_t ws_bytes,
+                                   dqd_stream stream);
 
 /* ------------------------------------------------------------------------
  * spec_verify_greedy — greedy verify of a speculative draft block, with

@@ -40,6 +40,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdlib>
+#include <mutex>
 
 namespace dqd {
 namespace {
@@ -58,19 +59,22 @@ struct Args {
   float* part_o;   // [rows][nchunks][128]
   float* part_ml;  // [rows][nchunks][2]
   int64_t num_blocks;
-  int max_blocks, B, W, Hq, Hkv, G, QR;
+  int max_blocks, max_context, B, W, Hq, Hkv, G, QR;
   int chunk_blocks, nchunks, qgroups;
   float scale_log2;  // softmax scale (times k_scale for FP8) times log2(e)
   float v_scale;     // 1 for bf16
 };
 
-__device__ __forceinline__ int seq_ctx(const Args& a, int b) {
-  int c = a.ctx[b];
-  return max(0, min(c, a.max_blocks * kBlk));
-}
-
-// Per-module device error word (kErrWaitTimeout when a bounded wait gave up).
+// Per-module device error word (kErrWaitTimeout when a bounded wait gave up,
+// kErrBadInput when an input was clamped into range).
 __device__ unsigned int g_attn_error;
+
+// The context of sequence b, clamped to what the block table and the split
+// plan (sized from the caller's max_context) can cover.
+__device__ __forceinline__ int seq_ctx(const Args& a, int b) {
+  const int c = a.ctx[b];
+  return max(0, min(c, min(a.max_context, a.max_blocks * kBlk)));
+}
 
 template <int QT, bool F8>
 struct Cfg {
@@ -117,6 +121,11 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
   grid_dependency_wait();  // q, the tables and the cache may come from the previous kernel
   allow_dependent_launch();
   const int ctx = seq_ctx(a, b);
+  if (chunk == 0 && g == 0 && qg == 0 && threadIdx.x == 0) {
+    // one CTA per sequence reports a context outside [w, max_context]
+    const int raw = a.ctx[b];
+    if (raw < a.W || raw != ctx) atomicOr(&g_attn_error, kErrBadInput);
+  }
   const int nblk_seq = (ctx + kBlk - 1) / kBlk;
   const int blk0 = chunk * a.chunk_blocks;
   if (blk0 >= nblk_seq) {  // whole CTA: nothing of this sequence here
@@ -167,6 +176,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const __grid_const
       const int blk = blk0 + grp + KS * (i + lane);
       const int32_t v = (i + lane < nb) ? a.table[tab_row + blk] : 0;
       tab = v < 0 ? 0 : (v >= a.num_blocks ? (int32_t)(a.num_blocks - 1) : v);
+      if (tab != v) atomicOr(&g_attn_error, kErrBadInput);  // clamped: reads stay inside the pool
     }
     return __shfl_sync(0xffffffffu, tab, i - tab_base);
   };
@@ -682,25 +692,63 @@ static __device__ __align__(256) uint8_t g_attn_static_scratch[kStaticScratchByt
 
 size_t attn_static_scratch_bytes() { return kStaticScratchBytes; }
 
-// Device address of the static scratch on the current device. In host code the
-// array's name is only a host-side stand-in, so the address is looked up with
-// cudaGetSymbolAddress once per device (with that device current) and cached.
+// Device address of the static scratch in the current CUDA context. In host
+// code the array's name is only a host-side stand-in, so the address is
+// looked up with cudaGetSymbolAddress (the first lookup in a context may load
+// this module there, which reserves the array) and cached under the context's
+// id, which the driver never reuses within a process: after a device reset
+// the new context looks the address up again instead of reusing a stale one.
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+bool current_ctx_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+}  // namespace
+
 cudaError_t attn_static_scratch(void** ptr) {
-  static std::atomic<void*> cache[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64) {
-    void* p = cache[dev].load(std::memory_order_acquire);
-    if (p) {
-      *ptr = p;
-      return cudaSuccess;
-    }
+  static std::mutex mu;
+  static unsigned long long ids[64];
+  static void* addrs[64];
+  static int used = 0, next = 0;
+  unsigned long long id = 0;
+  bool have_id = current_ctx_id(&id);
+  if (have_id) {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+      if (ids[i] == id) {
+        *ptr = addrs[i];
+        return cudaSuccess;
+      }
   }
   void* p = nullptr;
-  e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+  cudaError_t e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64) cache[dev].store(p, std::memory_order_release);
+  if (!have_id) have_id = current_ctx_id(&id);  // the lookup made the context current
+  if (have_id) {
+    std::lock_guard<std::mutex> lk(mu);
+    ids[next] = id;
+    addrs[next] = p;
+    next = (next + 1) % 64;
+    used = used < 64 ? used + 1 : 64;
+  }
   *ptr = p;
   return cudaSuccess;
 }
@@ -822,6 +870,7 @@ cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) 
   }
   a.num_blocks = l.num_blocks;
   a.max_blocks = l.max_blocks;
+  a.max_context = l.max_context;
   a.B = l.b;
   a.W = l.w;
   a.Hq = l.hq;

@@ -32,6 +32,7 @@
 //    them in split order, so the result does not depend on arrival order.
 #include "dqd_device.cuh"
 #include "dqd_internal.h"
+#include "rope_device.cuh"
 
 #include <algorithm>
 #include <atomic>
@@ -261,9 +262,14 @@ __device__ __forceinline__ void compute_stage(float (&acc)[MT][4], uint32_t slot
 
 // Epilogue shared by the dq_gemm kernels (every thread of the CTA calls it):
 // bf16 output, or fp32 split-K partials reduced by the last-arriving CTA.
-template <int WT, int MT, int WARPS, int THREADS>
+// ROPE: the output is a QKV projection row per token (head dim 128, n a
+// multiple of 16); instead of y, each bf16 output goes through rope_store
+// with its rotation partner (column nn ^ 1, same token), which every path
+// below has at hand: a lane 4 apart in the MMA fragment, or the pair a thread
+// reduces itself.
+template <int WT, int MT, int WARPS, int THREADS, bool ROPE>
 __device__ __forceinline__ void finish(const Args& a, float (&acc)[MT][4], int64_t tile0, int64_t m0,
-                                       bool tile_ok) {
+                                       bool tile_ok, const typename EpiOf<ROPE>::type& epi) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int64_t tile = tile0 + warp;
@@ -276,18 +282,35 @@ __device__ __forceinline__ void finish(const Args& a, float (&acc)[MT][4], int64
       s0 = r0 < a.n ? sc[r0] : 0.f;
       s1 = r1 < a.n ? sc[r1] : 0.f;
     }
+    if constexpr (ROPE) {
+      bool bad = false;
 #pragma unroll
-    for (int j = 0; j < MT; ++j)
+      for (int j = 0; j < MT; ++j)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int64_t mm = m0 + 8 * j + 2 * t + (q & 1);
-        const int64_t nn = (q & 2) ? r1 : r0;
-        if (mm < a.m && nn < a.n) {
+        for (int q = 0; q < 4; ++q) {
+          const int64_t mm = m0 + 8 * j + 2 * t + (q & 1);
+          const int64_t nn = (q & 2) ? r1 : r0;
           float v = acc[j][q];
           if constexpr (WT == kFP8) v *= (q & 2) ? s1 : s0;
-          a.y[mm * a.n + nn] = f32_to_bf16(v);
+          const float vb = bf16_round(v);
+          const float partner = __shfl_xor_sync(0xffffffffu, vb, 4);  // row g ^ 1, same token
+          if (mm < a.m && nn < a.n) bad |= rope_store(epi, mm, nn, vb, partner);
         }
-      }
+      if (bad) atomicOr(&g_gemm_error, kErrBadInput);
+    } else {
+#pragma unroll
+      for (int j = 0; j < MT; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int64_t mm = m0 + 8 * j + 2 * t + (q & 1);
+          const int64_t nn = (q & 2) ? r1 : r0;
+          if (mm < a.m && nn < a.n) {
+            float v = acc[j][q];
+            if constexpr (WT == kFP8) v *= (q & 2) ? s1 : s0;
+            a.y[mm * a.n + nn] = f32_to_bf16(v);
+          }
+        }
+    }
     return;
   }
   if (a.cluster) {
@@ -312,16 +335,41 @@ __device__ __forceinline__ void finish(const Args& a, float (&acc)[MT][4], int64
     cluster_sync_all();
     const int S = a.splits, rank = (int)blockIdx.y;
     const int cols = (int)min((int64_t)(8 * MT), a.m - m0);
-    const int ev = cols * RT, e0 = (int)((int64_t)rank * ev / S), e1 = (int)((int64_t)(rank + 1) * ev / S);
     const uint32_t sbase = smem_addr(stage);
-    for (int e = e0 + threadIdx.x; e < e1; e += THREADS) {
-      const int col = e / RT, rid = e % RT;
-      const int64_t nn = tile0 * 16 + rid, mm = m0 + col;
-      float v = 0.f;
-      for (int p = 0; p < S; ++p) v += ld_dsmem_f32(sbase + 4u * (uint32_t)e, (uint32_t)p);
-      if (nn < a.n) {
-        if constexpr (WT == kFP8) v *= reinterpret_cast<const float*>(a.ws)[nn];
-        a.y[mm * a.n + nn] = f32_to_bf16(v);
+    if constexpr (ROPE) {
+      // shares of whole (even row, odd row) pairs: a thread reduces both
+      const int pv = cols * RT / 2, p0 = (int)((int64_t)rank * pv / S), p1 = (int)((int64_t)(rank + 1) * pv / S);
+      bool bad = false;
+      for (int pe = p0 + threadIdx.x; pe < p1; pe += THREADS) {
+        const int e = 2 * pe, col = e / RT, rid = e % RT;
+        const int64_t nn = tile0 * 16 + rid, mm = m0 + col;
+        float v0 = 0.f, v1 = 0.f;
+        for (int p = 0; p < S; ++p) {
+          v0 += ld_dsmem_f32(sbase + 4u * (uint32_t)e, (uint32_t)p);
+          v1 += ld_dsmem_f32(sbase + 4u * (uint32_t)(e + 1), (uint32_t)p);
+        }
+        if (nn < a.n) {
+          if constexpr (WT == kFP8) {
+            v0 *= reinterpret_cast<const float*>(a.ws)[nn];
+            v1 *= reinterpret_cast<const float*>(a.ws)[nn + 1];
+          }
+          const float b0 = bf16_round(v0), b1 = bf16_round(v1);
+          bad |= rope_store(epi, mm, nn, b0, b1);
+          bad |= rope_store(epi, mm, nn + 1, b1, b0);
+        }
+      }
+      if (bad) atomicOr(&g_gemm_error, kErrBadInput);
+    } else {
+      const int ev = cols * RT, e0 = (int)((int64_t)rank * ev / S), e1 = (int)((int64_t)(rank + 1) * ev / S);
+      for (int e = e0 + threadIdx.x; e < e1; e += THREADS) {
+        const int col = e / RT, rid = e % RT;
+        const int64_t nn = tile0 * 16 + rid, mm = m0 + col;
+        float v = 0.f;
+        for (int p = 0; p < S; ++p) v += ld_dsmem_f32(sbase + 4u * (uint32_t)e, (uint32_t)p);
+        if (nn < a.n) {
+          if constexpr (WT == kFP8) v *= reinterpret_cast<const float*>(a.ws)[nn];
+          a.y[mm * a.n + nn] = f32_to_bf16(v);
+        }
       }
     }
     cluster_sync_all();
@@ -350,29 +398,53 @@ __device__ __forceinline__ void finish(const Args& a, float (&acc)[MT][4], int64
   // and sums their split partials in split order (loads issued ahead of adds).
   const int64_t n0 = tile0 * 16;
   const int64_t S = a.splits, plane = a.m * a.n;
-  for (int e = threadIdx.x; e < WARPS * 16 * (8 * MT); e += THREADS) {
-    const int64_t nn = n0 + e / (8 * MT), mm = m0 + e % (8 * MT);
-    if (nn >= a.n || mm >= a.m) continue;
-    const float* p = a.part + mm * a.n + nn;
-    float sacc = 0.f;
-    int64_t sp = 0;
-    for (; sp + 4 <= S; sp += 4) {
-      const float v0 = __ldcg(p + sp * plane), v1 = __ldcg(p + (sp + 1) * plane);
-      const float v2 = __ldcg(p + (sp + 2) * plane), v3 = __ldcg(p + (sp + 3) * plane);
-      sacc += v0;
-      sacc += v1;
-      sacc += v2;
-      sacc += v3;
+  if constexpr (ROPE) {
+    // a thread owns the (even row, odd row) pair of one token
+    bool bad = false;
+    for (int e = threadIdx.x; e < WARPS * 8 * (8 * MT); e += THREADS) {
+      const int64_t nn = n0 + 2 * (e / (8 * MT)), mm = m0 + e % (8 * MT);
+      if (nn >= a.n || mm >= a.m) continue;
+      const float* p = a.part + mm * a.n + nn;
+      float v0 = 0.f, v1 = 0.f;
+      for (int64_t sp = 0; sp < S; ++sp) {
+        v0 += __ldcg(p + sp * plane);
+        v1 += __ldcg(p + sp * plane + 1);
+      }
+      if constexpr (WT == kFP8) {
+        v0 *= reinterpret_cast<const float*>(a.ws)[nn];
+        v1 *= reinterpret_cast<const float*>(a.ws)[nn + 1];
+      }
+      const float b0 = bf16_round(v0), b1 = bf16_round(v1);
+      bad |= rope_store(epi, mm, nn, b0, b1);
+      bad |= rope_store(epi, mm, nn + 1, b1, b0);
     }
-    for (; sp < S; ++sp) sacc += __ldcg(p + sp * plane);
-    if constexpr (WT == kFP8) sacc *= reinterpret_cast<const float*>(a.ws)[nn];
-    a.y[mm * a.n + nn] = f32_to_bf16(sacc);
+    if (bad) atomicOr(&g_gemm_error, kErrBadInput);
+  } else {
+    for (int e = threadIdx.x; e < WARPS * 16 * (8 * MT); e += THREADS) {
+      const int64_t nn = n0 + e / (8 * MT), mm = m0 + e % (8 * MT);
+      if (nn >= a.n || mm >= a.m) continue;
+      const float* p = a.part + mm * a.n + nn;
+      float sacc = 0.f;
+      int64_t sp = 0;
+      for (; sp + 4 <= S; sp += 4) {
+        const float v0 = __ldcg(p + sp * plane), v1 = __ldcg(p + (sp + 1) * plane);
+        const float v2 = __ldcg(p + (sp + 2) * plane), v3 = __ldcg(p + (sp + 3) * plane);
+        sacc += v0;
+        sacc += v1;
+        sacc += v2;
+        sacc += v3;
+      }
+      for (; sp < S; ++sp) sacc += __ldcg(p + sp * plane);
+      if constexpr (WT == kFP8) sacc *= reinterpret_cast<const float*>(a.ws)[nn];
+      a.y[mm * a.n + nn] = f32_to_bf16(sacc);
+    }
   }
   if (threadIdx.x == 0) *cnt = 0u;  // leave the counter at zero for the next call
 }
 
-template <int WT, int MT>
-__global__ void __launch_bounds__(Cfg<WT, MT>::THREADS) dq_gemm_kernel(const Args a) {
+template <int WT, int MT, bool ROPE>
+__global__ void __launch_bounds__(Cfg<WT, MT>::THREADS)
+    dq_gemm_kernel(const Args a, const __grid_constant__ typename EpiOf<ROPE>::type epi) {
   using C = Cfg<WT, MT>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -420,7 +492,7 @@ __global__ void __launch_bounds__(Cfg<WT, MT>::THREADS) dq_gemm_kernel(const Arg
   }
   cp_async_wait<0>();
 
-  finish<WT, MT, C::WARPS, C::THREADS>(a, acc, tile0, m0, tile_ok);
+  finish<WT, MT, C::WARPS, C::THREADS, ROPE>(a, acc, tile0, m0, tile_ok, epi);
 }
 
 // ------------------------------------------------------------------------
@@ -447,8 +519,9 @@ struct Int4Cfg {
   static constexpr int XSTR = KC * 2 + 64;                    // padded activation row
 };
 
-template <int MT, int W>
-__global__ void __launch_bounds__(Int4Cfg<MT, W>::THREADS) dq_gemm_int4_kernel(const Args a) {
+template <int MT, int W, bool ROPE>
+__global__ void __launch_bounds__(Int4Cfg<MT, W>::THREADS)
+    dq_gemm_int4_kernel(const Args a, const __grid_constant__ typename EpiOf<ROPE>::type epi) {
   using C = Int4Cfg<MT, W>;
   const int NS = a.ns;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -607,7 +680,7 @@ __global__ void __launch_bounds__(Int4Cfg<MT, W>::THREADS) dq_gemm_int4_kernel(c
     // Let the copies already in flight land (bounded) before the CTA moves on.
     for (int i = 0; i < min(NS, nst); ++i) (void)mbar_wait(full0 + 8 * i, 0);
   }
-  finish<kINT4, MT, C::WARPS, C::THREADS>(a, acc, tile0, m0, tile_ok);
+  finish<kINT4, MT, C::WARPS, C::THREADS, ROPE>(a, acc, tile0, m0, tile_ok, epi);
 }
 
 struct KernelInfo {
@@ -642,16 +715,16 @@ KernelInfo info_of(int wt, int mt, int warps) {
 #undef DQD_INFO
 }
 
-template <int WT, int MT, int W = (MT <= 2 ? 8 : 4)>
+template <int WT, int MT, int W, bool ROPE>
 cudaError_t launch_t(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   using C = Cfg<WT, MT>;
   static std::atomic<int> configured[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || configured[dev].load(std::memory_order_relaxed) < p.smem_bytes) {
-    cudaError_t e = WT == kINT4 ? cudaFuncSetAttribute(dq_gemm_int4_kernel<MT, W>,
+    cudaError_t e = WT == kINT4 ? cudaFuncSetAttribute(dq_gemm_int4_kernel<MT, W, ROPE>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes)
-                                : cudaFuncSetAttribute(dq_gemm_kernel<WT, MT>,
+                                : cudaFuncSetAttribute(dq_gemm_kernel<WT, MT, ROPE>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev].store(p.smem_bytes, std::memory_order_relaxed);
@@ -674,31 +747,34 @@ cudaError_t launch_t(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   a.slot = p.slot_bytes;
   a.cluster = p.cluster;
   a.ns = p.int4_slots;
+  typename EpiOf<ROPE>::type epi{};
+  if constexpr (ROPE) epi = *l.rope;
   dim3 grid(p.grid_x, p.splits, p.m_chunks);
   if constexpr (WT == kINT4) {
     if (p.cluster)
-      return launch_pdl_cluster(dq_gemm_int4_kernel<MT, W>, grid, dim3(Int4Cfg<MT, W>::THREADS), p.smem_bytes, s,
-                                (unsigned)p.splits, a);
-    return launch_pdl(dq_gemm_int4_kernel<MT, W>, grid, dim3(Int4Cfg<MT, W>::THREADS), p.smem_bytes, s, a);
+      return launch_pdl_cluster(dq_gemm_int4_kernel<MT, W, ROPE>, grid, dim3(Int4Cfg<MT, W>::THREADS), p.smem_bytes,
+                                s, (unsigned)p.splits, a, epi);
+    return launch_pdl(dq_gemm_int4_kernel<MT, W, ROPE>, grid, dim3(Int4Cfg<MT, W>::THREADS), p.smem_bytes, s, a,
+                      epi);
   } else {
     if (p.cluster)
-      return launch_pdl_cluster(dq_gemm_kernel<WT, MT>, grid, dim3(C::THREADS), p.smem_bytes, s, (unsigned)p.splits,
-                                a);
-    return launch_pdl(dq_gemm_kernel<WT, MT>, grid, dim3(C::THREADS), p.smem_bytes, s, a);
+      return launch_pdl_cluster(dq_gemm_kernel<WT, MT, ROPE>, grid, dim3(C::THREADS), p.smem_bytes, s,
+                                (unsigned)p.splits, a, epi);
+    return launch_pdl(dq_gemm_kernel<WT, MT, ROPE>, grid, dim3(C::THREADS), p.smem_bytes, s, a, epi);
   }
 }
 
-template <int WT>
+template <int WT, bool ROPE>
 cudaError_t launch_wt(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   if constexpr (WT == kINT4) {
-    if (p.mt == 1 && p.warps == 4) return launch_t<WT, 1, 4>(l, p, s);
-    if (p.mt == 2 && p.warps == 4) return launch_t<WT, 2, 4>(l, p, s);
+    if (p.mt == 1 && p.warps == 4) return launch_t<WT, 1, 4, ROPE>(l, p, s);
+    if (p.mt == 2 && p.warps == 4) return launch_t<WT, 2, 4, ROPE>(l, p, s);
   }
   switch (p.mt) {
-    case 1: return launch_t<WT, 1>(l, p, s);
-    case 2: return launch_t<WT, 2>(l, p, s);
-    case 4: return launch_t<WT, 4>(l, p, s);
-    default: return launch_t<WT, 8>(l, p, s);
+    case 1: return launch_t<WT, 1, 8, ROPE>(l, p, s);
+    case 2: return launch_t<WT, 2, 8, ROPE>(l, p, s);
+    case 4: return launch_t<WT, 4, 4, ROPE>(l, p, s);
+    default: return launch_t<WT, 8, 4, ROPE>(l, p, s);
   }
 }
 
@@ -831,10 +907,17 @@ cudaError_t gemm_take_device_error(uint32_t* flags) {
 
 cudaError_t launch_dq_gemm(const GemmLaunch& l, const GemmPlan& p, cudaStream_t s) {
   if (p.tc) return launch_dq_gemm_tc(l, p, s);
+  if (l.rope) {
+    switch (l.wtype) {
+      case kBF16: return launch_wt<kBF16, true>(l, p, s);
+      case kFP8: return launch_wt<kFP8, true>(l, p, s);
+      default: return launch_wt<kINT4, true>(l, p, s);
+    }
+  }
   switch (l.wtype) {
-    case kBF16: return launch_wt<kBF16>(l, p, s);
-    case kFP8: return launch_wt<kFP8>(l, p, s);
-    default: return launch_wt<kINT4>(l, p, s);
+    case kBF16: return launch_wt<kBF16, false>(l, p, s);
+    case kFP8: return launch_wt<kFP8, false>(l, p, s);
+    default: return launch_wt<kINT4, false>(l, p, s);
   }
 }
 

@@ -37,6 +37,7 @@
 // Every wait is bounded; tensor memory is released on every path.
 #include "dqd_device.cuh"
 #include "dqd_internal.h"
+#include "rope_device.cuh"
 
 #include <algorithm>
 #include <atomic>
@@ -211,8 +212,12 @@ __device__ __forceinline__ float4 ldcg4(const float* p) {
 // Last-arriving CTA of a split-K tile: y = bf16(sum of the split partials in
 // split order) over the tile's rows [r0, r0 + rows) and tokens [m0, m0 + toks).
 // Each thread keeps four outputs' partial loads of up to four splits in flight.
-__device__ __forceinline__ void reduce_splits(const TcArgs& a, int64_t r0, int rows, int64_t m0, int toks, int tid,
-                                              int nthreads) {
+// ROPE: the four consecutive rows of a unit are two rotation pairs, stored
+// through rope_store instead of y (n is a multiple of 128 there).
+template <bool ROPE>
+__device__ __forceinline__ bool reduce_splits(const TcArgs& a, int64_t r0, int rows, int64_t m0, int toks, int tid,
+                                              int nthreads, const typename EpiOf<ROPE>::type& epi) {
+  bool bad = false;
   const int64_t plane = a.m * a.n;
   const float* part = a.part;
   if ((a.n & 3) == 0) {
@@ -260,13 +265,23 @@ __device__ __forceinline__ void reduce_splits(const TcArgs& a, int64_t r0, int r
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if (live[q]) {
-          uint2 o;
-          o.x = pack_bf16x2(acc[q].x, acc[q].y);
-          o.y = pack_bf16x2(acc[q].z, acc[q].w);
-          *reinterpret_cast<uint2*>(a.y + off[q]) = o;
+          if constexpr (ROPE) {
+            const int64_t mm = off[q] / a.n, nn = off[q] % a.n;
+            const float b0 = bf16_round(acc[q].x), b1 = bf16_round(acc[q].y);
+            const float b2 = bf16_round(acc[q].z), b3 = bf16_round(acc[q].w);
+            bad |= rope_store(epi, mm, nn, b0, b1);
+            bad |= rope_store(epi, mm, nn + 1, b1, b0);
+            bad |= rope_store(epi, mm, nn + 2, b2, b3);
+            bad |= rope_store(epi, mm, nn + 3, b3, b2);
+          } else {
+            uint2 o;
+            o.x = pack_bf16x2(acc[q].x, acc[q].y);
+            o.y = pack_bf16x2(acc[q].z, acc[q].w);
+            *reinterpret_cast<uint2*>(a.y + off[q]) = o;
+          }
         }
     }
-  } else {
+  } else if constexpr (!ROPE) {
     const int units = rows * toks;
     for (int u = tid; u < units; u += nthreads) {
       const int64_t off = (m0 + u / rows) * a.n + r0 + u % rows;
@@ -275,12 +290,14 @@ __device__ __forceinline__ void reduce_splits(const TcArgs& a, int64_t r0, int r
       a.y[off] = f32_to_bf16(a.wscale ? acc * a.wscale[r0 + u % rows] : acc);
     }
   }
+  return bad;
 }
 
-template <int WT>
+template <int WT, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
-                      const __grid_constant__ CUtensorMap tms, const TcArgs a) {
+                      const __grid_constant__ CUtensorMap tms, const TcArgs a,
+                      const __grid_constant__ typename EpiOf<ROPE>::type epi) {
   constexpr int CSLOT = code_slot(WT);
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * kMaxCSlots + 2 * kMaxASlots + 2 * kMaxBSlots + 1];
@@ -625,7 +642,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
       }
-      if (good && row < a.n) {
+      if (ROPE && !part) {
+        // rotation partner: row ^ 1, the neighbouring lane of this warp
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float vb = bf16_round(__uint_as_float(r[j]) * rscale);
+          const float partner = __shfl_xor_sync(0xffffffffu, vb, 1);
+          const int64_t mm = m0 + cc * 32 + j;
+          if constexpr (ROPE)
+            if (good && row < a.n && cc * 32 + j < a.ntok && mm < a.m) bad |= rope_store(epi, mm, row, vb, partner);
+        }
+        if (bad) atomicOr(&g_tc_error, kErrBadInput);
+      } else if (good && row < a.n) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int64_t mm = m0 + cc * 32 + j;
@@ -649,7 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         const int rows = (int)min((int64_t)kRows, a.n - row0);
         const int toks = (int)min((int64_t)a.ntok, a.m - m0);
-        reduce_splits(a, row0, rows, m0, toks, threadIdx.x - kDeq0 * 32, kDeqWarps * 32);
+        if (reduce_splits<ROPE>(a, row0, rows, m0, toks, threadIdx.x - kDeq0 * 32, kDeqWarps * 32, epi))
+          atomicOr(&g_tc_error, kErrBadInput);
         if (warp == kDeq0 && lane == 0) *cnt = 0u;  // leave the ticket at zero for the next call
       }
     }
@@ -662,9 +692,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int WT>
+template <int WT, bool ROPE>
 void* tc_kernel() {
-  return reinterpret_cast<void*>(dq_gemm_tc_kernel<WT>);
+  return reinterpret_cast<void*>(dq_gemm_tc_kernel<WT, ROPE>);
 }
 
 }  // namespace
@@ -798,15 +828,19 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
     const Rings R = rings(l.wtype, (int)p.ra);
     if ((R.nas | R.nbs) & 1) return cudaErrorInvalidValue;
   }
-  static std::atomic<int> configured[64][3];
+  static std::atomic<int> configured[64][6];
   int dev = 0;
   cudaGetDevice(&dev);
   const int wi = l.wtype == kBF16 ? 0 : (l.wtype == kFP8 ? 1 : 2);
-  if (dev < 0 || dev >= 64 || !configured[dev][wi].load(std::memory_order_relaxed)) {
-    void* fn = wi == 0 ? tc_kernel<kBF16>() : (wi == 1 ? tc_kernel<kFP8>() : tc_kernel<kINT4>());
+  const bool rope = l.rope != nullptr;
+  const int fi = wi + (rope ? 3 : 0);
+  if (dev < 0 || dev >= 64 || !configured[dev][fi].load(std::memory_order_relaxed)) {
+    void* fn = rope ? (wi == 0 ? tc_kernel<kBF16, true>() : (wi == 1 ? tc_kernel<kFP8, true>() : tc_kernel<kINT4, true>()))
+                    : (wi == 0 ? tc_kernel<kBF16, false>()
+                               : (wi == 1 ? tc_kernel<kFP8, false>() : tc_kernel<kINT4, false>()));
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev][wi].store(1, std::memory_order_relaxed);
+    if (dev >= 0 && dev < 64) configured[dev][fi].store(1, std::memory_order_relaxed);
   }
   TcArgs a;
   a.wz = static_cast<const uint8_t*>(l.zeros);
@@ -821,10 +855,20 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
   a.splits = p.splits;
   a.slabs_per_split = (int)(p.k_per_split / kSlabK);
   const dim3 grid(p.m_chunks, p.grid_x, p.splits);
+  const size_t smem = (size_t)p.smem_bytes;
+  if (rope) {
+    const RopeEpi& r = *l.rope;
+    switch (wi) {
+      case 0: return launch_pdl(dq_gemm_tc_kernel<kBF16, true>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, r);
+      case 1: return launch_pdl(dq_gemm_tc_kernel<kFP8, true>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, r);
+      default: return launch_pdl(dq_gemm_tc_kernel<kINT4, true>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, r);
+    }
+  }
+  const NoEpi none{};
   switch (wi) {
-    case 0: return launch_pdl(dq_gemm_tc_kernel<kBF16>, grid, dim3(kThreads), (size_t)p.smem_bytes, s, tmx, tmw, tms, a);
-    case 1: return launch_pdl(dq_gemm_tc_kernel<kFP8>, grid, dim3(kThreads), (size_t)p.smem_bytes, s, tmx, tmw, tms, a);
-    default: return launch_pdl(dq_gemm_tc_kernel<kINT4>, grid, dim3(kThreads), (size_t)p.smem_bytes, s, tmx, tmw, tms, a);
+    case 0: return launch_pdl(dq_gemm_tc_kernel<kBF16, false>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, none);
+    case 1: return launch_pdl(dq_gemm_tc_kernel<kFP8, false>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, none);
+    default: return launch_pdl(dq_gemm_tc_kernel<kINT4, false>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, none);
   }
 }
 

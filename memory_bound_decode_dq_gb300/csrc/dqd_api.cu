@@ -109,6 +109,7 @@ dqd_status dqd_device_errors(uint32_t* flags) {
   *flags = 0;
   cudaError_t e = dqd::attn_take_device_error(flags);
   if (e == cudaSuccess) e = dqd::gemm_take_device_error(flags);
+  if (e == cudaSuccess) e = dqd::rope_take_device_error(flags);
   if (e == cudaSuccess) e = dqd::selftest_take_device_error(flags);
   if (e != cudaSuccess) return fail(DQD_ERR_CUDA, "reading the device error words: %s", cudaGetErrorString(e));
   return DQD_OK;
@@ -281,6 +282,7 @@ dqd_status dq_gemm(const dqd_weight* w, const uint16_t* x_bf16, int64_t m, uint1
       return fail(DQD_ERR_WORKSPACE, "dq_gemm workspace too small: %zu < %zu bytes", ws_bytes, plan.ws_bytes);
   }
   dqd::GemmLaunch l;
+  l.rope = nullptr;
   l.wtype = w->type;
   l.data = w->data;
   l.scales = w->scales;
@@ -293,6 +295,75 @@ dqd_status dq_gemm(const dqd_weight* w, const uint16_t* x_bf16, int64_t m, uint1
   l.workspace = plan.ws_bytes > 0 ? workspace : nullptr;
   return check_launch(dqd::launch_dq_gemm(l, plan, reinterpret_cast<cudaStream_t>(stream)),
                       "dq_gemm launch");
+}
+
+dqd_status dq_gemm_qkv_rope_append(const dqd_weight* w, const uint16_t* x_bf16, int32_t b, int32_t wv,
+                                   int32_t hq, int32_t hkv, int32_t d, float rope_base,
+                                   const int32_t* block_table, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, int64_t num_blocks, void* k_pool, void* v_pool,
+                                   int32_t kv_fp8, float k_scale, float v_scale, uint16_t* q_out,
+                                   void* workspace, size_t ws_bytes, dqd_stream stream) {
+  g_last_error.clear();
+  dqd_status st = check_weight(w);
+  if (st != DQD_OK) return st;
+  if (b < 1 || wv < 1 || hq < 1 || hkv < 1 || num_blocks < 1 || max_blocks_per_seq < 1)
+    return fail(DQD_ERR_INVALID_ARG, "dq_gemm_qkv_rope_append needs b, w, hq, hkv, num_blocks, "
+                                     "max_blocks_per_seq >= 1");
+  if (d != 128) return fail(DQD_ERR_UNSUPPORTED, "dq_gemm_qkv_rope_append: head_dim must be 128 (d=%d)", d);
+  const int64_t m = (int64_t)b * wv;
+  if (m > 65536) return fail(DQD_ERR_UNSUPPORTED, "dq_gemm_qkv_rope_append: b * w must be <= 65536");
+  if (w->n != ((int64_t)hq + 2 * (int64_t)hkv) * d)
+    return fail(DQD_ERR_INVALID_ARG, "dq_gemm_qkv_rope_append: W has %lld rows, (hq + 2 hkv) * d = %lld",
+                (long long)w->n, ((long long)hq + 2LL * hkv) * d);
+  if (w->k < 1) return fail(DQD_ERR_INVALID_ARG, "dq_gemm_qkv_rope_append needs k >= 1");
+  if (!(rope_base > 1.f) || rope_base == INFINITY) return fail(DQD_ERR_INVALID_ARG, "rope_base must be finite and > 1");
+  if (kv_fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale == INFINITY || v_scale == INFINITY))
+    return fail(DQD_ERR_INVALID_ARG, "an FP8 cache needs finite positive k_scale and v_scale");
+  const void* p16[] = {x_bf16, q_out, k_pool, v_pool};
+  for (const void* p : p16)
+    if (!p || !aligned16(p)) return fail(DQD_ERR_INVALID_ARG, "dq_gemm_qkv_rope_append: NULL or misaligned pointer");
+  if (!block_table || !context_lens || !aligned4(block_table) || !aligned4(context_lens))
+    return fail(DQD_ERR_INVALID_ARG, "dq_gemm_qkv_rope_append: NULL or misaligned table or context_lens");
+  int sms = 0;
+  if ((st = sm_count(&sms)) != DQD_OK) return st;
+  const dqd::GemmPlan plan = dqd::plan_dq_gemm(w->type, m, w->n, w->k, sms);
+  if (plan.ws_bytes > 0) {
+    if (!workspace || !aligned16(workspace))
+      return fail(DQD_ERR_WORKSPACE, "dq_gemm_qkv_rope_append needs a 16-byte aligned workspace of %zu bytes",
+                  plan.ws_bytes);
+    if (ws_bytes < plan.ws_bytes)
+      return fail(DQD_ERR_WORKSPACE, "dq_gemm_qkv_rope_append workspace too small: %zu < %zu bytes", ws_bytes,
+                  plan.ws_bytes);
+  }
+  dqd::RopeEpi r;
+  dqd::rope_turns((double)rope_base, d, d / 2, r.turns);
+  r.table = block_table;
+  r.ctx = context_lens;
+  r.k_pool = k_pool;
+  r.v_pool = v_pool;
+  r.q_out = q_out;
+  r.num_blocks = num_blocks;
+  r.max_blocks = max_blocks_per_seq;
+  r.w = wv;
+  r.hq = hq;
+  r.hkv = hkv;
+  r.kv_fp8 = kv_fp8 ? 1 : 0;
+  r.k_scale = k_scale;
+  r.v_scale = v_scale;
+  dqd::GemmLaunch l;
+  l.rope = &r;
+  l.wtype = w->type;
+  l.data = w->data;
+  l.scales = w->scales;
+  l.zeros = w->zeros;
+  l.x = x_bf16;
+  l.y = nullptr;  // never written: the epilogue stores into q_out and the pools
+  l.m = m;
+  l.n = w->n;
+  l.k = w->k;
+  l.workspace = plan.ws_bytes > 0 ? workspace : nullptr;
+  return check_launch(dqd::launch_dq_gemm(l, plan, reinterpret_cast<cudaStream_t>(stream)),
+                      "dq_gemm_qkv_rope_append launch");
 }
 
 static dqd_status check_attn_shape(int32_t b, int32_t w, int32_t hq, int32_t hkv, int32_t d,
@@ -372,6 +443,7 @@ static dqd_status prepare_attn(const uint16_t* q, const void* k_pool, const void
   l->block_table = block_table;
   l->max_blocks = max_blocks_per_seq;
   l->context_lens = context_lens;
+  l->max_context = max_context;
   l->b = b;
   l->w = w;
   l->hq = hq;

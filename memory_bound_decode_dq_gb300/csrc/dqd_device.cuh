@@ -238,6 +238,11 @@ constexpr uint32_t kSpinLimit = 1u << 22;
 
 // Bit set in a module's device error word when a bounded wait gives up.
 constexpr uint32_t kErrWaitTimeout = 1u;
+// Bit set when a kernel met an input outside its documented range and clamped
+// it so that every access stays in bounds (a block-table entry outside
+// [0, num_blocks), a context shorter than the verify width or longer than the
+// caller's max_context); the output of that call is then not meaningful.
+constexpr uint32_t kErrBadInput = 2u;
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

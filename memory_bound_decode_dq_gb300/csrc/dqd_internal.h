@@ -107,7 +107,28 @@ struct GemmPlan {
 GemmPlan plan_dq_gemm(int wtype, int64_t m, int64_t n, int64_t k, int num_sms);
 
 
+// The destinations of the QKV projection fused with RoPE and the paged KV
+// append (dq_gemm_qkv_rope_append): the rotation frequencies for head dim 128
+// and what rope_kv_append takes. Passed by value as a kernel parameter.
+struct RopeEpi {
+  uint64_t turns[64];     // base^(-2i/128) / 2pi as fractions of 2^64, i < 64
+  const int32_t* table;   // [b][max_blocks]
+  const int32_t* ctx;     // [b]
+  void* k_pool;           // [num_blocks][hkv][16][128] bf16 or E4M3 codes
+  void* v_pool;
+  uint16_t* q_out;        // [b][w][hq][128] bf16
+  int64_t num_blocks;
+  int max_blocks, w, hq, hkv;
+  int kv_fp8;
+  float k_scale, v_scale;
+};
+
+// Fixed-point rotation frequencies of RoPE: base^(-2i/d) / 2pi as a fraction
+// of 2^64 for i < n (n <= d / 2), computed in double.
+void rope_turns(double base, int d, int n, uint64_t* turns);
+
 struct GemmLaunch {
+  const RopeEpi* rope;  // non-null: the fused QKV + RoPE + append epilogue
   int wtype;
   const void* data;
   const void* scales;
@@ -152,6 +173,7 @@ struct AttnLaunch {
   const int32_t* block_table;
   int max_blocks;
   const int32_t* context_lens;
+  int max_context;  // the caller's bound on context_lens (the plan covers it)
   int b, w, hq, hkv;
   float softmax_scale;
   float k_scale, v_scale;  // FP8 cache only
@@ -162,7 +184,8 @@ struct AttnLaunch {
 cudaError_t launch_attn(const AttnLaunch& a, const AttnPlan& p, cudaStream_t s);
 
 // Library-owned attention scratch (a static __device__ array in attn.cu):
-// its size, and its device address on the current device.
+// its size, and its device address in the current CUDA context (looked up on
+// the first call in each context, cached by context id).
 size_t attn_static_scratch_bytes();
 cudaError_t attn_static_scratch(void** ptr);
 
@@ -182,6 +205,9 @@ cudaError_t launch_quant_int4(const uint16_t* w, int64_t n, int64_t k, uint8_t* 
                               uint8_t* zeros, cudaStream_t s);
 
 // ------------------------------------------------------ RoPE and append --
+
+// ORs the RoPE/append module's device error word into *flags and clears it.
+cudaError_t rope_take_device_error(uint32_t* flags);
 
 cudaError_t launch_rope_kv_append(const uint16_t* qkv, int b, int w, int hq, int hkv, int d, double rope_base,
                                   const int32_t* table, int max_blocks, const int32_t* ctx, int64_t num_blocks,

@@ -8,20 +8,17 @@
 //
 // Grid: (new token, group of 256 (head, pair) units). Token (b, i) sits at
 // position pos = context_lens[b] - w + i, so the cache already counts the new
-// tokens, as the attention expects. Each thread owns one unit: dims 2p, 2p+1
-// of one head of the token's qkv row. The angle pos * theta_p is reduced
-// exactly, in turns: the host computes theta_p / 2pi (theta_p = base^(-2p/d))
-// once per call as a 64-bit fixed-point fraction F_p, and pos * F_p mod 2^64
-// (an integer multiply) is the angle's fraction of a turn to 2^-45 turns for
-// positions up to 2^20 (a binary32 angle would be off by 1e-2 rad there, and
-// fp64 arithmetic is scarce on this part); its top 32 bits, centred on
-// [-1/2, 1/2) turns, feed sincospi in binary32, and the rotation is binary32. q heads go to q_out (bf16, the attention's layout), k heads
-// into the K pool, v heads are copied into the V pool, at slot pos % 16 of
-// physical block block_table[b][pos / 16]. For an FP8 pool the value is
-// divided by the pool's scale (IEEE binary32) and rounded to E4M3 with
-// saturation, like quant_fp8_rowwise.
+// tokens, as the attention expects. Each thread owns VEC consecutive pairs
+// (2p, 2p+1) of one head of the token's qkv row and rotates them with
+// rope_rotate (rope_device.cuh: the angle reduced exactly in turns, sin and
+// cos and the rotation in binary32). q heads go to q_out (bf16, the
+// attention's layout), k heads into the K pool, v heads are copied into the V
+// pool, at slot pos % 16 of physical block block_table[b][pos / 16]. For an
+// FP8 pool the value is divided by the pool's scale (IEEE binary32) and
+// rounded to E4M3 with saturation, like quant_fp8_rowwise.
 #include "dqd_device.cuh"
 #include "dqd_internal.h"
+#include "rope_device.cuh"
 
 #include <cmath>
 
@@ -29,14 +26,12 @@ namespace dqd {
 namespace {
 
 constexpr int kRopeThreads = 256;
-constexpr int kMaxHalfD = 256;
 
-__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
-  uint16_t pair;
-  // cvt packs its first source into the upper byte
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(hi), "f"(lo));
-  return pair;
-}
+// Device error word of this module (kErrBadInput when a block-table entry was
+// clamped into the pool).
+__device__ unsigned int g_rope_error;
+
+constexpr int kMaxHalfD = kRopeMaxHalfD;
 
 struct RopeFreqs {
   uint64_t turns[kMaxHalfD];  // base^(-2p/d) / 2pi as a fraction of 2^64, p < d/2
@@ -44,16 +39,7 @@ struct RopeFreqs {
 
 // Rotates dims (2p, 2p+1) held as one bf16 pair in x, at position pos.
 __device__ __forceinline__ void rope_pair(uint32_t x, int64_t pos, uint64_t turns, float& x0, float& x1) {
-  x0 = __uint_as_float(x << 16);
-  x1 = __uint_as_float(x & 0xFFFF0000u);
-  const uint64_t frac = (uint64_t)pos * turns;  // mod 2^64: the angle in turns
-  float t = (float)(uint32_t)(frac >> 32) * 0x1p-32f;
-  t -= rintf(t);  // [-1/2, 1/2] turns
-  float sv, cv;
-  sincospif(2.f * t, &sv, &cv);
-  const float y0 = x0 * cv - x1 * sv, y1 = x0 * sv + x1 * cv;
-  x0 = y0;
-  x1 = y1;
+  rope_rotate(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u), pos, turns, x0, x1);
 }
 
 // VEC consecutive pairs per thread (4 with 16-byte accesses when d % 8 == 0, else 1).
@@ -99,8 +85,9 @@ rope_kv_append_kernel(const uint16_t* __restrict__ qkv, int w, int hq, int hkv, 
     dst = reinterpret_cast<uint32_t*>(q_out + (row * hq + head) * (int64_t)d) + p;
   } else {
     if (pos < 0 || pos / 16 >= max_blocks) return;  // nowhere to append
-    int32_t phys = table[(int64_t)b * max_blocks + pos / 16];
-    phys = phys < 0 ? 0 : (phys >= num_blocks ? (int32_t)(num_blocks - 1) : phys);
+    const int32_t entry = table[(int64_t)b * max_blocks + pos / 16];
+    const int32_t phys = entry < 0 ? 0 : (entry >= num_blocks ? (int32_t)(num_blocks - 1) : entry);
+    if (phys != entry) atomicOr(&g_rope_error, kErrBadInput);
     const int g = rotate ? head - hq : head - hq - hkv;
     const int64_t elem = (((int64_t)phys * hkv + g) * 16 + pos % 16) * d + 2 * p;
     void* pool = rotate ? k_pool : v_pool;
@@ -108,7 +95,7 @@ rope_kv_append_kernel(const uint16_t* __restrict__ qkv, int w, int hq, int hkv, 
       const float sc = rotate ? k_scale : v_scale;
       uint16_t c[VEC];
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) c[j] = e4m3x2(__fdiv_rn(f[j][0], sc), __fdiv_rn(f[j][1], sc));
+      for (int j = 0; j < VEC; ++j) c[j] = e4m3x2_rn_satfinite(__fdiv_rn(f[j][0], sc), __fdiv_rn(f[j][1], sc));
       uint8_t* o = static_cast<uint8_t*>(pool) + elem;
       if constexpr (VEC == 4) {
         *reinterpret_cast<uint2*>(o) = make_uint2(c[0] | ((uint32_t)c[1] << 16), c[2] | ((uint32_t)c[3] << 16));
@@ -128,16 +115,29 @@ rope_kv_append_kernel(const uint16_t* __restrict__ qkv, int w, int hq, int hkv, 
 
 }  // namespace
 
+void rope_turns(double base, int d, int n, uint64_t* turns) {
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int p = 0; p < n; ++p) {
+    const double t = std::pow(base, -2.0 * p / d) / two_pi;  // < 1/6: fits the fraction
+    turns[p] = (uint64_t)std::ldexp(t, 64);
+  }
+}
+
+cudaError_t rope_take_device_error(uint32_t* flags) {
+  uint32_t v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_rope_error, sizeof v);
+  if (e != cudaSuccess) return e;
+  if (v) e = cudaMemcpyToSymbol(g_rope_error, &zero, sizeof zero);
+  *flags |= v;
+  return e;
+}
+
 cudaError_t launch_rope_kv_append(const uint16_t* qkv, int b, int w, int hq, int hkv, int d, double rope_base,
                                   const int32_t* table, int max_blocks, const int32_t* ctx, int64_t num_blocks,
                                   void* k_pool, void* v_pool, bool kv_fp8, float k_scale, float v_scale,
                                   uint16_t* q_out, cudaStream_t s) {
   RopeFreqs f{};
-  const double two_pi = 6.283185307179586476925286766559;
-  for (int p = 0; p < d / 2 && p < kMaxHalfD; ++p) {
-    const double turns = std::pow(rope_base, -2.0 * p / d) / two_pi;  // < 1/6: fits the fraction
-    f.turns[p] = (uint64_t)std::ldexp(turns, 64);
-  }
+  rope_turns(rope_base, d, d / 2 < kMaxHalfD ? d / 2 : kMaxHalfD, f.turns);
   const int units = (hq + 2 * hkv) * (d / 2);
   const bool vec = d % 8 == 0;  // 4 pairs per thread, 16-byte rows and stores
   const int per_thread = vec ? 4 : 1;

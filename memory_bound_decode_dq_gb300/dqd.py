@@ -31,6 +31,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 DQD_OK, DQD_ERR_INVALID_ARG, DQD_ERR_UNSUPPORTED, DQD_ERR_WORKSPACE, DQD_ERR_CUDA = range(5)
 DQD_W_BF16, DQD_W_FP8_E4M3, DQD_W_INT4_G128 = 0, 1, 2
 DQD_WS_COUNTER_BYTES = 65536
+DQD_DEVICE_ERR_WAIT_TIMEOUT, DQD_DEVICE_ERR_BAD_INPUT = 1, 2
 
 
 class _WeightDesc(ctypes.Structure):
@@ -54,6 +55,9 @@ _SIGS = {
     "rope_kv_append": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _I32, ctypes.c_float, _P, _I32, _P, _I64,
                                       _P, _P, _I32, ctypes.c_float, ctypes.c_float, _P, _P]),
     "spec_verify_sample": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _P, _P, _P, _P]),
+    "dq_gemm_qkv_rope_append": (ctypes.c_int, [ctypes.POINTER(_WeightDesc), _P, _I32, _I32, _I32, _I32, _I32,
+                                               ctypes.c_float, _P, _I32, _P, _I64, _P, _P, _I32, ctypes.c_float,
+                                               ctypes.c_float, _P, _P, _SZ, _P]),
     "dq_gemm_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(_WeightDesc), _I64, ctypes.POINTER(_SZ)]),
     "dq_gemm": (ctypes.c_int, [ctypes.POINTER(_WeightDesc), _P, _I64, _P, _P, _SZ, _P]),
     "gqa_decode_attn_workspace_bytes": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32,
@@ -91,7 +95,9 @@ def version() -> str:
 
 def device_errors() -> int:
     """OR of the kernels' device error flags since the last call (0: none;
-    bit 0: a bounded wait on an asynchronous copy gave up). Synchronises."""
+    DQD_DEVICE_ERR_WAIT_TIMEOUT: a bounded wait on an asynchronous copy gave
+    up; DQD_DEVICE_ERR_BAD_INPUT: an input outside its documented range was
+    clamped). Synchronises and clears the flags."""
     v = ctypes.c_uint32(0)
     _check(_lib.dqd_device_errors(ctypes.byref(v)), "dqd_device_errors")
     return int(v.value)
@@ -452,4 +458,42 @@ def rope_kv_append(qkv: torch.Tensor, b: int, w: int, hq: int, hkv: int, k_pool:
                                block_table.shape[1], _ptr(context_lens), k_pool.shape[0], _ptr(k_pool),
                                _ptr(v_pool), 1 if fp8 else 0, float(k_scale), float(v_scale), _ptr(q_out),
                                _stream(stream)), "rope_kv_append")
+    return q_out
+
+
+def dq_gemm_qkv_rope_append(weight: Weight, x: torch.Tensor, b: int, w: int, hq: int, hkv: int,
+                            k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
+                            context_lens: torch.Tensor, rope_base: float = 10000.0, k_scale: float = 1.0,
+                            v_scale: float = 1.0, q_out: torch.Tensor | None = None,
+                            ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The QKV projection of the new tokens fused with rope_kv_append: x bf16
+    [b*w, k], weight [(hq + 2*hkv) * 128, k]; rotates q and k, appends k and v
+    to the paged cache (bf16 pools, or uint8 / float8_e4m3fn for an FP8 cache
+    with k_scale, v_scale). Returns q_out bf16 [b, w, hq, 128]."""
+    _need(x, "x", _B16)
+    dev = x.device
+    f8_types = _U8 + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+    fp8 = k_pool.dtype in f8_types
+    _need(k_pool, "k_pool", f8_types if fp8 else _B16, dev)
+    _need(v_pool, "v_pool", f8_types if fp8 else _B16, dev)
+    _need(block_table, "block_table", _I32T, dev)
+    _need(context_lens, "context_lens", _I32T, dev)
+    d = 128
+    if tuple(x.shape) != (b * w, weight.k) or weight.n != (hq + 2 * hkv) * d \
+            or tuple(k_pool.shape[1:]) != (hkv, 16, d) or v_pool.shape != k_pool.shape:
+        raise ValueError("dq_gemm_qkv_rope_append: x must be [b*w, k], W [(hq+2*hkv)*128, k], "
+                         "pools [num_blocks, hkv, 16, 128]")
+    if q_out is None:
+        q_out = torch.empty((b, w, hq, d), dtype=torch.bfloat16, device=dev)
+    _need(q_out, "q_out", _B16, dev)
+    need = dq_gemm_workspace_bytes(weight, b * w)
+    if ws is None:
+        ws = workspace(need, dev, stream)
+    desc = weight.desc()
+    _check(_lib.dq_gemm_qkv_rope_append(ctypes.byref(desc), _ptr(x), b, w, hq, hkv, d, float(rope_base),
+                                        _ptr(block_table), block_table.shape[1], _ptr(context_lens),
+                                        k_pool.shape[0], _ptr(k_pool), _ptr(v_pool), 1 if fp8 else 0,
+                                        float(k_scale), float(v_scale), _ptr(q_out), _ptr(ws),
+                                        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+           "dq_gemm_qkv_rope_append")
     return q_out

@@ -17,7 +17,7 @@
  *   [CS10] "第 10 讲：推理" (CS336 lecture 10 notes), semidirectx.com
  *   [ATC]  "AcceptedTokens 阅读笔记" (reading notes on speculative-decoding energy), zhongzhuzhou.org
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent (each is also listed in the design notes):
  *   - INT4 g128: unsigned codes 0..15 with a 4-bit zero point and a bf16 scale
  *     per 128-weight group; deq = bf16_RNE((q - z) * s), one rounding.
  *   - FP8 row-wise: scale = fp32(max|w|) / 448 (IEEE binary32 division),

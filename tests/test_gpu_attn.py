@@ -157,6 +157,7 @@ def test_stale_pool_contents_do_not_leak(dev, dqd):
 
 
 def test_context_shorter_than_width_gives_zero_rows(dev, dqd):
+    assert dqd.device_errors() == 0
     kv = synth.paged_kv(8, "kv", (10,), 1)
     q = synth.normal_bf16(8, "q", (1, 4, 2, 128))
     out = f64(run(dqd, dev, q, kv, 1, ctx=np.array([2], np.int32), max_context=10))
@@ -165,6 +166,44 @@ def test_context_shorter_than_width_gives_zero_rows(dev, dqd):
     ref_rows = oracle.gqa_decode_attn(q[:, 2:], kv.k_pool, kv.v_pool, kv.block_table, np.array([2], np.int32),
                                       1, 1 / math.sqrt(128))
     assert_close(out[:, 2:], ref_rows, what="rows with keys")
+    # a context below the width breaks the caller's precondition: reported once
+    assert dqd.device_errors() == dqd.DQD_DEVICE_ERR_BAD_INPUT
+    assert dqd.device_errors() == 0
+
+
+def test_out_of_range_table_entry_is_clamped_and_reported(dev, dqd):
+    """A corrupt block-table entry reads a block inside the pool (no fault),
+    raises the bad-input flag, and leaves the context usable."""
+    assert dqd.device_errors() == 0
+    ctx = (40, 70)
+    kv = synth.paged_kv(11, "kv", ctx, 2)
+    q = synth.normal_bf16(11, "q", (2, 1, 8, 128))
+    bad = kv.block_table.copy()
+    bad[1, 2] = kv.num_blocks + 5          # past the pool: clamped to the last block
+    out = f64(run(dqd, dev, q, kv, 2, table=bad))
+    assert np.all(np.isfinite(out))
+    assert_close(out[0], ref(q, kv, 2)[0], what="the sequence with a valid table")
+    assert dqd.device_errors() == dqd.DQD_DEVICE_ERR_BAD_INPUT
+    bad[1, 2] = -3                         # negative: clamped to block 0
+    run(dqd, dev, q, kv, 2, table=bad)
+    assert dqd.device_errors() == dqd.DQD_DEVICE_ERR_BAD_INPUT
+    # the next, valid call is correct and raises nothing
+    assert_close(f64(run(dqd, dev, q, kv, 2)), ref(q, kv, 2), what="after the clamped calls")
+    assert dqd.device_errors() == 0
+
+
+def test_context_above_max_context_is_taken_as_max_context(dev, dqd):
+    """context_lens[b] > max_context breaks the caller's precondition: the
+    kernel attends as if the context were max_context (bit-identical to that
+    call) and raises the bad-input flag."""
+    assert dqd.device_errors() == 0
+    kv = synth.paged_kv(12, "kv", (300, 300), 2)
+    q = synth.normal_bf16(12, "q", (2, 3, 8, 128))
+    over = bits(run(dqd, dev, q, kv, 2, ctx=np.array([300, 260], np.int32), max_context=260))
+    assert dqd.device_errors() == dqd.DQD_DEVICE_ERR_BAD_INPUT
+    same = bits(run(dqd, dev, q, kv, 2, ctx=np.array([260, 260], np.int32), max_context=260))
+    assert np.array_equal(over, same)
+    assert dqd.device_errors() == 0
 
 
 def test_rejects_bad_arguments(dev, dqd):

@@ -130,5 +130,21 @@ def test_rejects_bad_arguments(dev, dqd):
         dqd.rope_kv_append(qkv, 2, 1, 32, 8, kp, kp, t, c, rope_base=0.5)
 
 
+def test_out_of_range_table_entry_is_clamped_and_reported(dev, dqd):
+    """A table entry past the pool appends into the pool's last block (no
+    write outside the pool) and raises the bad-input flag once."""
+    assert dqd.device_errors() == 0
+    B, W, hq, hkv, d = 1, 2, 8, 2, 128
+    qkv, table, nblk, ctx = _case(12, B, W, hq, hkv, d, (40,))
+    kp = bf(np.zeros((nblk, hkv, 16, d), np.uint16), dev)
+    vp = bf(np.zeros((nblk, hkv, 16, d), np.uint16), dev)
+    bad = table.copy()
+    bad[0, (int(ctx[0]) - 1) // 16] = nblk + 7
+    dqd.rope_kv_append(bf(qkv, dev), B, W, hq, hkv, kp, vp, i32(bad, dev), i32(ctx, dev))
+    assert dqd.device_errors() == dqd.DQD_DEVICE_ERR_BAD_INPUT
+    assert np.any(bits(vp)[nblk - 1] != 0)     # the clamped append landed in the last block
+    assert dqd.device_errors() == 0
+
+
 def test_no_device_error_flags(dev, dqd):
     assert dqd.device_errors() == 0
