@@ -75,6 +75,17 @@ def rope_append_bytes(tokens: int, hq: int, hkv: int, d: int = 128, kv_bytes_per
     return float(tokens * ((hq + 2 * hkv) * d * 2 + hq * d * 2 + 2 * hkv * d * kv_bytes_per_element + 8))
 
 
+def qkv_rope_append_bytes(wtype: int, tokens: int, k: int, hq: int, hkv: int, d: int = 128,
+                          kv_bytes_per_element: int = 2) -> float:
+    """The QKV projection fused with RoPE + KV append: the projection's
+    weights and activations, then per token its rotated q (bf16), its k and v
+    written into the cache, its context length and its block-table entry (the
+    qkv row itself never reaches memory)."""
+    n = (hq + 2 * hkv) * d
+    return float(weight_bytes(wtype, n, k) + 2.0 * tokens * k +
+                 tokens * (hq * d * 2 + 2 * hkv * d * kv_bytes_per_element + 8))
+
+
 def verify_bytes(batch: int, width: int, vocab: int) -> float:
     """Greedy verify: the target's bf16 logits, the drafts, the predictions,
     the counts and the context lengths (read and written)."""

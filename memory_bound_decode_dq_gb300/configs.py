@@ -67,6 +67,23 @@ class RopeCase:
 
 
 @dataclass(frozen=True)
+class QkvRopeCase:
+    """The QKV projection of the new tokens fused with RoPE and the KV append
+    (dq_gemm_qkv_rope_append): x [batch * width, k], W [(hq + 2 hkv) * 128, k],
+    bf16 paged cache."""
+    name: str
+    wtype: int
+    batch: int
+    width: int
+    hq: int
+    hkv: int
+    k: int
+    context: tuple
+    rope_base: float = 500000.0
+    d: int = 128
+
+
+@dataclass(frozen=True)
 class Workload:
     name: str
     seed: int
@@ -74,6 +91,7 @@ class Workload:
     attns: tuple = field(default_factory=tuple)
     verifies: tuple = field(default_factory=tuple)
     ropes: tuple = field(default_factory=tuple)
+    qkv_ropes: tuple = field(default_factory=tuple)
 
 
 def _ctx_uniform(seed: int, batch: int, lo: int, hi: int) -> tuple:
@@ -91,15 +109,17 @@ def tiny() -> Workload:
 
 def llama3_8b_b1() -> Workload:
     """Llama-3-8B-shaped decode layer at batch 1: four projections in BF16 and
-    INT4 g128, the rotary embedding and KV append of the new token, attention
-    32/8 heads over 8192 paged tokens."""
+    INT4 g128, the BF16 QKV projection fused with the rotary embedding and KV
+    append of the new token, attention 32/8 heads over 8192 paged tokens."""
     g = []
     for wt in (W_BF16, W_INT4_G128):
         for name, n, k in LLAMA3_8B_PROJ:
+            if wt == W_BF16 and name == "qkv":
+                continue  # fused with RoPE and the append below
             g.append(GemmCase(f"{name}_{WTYPE_NAMES[wt]}", wt, 1, n, k))
     return Workload("llama3_8b_decode_b1_ctx8192", 1, gemms=tuple(g),
                     attns=(AttnCase("attn_32_8_ctx8192", 1, 1, 32, 8, (8192,)),),
-                    ropes=(RopeCase("rope_append_32_8", 1, 1, 32, 8, (8192,)),))
+                    qkv_ropes=(QkvRopeCase("qkv_bf16_rope_append_32_8", W_BF16, 1, 1, 32, 8, 4096, (8192,)),))
 
 
 def dense70b_b32() -> Workload:
@@ -127,12 +147,15 @@ def verify_8b() -> Workload:
         for width in (6, 16):
             m = batch * width
             for name, n, k in LLAMA3_8B_PROJ:
+                if name == "qkv" and batch == 64 and width == 16:
+                    continue  # fused with RoPE and the append below
                 g.append(GemmCase(f"{name}_int4_m{m}", W_INT4_G128, m, n, k))
             a.append(AttnCase(f"attn_verify_b{batch}_w{width}", batch, width, 32, 8,
                               _ctx_uniform(3, batch, 512, 4096)))
             v.append(VerifyCase(f"accept_greedy_b{batch}_w{width}", batch, width, LLAMA3_8B_VOCAB))
-    r = (RopeCase("rope_append_b64_w16", 64, 16, 32, 8, _ctx_uniform(3, 64, 512, 4096)),)
-    return Workload("verify_8b_int4", 3, gemms=tuple(g), attns=tuple(a), verifies=tuple(v), ropes=r)
+    r = (QkvRopeCase("qkv_int4_m1024_rope_append_b64_w16", W_INT4_G128, 64, 16, 32, 8, 4096,
+                     _ctx_uniform(3, 64, 512, 4096)),)
+    return Workload("verify_8b_int4", 3, gemms=tuple(g), attns=tuple(a), verifies=tuple(v), qkv_ropes=r)
 
 
 def longctx_70b_b8() -> Workload:

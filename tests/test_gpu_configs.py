@@ -227,7 +227,69 @@ def check_rope(dqd, dev, case, seed, max_tokens=16):
             assert np.array_equal(bits(vr[row]), one[0, (case.hq + case.hkv + g) * case.d:(case.hq + case.hkv + g + 1) * case.d])
 
 
+# the standalone RoPE + append at the shapes of the 8B decode and verify steps
+ROPE_CASES = [configs.RopeCase("rope_append_32_8", 1, 1, 32, 8, (8192,)),
+              configs.RopeCase("rope_append_b64_w16", 64, 16, 32, 8, configs._ctx_uniform(3, 64, 512, 4096))]
+
+
+@pytest.mark.parametrize("case", ROPE_CASES, ids=lambda c: c.name)
+def test_rope_append(dev, dqd, case):
+    check_rope(dqd, dev, case, 3)
+
+
+def check_qkv_rope(dqd, dev, case, seed, max_tokens=12):
+    """The bench's fused QKV + RoPE + append call at full size: bit for bit
+    equal to the two-call chain (dq_gemm, rope_kv_append) on the same inputs,
+    and sampled tokens against the oracle's float64 projection and rotation
+    (rotated outputs bounded per pair: the rotation is an isometry)."""
+    d, hq, hkv = case.d, case.hq, case.hkv
+    n, k, m = (hq + 2 * hkv) * d, case.k, case.batch * case.width
+    ctx = np.asarray(case.context, np.int32)
+    table, nblk = synth.block_table(seed, case.name + ".table", ctx, True)
+    x = synth.normal_bf16(seed, case.name + ".x", (m, k), device=dev)
+    if case.wtype == oracle.W_INT4_G128:
+        wq = synth.int4_weight(seed, case.name, n, k, device=dev)
+        weight = dqd.Weight.int4(dqd.pack_int4_g128(wq.codes, wq.scales, wq.zeros))
+        host = (wq.codes.cpu().numpy(), bits(wq.scales), wq.zeros.cpu().numpy())
+    else:
+        w = synth.normal_bf16(seed, case.name, (n, k), 0.02, device=dev)
+        weight = dqd.Weight.bf16(w)
+        host = (bits(w), None, None)
+    t, c = torch.from_numpy(table).to(dev), torch.from_numpy(ctx).to(dev)
+    kp = torch.zeros((nblk, hkv, 16, d), dtype=torch.bfloat16, device=dev)
+    vp = torch.zeros_like(kp)
+    kp2, vp2 = kp.clone(), vp.clone()
+    q = dqd.dq_gemm_qkv_rope_append(weight, x, case.batch, case.width, hq, hkv, kp, vp, t, c,
+                                    rope_base=case.rope_base)
+    q2 = dqd.rope_kv_append(dqd.dq_gemm(weight, x), case.batch, case.width, hq, hkv, kp2, vp2, t, c,
+                            rope_base=case.rope_base)
+    for a, b_ in ((q, q2), (kp, kp2), (vp, vp2)):
+        assert torch.equal(a.view(torch.int16), b_.view(torch.int16)), f"{case.name}: fused differs from the chain"
+    toks = sample_rows(m, max_tokens, seed)
+    y = oracle.dq_gemm(case.wtype, *host, bits(x[torch.as_tensor(toks, device=dev)])).reshape(len(toks), -1, d)
+    kr, vr = kp.view(-1, d), vp.view(-1, d)
+    for j, tk in enumerate(toks):
+        b, i = divmod(int(tk), case.width)
+        pos = float(ctx[b] - case.width + i)
+        rq = oracle.rope(y[j, :hq], np.full(hq, pos), case.rope_base)
+        rk = oracle.rope(y[j, hq:hq + hkv], np.full(hkv, pos), case.rope_base)
+        got_q = f64(q[b, i]).reshape(-1, 2)
+        slot = oracle.rope_kv_append(oracle.bf16_round(y[j:j + 1].reshape(1, -1)), 1, 1, hq, hkv,
+                                     case.rope_base, ctx[b:b + 1] - (case.width - 1 - i), table[b:b + 1],
+                                     nblk)[3][0, 0]
+        got_k = np.stack([f64(kr[int(slot) + 16 * g]) for g in range(hkv)])
+        got_v = np.stack([f64(vr[int(slot) + 16 * g]) for g in range(hkv)])
+        for name, got, ref in (("q", got_q, rq), ("k", got_k, rk)):
+            ref = ref.reshape(-1, 2)
+            rms = float(np.sqrt(np.mean(ref ** 2)))
+            bound = 1e-2 * (np.linalg.norm(ref, axis=1, keepdims=True) + rms)
+            assert np.all(np.abs(got.reshape(-1, 2) - ref) <= bound), f"{case.name} {name} token {tk}"
+        assert_close(got_v, y[j, hq + hkv:], what=f"{case.name} v token {tk}")
+
+
 @pytest.mark.parametrize("wl", ["llama3_8b_b1", "verify_8b"])
-def test_rope_append(dev, dqd, wl):
-    for case in WORKLOADS[wl].ropes:
-        check_rope(dqd, dev, case, WORKLOADS[wl].seed)
+def test_qkv_rope_append(dev, dqd, wl):
+    cases = WORKLOADS[wl].qkv_ropes
+    assert cases
+    for case in cases:
+        check_qkv_rope(dqd, dev, case, WORKLOADS[wl].seed)
