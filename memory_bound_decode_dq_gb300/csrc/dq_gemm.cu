@@ -159,6 +159,12 @@ __device__ __forceinline__ uint32_t lds8(uint32_t saddr) {
   return r;
 }
 
+// Activation row a lane reads for token column r of its MMA tiles: columns
+// past the staged rows read row 0 instead of branching around the load (an
+// MMA column depends only on its own B column, and those outputs are never
+// stored), so no quarter-warp diverges at m < 8.
+__device__ __forceinline__ int xrow(int r, int rows) { return r < rows ? r : 0; }
+
 // One warp's MMAs for one stage. acc[j][*]: rows (g, g+8) x token columns
 // (8j + 2t, 8j + 2t + 1). ngroups bounds the INT4 groups inside [kbeg, kend).
 template <int WT, int MT>
@@ -167,7 +173,6 @@ __device__ __forceinline__ void compute_stage(float (&acc)[MT][4], uint32_t slot
   using C = Cfg<WT, MT>;
   const int g = lane >> 2, t = lane & 3;
   const uint32_t xbase = slot + C::WSTAGE + C::MSTAGE;
-  const uint4 zero = make_uint4(0, 0, 0, 0);
   if constexpr (WT == kBF16) {
     const uint32_t wb = slot + warp * 16 * C::WROWB;
 #pragma unroll
@@ -178,8 +183,8 @@ __device__ __forceinline__ void compute_stage(float (&acc)[MT][4], uint32_t slot
       uint4 xv[MT];
 #pragma unroll
       for (int j = 0; j < MT; ++j) {
-        const int r = 8 * j + g;
-        xv[j] = r < ra ? lds128(xbase + r * C::XROWB + ((unit ^ xswz<WT>(r)) << 4)) : zero;
+        const int r = xrow(8 * j + g, ra);
+        xv[j] = lds128(xbase + r * C::XROWB + ((unit ^ xswz<WT>(r)) << 4));
       }
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -199,10 +204,10 @@ __device__ __forceinline__ void compute_stage(float (&acc)[MT][4], uint32_t slot
       uint4 xa[MT], xb[MT];
 #pragma unroll
       for (int j = 0; j < MT; ++j) {
-        const int r = 8 * j + g;
+        const int r = xrow(8 * j + g, ra);
         const int u0 = 8 * d + 2 * t;
-        xa[j] = r < ra ? lds128(xbase + r * C::XROWB + ((u0 ^ xswz<WT>(r)) << 4)) : zero;
-        xb[j] = r < ra ? lds128(xbase + r * C::XROWB + (((u0 + 1) ^ xswz<WT>(r)) << 4)) : zero;
+        xa[j] = lds128(xbase + r * C::XROWB + ((u0 ^ xswz<WT>(r)) << 4));
+        xb[j] = lds128(xbase + r * C::XROWB + (((u0 + 1) ^ xswz<WT>(r)) << 4));
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -235,9 +240,9 @@ __device__ __forceinline__ void compute_stage(float (&acc)[MT][4], uint32_t slot
         uint4 xv[MT];
 #pragma unroll
         for (int j = 0; j < MT; ++j) {
-          const int r = 8 * j + g;
+          const int r = xrow(8 * j + g, ra);
           const int unit = 16 * jg + 4 * c + t;
-          xv[j] = r < ra ? lds128(xbase + r * C::XROWB + ((unit ^ xswz<WT>(r)) << 4)) : zero;
+          xv[j] = lds128(xbase + r * C::XROWB + ((unit ^ xswz<WT>(r)) << 4));
         }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -614,7 +619,6 @@ __global__ void __launch_bounds__(Int4Cfg<MT, W>::THREADS)
         z[j] = (tile_ok && g0 + j < gend) ? ldg_u8(a.wz + (tile * G + g0 + j) * 8 + g) : 0u;
     };
     if (nst > 0 && !zbulk) load_zeros(0, znext);
-    const uint4 zero = make_uint4(0, 0, 0, 0);
     for (int s = 0; s < nst; ++s) {
       const int slot_i = s % NS;
       if (!mbar_wait(full0 + 8 * slot_i, (s / NS) & 1)) {
@@ -650,8 +654,8 @@ __global__ void __launch_bounds__(Int4Cfg<MT, W>::THREADS)
             uint4 xv[MT];
 #pragma unroll
             for (int j = 0; j < MT; ++j) {
-              const int r = 8 * j + g;
-              xv[j] = r < rows_valid ? lds128(xb + r * C::XSTR + (jg * 128 + 32 * c + 8 * t) * 2) : zero;
+              const int r = xrow(8 * j + g, rows_valid);
+              xv[j] = lds128(xb + r * C::XSTR + (jg * 128 + 32 * c + 8 * t) * 2);
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {

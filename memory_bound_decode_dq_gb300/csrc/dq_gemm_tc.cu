@@ -68,6 +68,7 @@ constexpr int kAccCols = 256;                 // column offset of the odd slabs'
 constexpr int kRingBytes = 222 * 1024;        // all rings
 constexpr int kSmem = kRingBytes + 1024;      // + alignment slack
 static_assert(kSmem + 1024 <= 227 * 1024, "shared memory");
+static_assert(256 * kRows * 2 <= kRingBytes, "the fused RoPE epilogue stages up to 256 tokens x 128 rows of bf16 in the rings");
 
 // Code slot bytes per weight type (INT4: codes + scales of one 64-k slab;
 // FP8: a 128 x 128 code tile, two slabs, so that every row is one full
@@ -643,17 +644,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
       }
       if (ROPE && !part) {
-        // rotation partner: row ^ 1, the neighbouring lane of this warp
-        bool bad = false;
+        // stage the projection's bf16 outputs, [token][128 rows of one head],
+        // in the ring memory (free once `done` has fired); every warp of the
+        // CTA then rotates and places them, four pairs per thread, after the
+        // barrier below
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float vb = bf16_round(__uint_as_float(r[j]) * rscale);
-          const float partner = __shfl_xor_sync(0xffffffffu, vb, 1);
-          const int64_t mm = m0 + cc * 32 + j;
-          if constexpr (ROPE)
-            if (good && row < a.n && cc * 32 + j < a.ntok && mm < a.m) bad |= rope_store(epi, mm, row, vb, partner);
-        }
-        if (bad) atomicOr(&g_tc_error, kErrBadInput);
+        for (int j = 0; j < 32; ++j)
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(aring + (cc * 32 + j) * 256 + (quarter * 32 + lane) * 2),
+                       "h"(f32_to_bf16(__uint_as_float(r[j]) * rscale))
+                       : "memory");
       } else if (good && row < a.n) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -689,6 +688,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if constexpr (ROPE) {
+    if (a.splits == 1) {
+      // the CTA's 128 rows are one head (n is a multiple of 128); unit u is
+      // eight dims of one token
+      const int toks = (int)min((int64_t)a.ntok, a.m - m0);
+      const int head = (int)(row0 >> 7);
+      bool bad = false;
+      for (int u = threadIdx.x; u < toks * 16; u += kThreads) {
+        const int tl = u >> 4, ch = u & 15;
+        const int64_t mm = m0 + tl;
+        const uint4 x = lds128(aring + tl * 256 + ch * 16);
+        bad |= rope_store8(epi, mm, (int)(mm / epi.w), (int)(mm % epi.w), head, ch * 8, x);
+      }
+      if (bad) atomicOr(&g_tc_error, kErrBadInput);
+    }
   }
 }
 

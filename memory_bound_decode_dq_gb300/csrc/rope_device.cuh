@@ -57,18 +57,18 @@ struct EpiOf<true> {
   using type = RopeEpi;
 };
 
-// Stores element (token mm, column nn) of a QKV projection whose row holds
-// the heads q_0.., k_0.., v_0.. (head dim 128). v is this element's value as
-// the projection rounds it (bf16, widened back to binary32); partner is the
-// same for column nn ^ 1 of the same token. q and k columns are rotated as a
-// pair at position ctx[b] - w + i (token mm = b * w + i): q goes to q_out,
-// k and v to row pos % 16 of block table[b][pos / 16] (nothing when the
-// position is below 0 or past the table). Returns true when a table entry
-// outside [0, num_blocks) was clamped into range.
-__device__ __forceinline__ bool rope_store(const RopeEpi& r, int64_t mm, int64_t nn, float v, float partner) {
+// Stores element (token mm = b * w + i, column nn) of a QKV projection whose
+// row holds the heads q_0.., k_0.., v_0.. (head dim 128). v is this element's
+// value as the projection rounds it (bf16, widened back to binary32); partner
+// is the same for column nn ^ 1 of the same token. q and k columns are
+// rotated as a pair at position ctx[b] - w + i: q goes to q_out, k and v to
+// row pos % 16 of block table[b][pos / 16] (nothing when the position is
+// below 0 or past the table). Returns true when a table entry outside
+// [0, num_blocks) was clamped into range.
+__device__ __forceinline__ bool rope_store_bi(const RopeEpi& r, int64_t mm, int b, int i, int64_t nn, float v,
+                                              float partner) {
   const int head = (int)(nn >> 7), dim = (int)(nn & 127);
   const bool odd = dim & 1;
-  const int b = (int)(mm / r.w), i = (int)(mm % r.w);
   const int64_t pos = (int64_t)r.ctx[b] - r.w + i;
   const bool rotated = head < r.hq + r.hkv;
   float val = v;
@@ -94,6 +94,57 @@ __device__ __forceinline__ bool rope_store(const RopeEpi& r, int64_t mm, int64_t
     static_cast<uint16_t*>(rotated ? r.k_pool : r.v_pool)[elem] = f32_to_bf16(val);
   }
   return phys != entry;
+}
+
+// Eight consecutive dims [dim0, dim0 + 8) of head `head` for token mm = b * w
+// + i, as four bf16 pairs in x: the same arithmetic and placement as
+// rope_store_bi on each element, with 16-byte stores (8-byte for E4M3 codes).
+__device__ __forceinline__ bool rope_store8(const RopeEpi& r, int64_t mm, int b, int i, int head, int dim0,
+                                            uint4 x) {
+  const int64_t pos = (int64_t)r.ctx[b] - r.w + i;
+  const bool rotated = head < r.hq + r.hkv;
+  uint32_t y[4];
+  float f[4][2];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t xj = word(x, j);
+    const float x0 = __uint_as_float(xj << 16), x1 = __uint_as_float(xj & 0xFFFF0000u);
+    if (rotated) {
+      rope_rotate(x0, x1, pos, r.turns[(dim0 >> 1) + j], f[j][0], f[j][1]);
+      y[j] = pack_bf16x2(f[j][0], f[j][1]);
+    } else {
+      f[j][0] = x0;
+      f[j][1] = x1;
+      y[j] = xj;  // v: the bits as they came
+    }
+  }
+  if (head < r.hq) {
+    *reinterpret_cast<uint4*>(r.q_out + (mm * r.hq + head) * 128 + dim0) = make_uint4(y[0], y[1], y[2], y[3]);
+    return false;
+  }
+  if (pos < 0 || pos / 16 >= r.max_blocks) return false;  // nowhere to append
+  const int32_t entry = r.table[(int64_t)b * r.max_blocks + pos / 16];
+  const int32_t phys = entry < 0 ? 0 : (entry >= r.num_blocks ? (int32_t)(r.num_blocks - 1) : entry);
+  const int g = rotated ? head - r.hq : head - r.hq - r.hkv;
+  const int64_t elem = (((int64_t)phys * r.hkv + g) * 16 + pos % 16) * 128 + dim0;
+  if (r.kv_fp8) {
+    const float sc = rotated ? r.k_scale : r.v_scale;
+    uint16_t c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j] = e4m3x2_rn_satfinite(__fdiv_rn(f[j][0], sc), __fdiv_rn(f[j][1], sc));
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(rotated ? r.k_pool : r.v_pool) + elem) =
+        make_uint2(c[0] | ((uint32_t)c[1] << 16), c[2] | ((uint32_t)c[3] << 16));
+  } else {
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(rotated ? r.k_pool : r.v_pool) + elem) =
+        make_uint4(y[0], y[1], y[2], y[3]);
+  }
+  return phys != entry;
+}
+
+// As rope_store_bi, with the token's sequence and position in it derived
+// from mm.
+__device__ __forceinline__ bool rope_store(const RopeEpi& r, int64_t mm, int64_t nn, float v, float partner) {
+  return rope_store_bi(r, mm, (int)(mm / r.w), (int)(mm % r.w), nn, v, partner);
 }
 
 // The projection's bf16 rounding of an fp32 output, widened back to binary32.
