@@ -43,6 +43,7 @@
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
+#include <type_traits>
 
 namespace dqd {
 namespace {
@@ -54,6 +55,7 @@ constexpr int kMaxN = 256;    // tokens per CTA at most (MMA N)
 constexpr int kSlabK = 64;    // k per slab: one 128-byte swizzle row of bf16
 constexpr int kABytes = kRows * kSlabK * 2;   // 16 KB
 constexpr int kMaxASlots = 12;
+constexpr int kMaxTSlots = 6;                 // A stages in tensor memory (64 columns each)
 constexpr int kMaxBSlots = 16;
 constexpr int kMaxCSlots = 12;
 constexpr int kI4Codes = 8 * 512;             // INT4: 8 tiles x half a group block
@@ -97,9 +99,27 @@ __host__ __device__ constexpr int code_slot(int wt) {
 struct Rings {
   int nas, nbs, ncs;
 };
-__host__ __device__ inline Rings rings(int wt, int ntok) {
+// Tensor-memory columns of each accumulator when A lives in tensor memory
+// (N tokens, rounded up to the 32-column reads of the epilogue).
+__host__ __device__ constexpr int tc_acc_cols(int ntok) {
+  return (ntok + 31) & ~31;
+}
+__host__ __device__ inline Rings rings(int wt, int ntok, bool atm = false) {
   const int bslot = ntok * kSlabK * 2;
   Rings r;
+  if (atm) {
+    // A in tensor memory, in stages of two slabs (128 k): the two
+    // accumulators take the first columns, every A stage 64 columns (128 rows
+    // x 128 k of bf16) of the rest; shared memory holds activation stages
+    // (two slabs each, about 64 KB) and code slots (one stage each, the
+    // rest). Every ring holds an even number of stages: the two issuers take
+    // alternate stages, and so do the two dequantising groups, so each code
+    // slot always serves the same group.
+    r.nas = min(kMaxTSlots, (kTmemCols - 2 * tc_acc_cols(ntok)) / 64) & ~1;
+    r.nbs = (min(kMaxBSlots, max(2, (64 * 1024) / (2 * bslot))) + 1) & ~1;
+    r.ncs = min(kMaxCSlots, (kRingBytes - r.nbs * 2 * bslot) / code_slot(wt)) & ~1;
+    return r;
+  }
   r.nbs = (min(kMaxBSlots, max(3, (64 * 1024) / bslot)) + 1) & ~1;
   // keep room for four A slots and two code slots
   if (r.nbs > 2 && r.nbs * bslot + 4 * kABytes + 2 * code_slot(wt) > kRingBytes) r.nbs -= 2;
@@ -154,6 +174,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint6
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same with A read from tensor memory (128 lanes = rows, K along columns,
+// two bf16 per 32-bit column, the lower k in the low half).
+__device__ __forceinline__ void umma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint32_t mbar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
                : "memory");
@@ -176,6 +207,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit values per warp: lane t of the warp writes
+// row (its quarter's first lane + t), columns taddr .. taddr + 31.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
@@ -294,26 +341,34 @@ __device__ __forceinline__ bool reduce_splits(const TcArgs& a, int64_t r0, int r
   return bad;
 }
 
-template <int WT, bool ROPE>
+// ATM: A (the dequantised weights) in tensor memory, written by the
+// dequantising warps with tcgen05.st (FP8, N <= 128); otherwise in shared memory.
+template <int WT, bool ROPE, bool ATM>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                       const __grid_constant__ CUtensorMap tms, const TcArgs a,
                       const __grid_constant__ typename EpiOf<ROPE>::type epi) {
   constexpr int CSLOT = code_slot(WT);
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * kMaxCSlots + 2 * kMaxASlots + 2 * kMaxBSlots + 1];
+  constexpr int kMaxA = kMaxASlots > kMaxTSlots ? kMaxASlots : kMaxTSlots;
+  __shared__ __align__(8) uint64_t bars[2 * kMaxCSlots + 2 * kMaxA + 2 * kMaxBSlots + 1];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int last_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Rings R = rings(WT, a.ntok);
+  const Rings R = rings(WT, a.ntok, ATM);
   const uint32_t bslot_bytes = (uint32_t)a.ntok * kSlabK * 2;
   const int nbs = R.nbs, nas = R.nas, ncs = R.ncs;
-  const uint32_t aring = (smem_addr(smem_raw) + 1023u) & ~1023u;
-  const uint32_t bring = aring + nas * kABytes;
-  const uint32_t cring = bring + nbs * bslot_bytes;
+  // tensor memory: accumulators at columns 0 and acc_off; with ATM the A
+  // slots from column a_tcol on
+  const uint32_t acc_off = ATM ? (uint32_t)tc_acc_cols(a.ntok) : (uint32_t)kAccCols;
+  const uint32_t a_tcol = 2 * acc_off;
+  const uint32_t aring = (smem_addr(smem_raw) + 1023u) & ~1023u;  // the ring memory (A slots first unless ATM)
+  const uint32_t bring = aring + (ATM ? 0 : nas) * kABytes;
+  const uint32_t bstage = (ATM ? 2 : 1) * bslot_bytes;  // activation bytes per stage (see SK below)
+  const uint32_t cring = bring + nbs * bstage;
   const uint32_t cfull = smem_addr(&bars[0]), cempty = cfull + 8 * kMaxCSlots;
-  const uint32_t afull = cempty + 8 * kMaxCSlots, aempty = afull + 8 * kMaxASlots;
-  const uint32_t bfull = aempty + 8 * kMaxASlots, bempty = bfull + 8 * kMaxBSlots;
+  const uint32_t afull = cempty + 8 * kMaxCSlots, aempty = afull + 8 * kMaxA;
+  const uint32_t bfull = aempty + 8 * kMaxA, bempty = bfull + 8 * kMaxBSlots;
   const uint32_t done = bempty + 8 * kMaxBSlots;
   // blockIdx.x walks the token chunks fastest, so the CTAs that use the same
   // weight tile run together and share it through L2.
@@ -324,6 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nslabs = (int)((a.k + kSlabK - 1) / kSlabK);
   const int jb = (int)blockIdx.z * a.slabs_per_split;
   const int nl = min(nslabs - jb, a.slabs_per_split);  // slabs of this CTA (>= 1)
+  // Pipeline stages: one slab, or with ATM two (128 k: one FP8 code slot).
+  // An odd last slab (only in the last split: FP8 splits hold whole code
+  // slots) is paired with a slab beyond k, which every copy fills with zeros.
+  constexpr int SK = ATM ? 2 : 1;
+  const int nu = (nl + SK - 1) / SK;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < ncs; ++i) {
@@ -331,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // INT4: one group of four warps per slot; FP8: both groups
       // one arrival per dequantising warp (lane 0, after __syncwarp): an FP8
       // code slot serves both groups, an INT4 one a single group
-      mbar_init(cempty + 8 * i, WT == kFP8 ? kDeqWarps : kDeqWarps / 2);
+      mbar_init(cempty + 8 * i, (WT == kFP8 && !ATM) ? kDeqWarps : kDeqWarps / 2);
     }
     for (int i = 0; i < nas; ++i) {
       mbar_init(afull + 8 * i, WT == kBF16 ? 1 : kDeqWarps / 2);
@@ -341,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bfull + 8 * i, 1);
       mbar_init(bempty + 8 * i, 1);
     }
-    mbar_init(done, nl >= 2 ? kMmaWarps : 1);  // one commit per issuer that has slabs
+    mbar_init(done, nu >= 2 ? kMmaWarps : 1);  // one commit per issuer that has stages
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(&tmem_base_sh), kTmemCols);
@@ -394,13 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       allow_dependent_launch();
       int s = 0;
       uint32_t ph = 0;
-      for (int i = 0; i < nl; ++i) {
-        if (i >= nbs && !mbar_wait(bempty + 8 * s, ph ^ 1u)) {
+      for (int u = 0; u < nu; ++u) {
+        if (u >= nbs && !mbar_wait(bempty + 8 * s, ph ^ 1u)) {
           atomicOr(&g_tc_error, kErrWaitTimeout);
           break;
         }
-        mbar_arrive_expect_tx(bfull + 8 * s, bslot_bytes);
-        tma_load_2d(bring + s * bslot_bytes, &tmx, bfull + 8 * s, (jb + i) * kSlabK, (int)m0);
+        mbar_arrive_expect_tx(bfull + 8 * s, bstage);
+#pragma unroll
+        for (int h = 0; h < SK; ++h)
+          tma_load_2d(bring + s * bstage + h * bslot_bytes, &tmx, bfull + 8 * s, (jb + SK * u + h) * kSlabK, (int)m0);
         if (++s == nbs) {
           s = 0;
           ph ^= 1u;
@@ -515,6 +577,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         advance();
       }
+    } else if constexpr (WT == kFP8 && ATM) {
+      // ---------------- FP8, A in tensor memory ----------------
+      // One weight row per thread: warp w may only reach tensor-memory lanes
+      // 32 (w % 4) .. + 31, so thread t of warp w converts row 32 (w % 4) + t.
+      // Group g takes stages g, g + 2, ...: each is one code slot, whose row
+      // of 128 codes (eight 16-byte chunks, swizzled by row & 7, so that each
+      // quarter-warp's loads of eight consecutive rows cover all 32 banks)
+      // becomes the stage's 64 tensor-memory columns, with two tcgen05.st.
+      // The code and A cursors (cs, s) start at the group's first stage and
+      // advance by two stages: both rings hold an even number of them.
+      const int quarter = warp & 3;
+      const int r = quarter * 32 + lane;
+      const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + a_tcol;
+      for (int u = grp; u < nu; u += 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait(cfull + 8 * cs, cph))) {
+          ok = false;
+          break;
+        }
+        if (u >= nas && !__all_sync(0xffffffffu, mbar_wait(aempty + 8 * s, sph ^ 1u))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();  // the MMAs that read this stage's previous contents are complete
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint4 cw[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            cw[j] = lds128(cring + cs * CSLOT + r * 128 + (((4 * h + j) ^ (r & 7)) << 4));
+          uint32_t v[32];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            v[8 * j + 0] = fp8_lo_to_bf16x2(cw[j].x);
+            v[8 * j + 1] = fp8_hi_to_bf16x2(cw[j].x);
+            v[8 * j + 2] = fp8_lo_to_bf16x2(cw[j].y);
+            v[8 * j + 3] = fp8_hi_to_bf16x2(cw[j].y);
+            v[8 * j + 4] = fp8_lo_to_bf16x2(cw[j].z);
+            v[8 * j + 5] = fp8_hi_to_bf16x2(cw[j].z);
+            v[8 * j + 6] = fp8_lo_to_bf16x2(cw[j].w);
+            v[8 * j + 7] = fp8_hi_to_bf16x2(cw[j].w);
+          }
+          tmem_st32(trow + (uint32_t)(s * 64 + h * 32), v);
+        }
+        tmem_wait_st();
+        tc_fence_before();  // the stores are ordered before the arrival below
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(afull + 8 * s);
+          mbar_arrive(cempty + 8 * cs);  // after the loaded codes were used
+        }
+        advance();
+      }
     } else if constexpr (WT == kFP8) {
       // ---------------- FP8 ----------------
       // A code slot holds rows of 128 codes (slabs 2c, 2c + 1, 128-byte
@@ -587,22 +701,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // which caps a slab below the time HBM needs for its dequantised weights;
     // two issuers overlap those latencies.
     const int e = warp - kMmaWarp;
-    if (lane == 0 && e < min(nl, kMmaWarps)) {
+    if (lane == 0 && e < min(nu, kMmaWarps)) {
       const uint32_t idesc = idesc_bf16(kRows, a.ntok);
-      const uint32_t acc = tmem + (uint32_t)(e * kAccCols);
+      const uint32_t acc = tmem + (uint32_t)e * acc_off;
       int sa = e, sb = e;  // slab i's slots i % nas, i % nbs and their parities, kept
       uint32_t pa = 0, pb = 0;  // incrementally (every ring holds an even number >= 2)
-      for (int i = e; i < nl; i += kMmaWarps) {
+      for (int i = e; i < nu; i += kMmaWarps) {
         if (!mbar_wait(afull + 8 * sa, pa) || !mbar_wait(bfull + 8 * sb, pb)) {
           atomicOr(&g_tc_error, kErrWaitTimeout);
           break;
         }
         tc_fence_after();
-        const uint32_t abase = aring + sa * kABytes, bbase = bring + sb * bslot_bytes;
+        const uint32_t bbase = bring + sb * bstage;
+        if constexpr (ATM) {
+          // eight 16-k steps over the stage's two slabs: A 8 columns per step,
+          // B 32 bytes per step within each slab's swizzled rows
+          const uint32_t at = tmem + a_tcol + (uint32_t)(sa * 64);
 #pragma unroll
-        for (int kk = 0; kk < kSlabK / 16; ++kk)
-          umma_bf16(acc, sw128_desc(abase + kk * 32), sw128_desc(bbase + kk * 32), idesc,
-                    (i > e || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < SK * kSlabK / 16; ++kk)
+            umma_bf16_ta(acc, at + kk * 8, sw128_desc(bbase + (kk >> 2) * bslot_bytes + (kk & 3) * 32), idesc,
+                         (i > e || kk > 0) ? 1u : 0u);
+        } else {
+          const uint32_t abase = aring + sa * kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kSlabK / 16; ++kk)
+            umma_bf16(acc, sw128_desc(abase + kk * 32), sw128_desc(bbase + kk * 32), idesc,
+                      (i > e || kk > 0) ? 1u : 0u);
+        }
         // both slots are free once these MMAs have read them
         umma_commit(aempty + 8 * sa);
         umma_commit(bempty + 8 * sb);
@@ -631,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nchunks = (a.ntok + 31) / 32;
     float* part = a.splits > 1 ? a.part + (int64_t)blockIdx.z * a.m * a.n : nullptr;
     const float rscale = (WT == kFP8 && row < a.n) ? a.wscale[row] : 1.f;
-    const bool two = nl >= 2;  // the odd slabs' accumulator holds a sum
+    const bool two = nu >= 2;  // the second issuer's accumulator holds a sum
 #pragma unroll 1
     for (int cc = half; cc < nchunks; cc += 2) {
       uint32_t r[32];
@@ -639,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(taddr, r);
       if (two) {
         uint32_t r2[32];
-        tmem_ld32(taddr + kAccCols, r2);
+        tmem_ld32(taddr + acc_off, r2);
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
       }
@@ -707,9 +832,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int WT, bool ROPE>
+template <int WT, bool ROPE, bool ATM>
 void* tc_kernel() {
-  return reinterpret_cast<void*>(dq_gemm_tc_kernel<WT, ROPE>);
+  return reinterpret_cast<void*>(dq_gemm_tc_kernel<WT, ROPE, ATM>);
+}
+
+template <int WT, bool ATM, class E>
+cudaError_t launch_tc(dim3 grid, size_t smem, cudaStream_t s, const CUtensorMap& tmx, const CUtensorMap& tmw,
+                      const CUtensorMap& tms, const TcArgs& a, const E& epi) {
+  constexpr bool ROPE = !std::is_same<E, NoEpi>::value;
+  return launch_pdl(dq_gemm_tc_kernel<WT, ROPE, ATM>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, epi);
 }
 
 }  // namespace
@@ -792,6 +924,17 @@ GemmPlan plan_dq_gemm_tc(int wtype, int64_t m, int64_t n, int64_t k, int num_sms
   }
   p.ra = (int)best_n;
   p.m_chunks = (int)((m + best_n - 1) / best_n);
+  // FP8 with N <= 64 keeps A in tensor memory, in 128-k stages: the shared
+  // memory then carries codes and activations only, and each MMA issuer
+  // checks two barriers and commits twice per eight MMAs. (70B gate+up at
+  // m = 32: 87.5 against 128.5 us; at N = 96..128 the MMAs bound both forms
+  // equally.) Test hook: DQD_GEMM_TC_ATM=0 keeps A in shared memory, =1 uses
+  // tensor memory up to N = 128.
+  {
+    const char* atm_env = std::getenv("DQD_GEMM_TC_ATM");
+    const int cap = atm_env ? (atm_env[0] == '0' ? 0 : 128) : 64;
+    p.tc_atm = (wtype == kFP8 && best_n <= cap) ? 1 : 0;
+  }
   const int64_t per_units = (units + best_sp - 1) / best_sp;
   p.splits = (int)((units + per_units - 1) / per_units);
   p.k_per_split = per_units * unit * kSlabK;
@@ -839,20 +982,28 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
     }
   }
   if (e != cudaSuccess) return e;
+  const bool atm = p.tc_atm != 0 && l.wtype == kFP8 && p.ra <= 128;
   {  // the two MMA issuers need even rings (see Rings)
-    const Rings R = rings(l.wtype, (int)p.ra);
-    if ((R.nas | R.nbs) & 1) return cudaErrorInvalidValue;
+    const Rings R = rings(l.wtype, (int)p.ra, atm);
+    if (((R.nas | R.nbs) & 1) || R.nas < 2 || R.nbs < 2 || (l.wtype != kBF16 && R.ncs < 2))
+      return cudaErrorInvalidValue;
   }
-  static std::atomic<int> configured[64][6];
+  static std::atomic<int> configured[64][12];
   int dev = 0;
   cudaGetDevice(&dev);
   const int wi = l.wtype == kBF16 ? 0 : (l.wtype == kFP8 ? 1 : 2);
   const bool rope = l.rope != nullptr;
-  const int fi = wi + (rope ? 3 : 0);
+  const int fi = wi + (rope ? 3 : 0) + (atm ? 6 : 0);
   if (dev < 0 || dev >= 64 || !configured[dev][fi].load(std::memory_order_relaxed)) {
-    void* fn = rope ? (wi == 0 ? tc_kernel<kBF16, true>() : (wi == 1 ? tc_kernel<kFP8, true>() : tc_kernel<kINT4, true>()))
-                    : (wi == 0 ? tc_kernel<kBF16, false>()
-                               : (wi == 1 ? tc_kernel<kFP8, false>() : tc_kernel<kINT4, false>()));
+    void* fn = nullptr;
+    if (atm)
+      fn = rope ? tc_kernel<kFP8, true, true>() : tc_kernel<kFP8, false, true>();
+    else if (rope)
+      fn = wi == 0 ? tc_kernel<kBF16, true, false>()
+                   : (wi == 1 ? tc_kernel<kFP8, true, false>() : tc_kernel<kINT4, true, false>());
+    else
+      fn = wi == 0 ? tc_kernel<kBF16, false, false>()
+                   : (wi == 1 ? tc_kernel<kFP8, false, false>() : tc_kernel<kINT4, false, false>());
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev][fi].store(1, std::memory_order_relaxed);
@@ -873,17 +1024,19 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
   const size_t smem = (size_t)p.smem_bytes;
   if (rope) {
     const RopeEpi& r = *l.rope;
+    if (atm) return launch_tc<kFP8, true>(grid, smem, s, tmx, tmw, tms, a, r);
     switch (wi) {
-      case 0: return launch_pdl(dq_gemm_tc_kernel<kBF16, true>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, r);
-      case 1: return launch_pdl(dq_gemm_tc_kernel<kFP8, true>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, r);
-      default: return launch_pdl(dq_gemm_tc_kernel<kINT4, true>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, r);
+      case 0: return launch_tc<kBF16, false>(grid, smem, s, tmx, tmw, tms, a, r);
+      case 1: return launch_tc<kFP8, false>(grid, smem, s, tmx, tmw, tms, a, r);
+      default: return launch_tc<kINT4, false>(grid, smem, s, tmx, tmw, tms, a, r);
     }
   }
   const NoEpi none{};
+  if (atm) return launch_tc<kFP8, true>(grid, smem, s, tmx, tmw, tms, a, none);
   switch (wi) {
-    case 0: return launch_pdl(dq_gemm_tc_kernel<kBF16, false>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, none);
-    case 1: return launch_pdl(dq_gemm_tc_kernel<kFP8, false>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, none);
-    default: return launch_pdl(dq_gemm_tc_kernel<kINT4, false>, grid, dim3(kThreads), smem, s, tmx, tmw, tms, a, none);
+    case 0: return launch_tc<kBF16, false>(grid, smem, s, tmx, tmw, tms, a, none);
+    case 1: return launch_tc<kFP8, false>(grid, smem, s, tmx, tmw, tms, a, none);
+    default: return launch_tc<kINT4, false>(grid, smem, s, tmx, tmw, tms, a, none);
   }
 }
 

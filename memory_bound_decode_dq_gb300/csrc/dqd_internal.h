@@ -89,6 +89,7 @@ constexpr size_t kCounterBytes = 65536;  // = DQD_WS_COUNTER_BYTES
 
 struct GemmPlan {
   int tc;            // 1: tensor-core (tcgen05) kernel for wide m
+  int tc_atm;        // tcgen05: 1 = A (dequantised weights) in tensor memory
   int mt;            // m8 tiles per CTA pass (1, 2, 4, 8)
   int warps;         // warp-MMA kernels: compute warps per CTA (one 16-row tile each)
   int int4_slots;    // INT4 warp-MMA kernel: ring slots (2 or 3)

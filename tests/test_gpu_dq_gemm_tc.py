@@ -195,3 +195,34 @@ def test_every_ring_layout(dev, dqd, monkeypatch, wtype, ntok):
     assert dqd.dq_gemm_workspace_bytes(w, m) == 0  # one split: the whole k in each CTA
     assert_close(f64(dqd.dq_gemm(w, bf(x, dev))), ref, what=f"tc {wtype} N={ntok}")
     assert dqd.device_errors() == 0
+
+
+@pytest.mark.parametrize("ntok", [16, 32, 48, 64, 96, 128])
+@pytest.mark.parametrize("k,split", [(64, 1), (1008, 1), (8192, 1), (8192, 3), (4160, 5)])
+def test_fp8_a_in_tensor_memory(dev, dqd, monkeypatch, ntok, k, split):
+    """FP8 at N <= 128 keeps the dequantised weights in tensor memory
+    (tcgen05.st by the dequantising warps, A read from tensor memory by the
+    MMA) in stages of two slabs, whose last one may lie beyond k (one-slab k,
+    ragged k, an odd last split). Within tolerance of the oracle; within one
+    bf16 ulp plus fp32 reordering error of the kernel with A in shared memory
+    (the two issuers' partial sums are split differently); bit-identical on a
+    rerun."""
+    monkeypatch.setenv("DQD_GEMM_TC", "1")
+    monkeypatch.setenv("DQD_GEMM_TC_N", str(ntok))
+    monkeypatch.setenv("DQD_GEMM_SPLITS", str(split))
+    monkeypatch.setenv("DQD_GEMM_TC_ATM", "1")  # tensor memory up to N = 128
+    m, n = ntok - 3 if ntok > 16 else 11, 300
+    w, host = _dense(dqd, dev, oracle.W_FP8_E4M3, n, k, seed=ntok + k)
+    x = synth.normal_bf16(ntok + k + split, "x", (m, k))
+    xd = bf(x, dev)
+    a = dqd.dq_gemm(w, xd)
+    assert np.array_equal(bits(a), bits(dqd.dq_gemm(w, xd)))
+    assert_close(f64(a), oracle.dq_gemm(oracle.W_FP8_E4M3, *host, x), what=f"tc fp8 tmem-A N={ntok} k={k}")
+    monkeypatch.setenv("DQD_GEMM_TC_ATM", "0")
+    b = f64(dqd.dq_gemm(w, xd))
+    # one bf16 ulp, plus what reordering an fp32 sum of k products can move
+    # (some 256 sequential adds per accumulator at k = 8192, each within 2^-24
+    # of the running sum; 1e-3 of the output rms bounds it here)
+    tol = 2.0 ** -7 * np.maximum(np.abs(f64(a)), np.abs(b)) + 1e-3 * np.sqrt(np.mean(b ** 2))
+    assert np.all(np.abs(f64(a) - b) <= tol)
+    assert dqd.device_errors() == 0
