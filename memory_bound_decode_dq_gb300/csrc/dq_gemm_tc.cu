@@ -75,8 +75,10 @@ static_assert(256 * kRows * 2 <= kRingBytes, "the fused RoPE epilogue stages up 
 // Code slot bytes per weight type (INT4: codes + scales of one 64-k slab;
 // FP8: a 128 x 128 code tile, two slabs, so that every row is one full
 // 128-byte line; BF16 has none: its weight tiles land straight in the A slots).
-__host__ __device__ constexpr int code_slot(int wt) {
-  return wt == kINT4 ? kI4Codes + kI4Scales : (wt == kFP8 ? kRows * 2 * kSlabK : 0);
+// With A in tensor memory a code slot holds a 128-k stage: FP8 unchanged
+// (a 128 x 128 tile), INT4 whole group blocks (both halves) and their scales.
+__host__ __device__ constexpr int code_slot(int wt, bool atm = false) {
+  return wt == kINT4 ? (atm ? 2 : 1) * kI4Codes + kI4Scales : (wt == kFP8 ? kRows * 2 * kSlabK : 0);
 }
 
 // Ring depths for N tokens per CTA: the activation ring gets about 64 KB
@@ -117,7 +119,7 @@ __host__ __device__ inline Rings rings(int wt, int ntok, bool atm = false) {
     // slot always serves the same group.
     r.nas = min(kMaxTSlots, (kTmemCols - 2 * tc_acc_cols(ntok)) / 64) & ~1;
     r.nbs = (min(kMaxBSlots, max(2, (64 * 1024) / (2 * bslot))) + 1) & ~1;
-    r.ncs = min(kMaxCSlots, (kRingBytes - r.nbs * 2 * bslot) / code_slot(wt)) & ~1;
+    r.ncs = min(kMaxCSlots, (kRingBytes - r.nbs * 2 * bslot) / code_slot(wt, true)) & ~1;
     return r;
   }
   r.nbs = (min(kMaxBSlots, max(3, (64 * 1024) / bslot)) + 1) & ~1;
@@ -348,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     dq_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                       const __grid_constant__ CUtensorMap tms, const TcArgs a,
                       const __grid_constant__ typename EpiOf<ROPE>::type epi) {
-  constexpr int CSLOT = code_slot(WT);
+  constexpr int CSLOT = code_slot(WT, ATM);
   extern __shared__ uint8_t smem_raw[];
   constexpr int kMaxA = kMaxASlots > kMaxTSlots ? kMaxASlots : kMaxTSlots;
   __shared__ __align__(8) uint64_t bars[2 * kMaxCSlots + 2 * kMaxA + 2 * kMaxBSlots + 1];
@@ -421,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       const int NSL = WT == kBF16 ? nas : ncs;
       const uint32_t empty = WT == kBF16 ? aempty : cempty, full = WT == kBF16 ? afull : cfull;
-      const int step = WT == kFP8 ? 2 : 1;  // slabs per weight slot
+      const int step = (WT == kFP8 || ATM) ? 2 : 1;  // slabs per weight slot
       for (int i = 0, slot_i = 0; i < nl; i += step, ++slot_i) {
         const int j = jb + i;
         if (slot_i >= NSL && !mbar_wait(empty + 8 * cs, ph ^ 1u)) {
@@ -435,6 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if constexpr (WT == kFP8) {
           mbar_arrive_expect_tx(fb, CSLOT);  // slabs j, j + 1 (j even)
           tma_load_2d(cring + cs * CSLOT, &tmw, fb, j * kSlabK, (int)row0);
+        } else if constexpr (ATM) {
+          // a whole group (slabs j, j + 1; j even): both halves of the eight
+          // tiles' blocks, then their scales
+          const uint32_t dst = cring + cs * CSLOT;
+          mbar_arrive_expect_tx(fb, CSLOT);
+          tma_load_2d(dst, &tmw, fb, j * 128, (int)tile0);
+          tma_load_2d(dst + kI4Codes, &tmw, fb, (j + 1) * 128, (int)tile0);
+          tma_load_2d(dst + 2 * kI4Codes, &tms, fb, (j >> 1) * 8, (int)tile0);
         } else {
           const uint32_t dst = cring + cs * CSLOT;
           mbar_arrive_expect_tx(fb, CSLOT);
@@ -489,7 +499,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         sph ^= 1u;
       }
     };
-    if constexpr (WT == kINT4) {
+    if constexpr (WT == kINT4 && ATM) {
+      // ---------------- INT4, A in tensor memory ----------------
+      // One weight row per thread (row r = 32 (w % 4) + t, the lanes warp w
+      // may reach), one 128-k group per stage; group g takes stages g, g + 2.
+      // In the packed block of row tile T, rows r0 and r0 + 8 (r0 = r % 8)
+      // share 64 contiguous bytes per half-group, 16 words: word 4t + j holds
+      // four k of both rows, k = 64 h + 32 (j >> 1) + 8 t + 4 (j & 1) + 0..3,
+      // row r0 in nibbles 0, 4, 2, 6 (k + 0, + 1, + 2, + 3) and row r0 + 8 in
+      // nibbles 1, 5, 3, 7. Shifting the word right by 4 for the upper row
+      // puts (k, k + 1) in nibbles 0 and 4 and (k + 2, k + 3) in nibbles 2
+      // and 6: two bf16x2 of 128 + q each with the 0x4300 magic, then the
+      // exact subtraction of 128 + z and one rounded multiply by the scale.
+      const int quarter = warp & 3;
+      const int tl = quarter * 2 + (lane >> 4);  // row tile within the CTA
+      const int r0 = lane & 7;
+      const uint32_t shift = (lane & 8) ? 4u : 0u;
+      const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16) + a_tcol;
+      const int G = (int)(a.k / 128);
+      const bool live = tile0 + tl < ntiles;
+      const uint8_t* zp = a.wz + (tile0 + tl) * G * 8 + r0;  // zero byte of group gr at zp[8 gr]
+      int gr = (jb >> 1) + grp;
+      uint32_t znext = (live && gr < G) ? ldg_u8(zp + 8 * gr) : 0u;
+      for (int u = grp; u < nu; u += 2) {
+        const uint32_t zz = int4_zero_pair(znext >> shift);
+        znext = (live && gr + 2 < G) ? ldg_u8(zp + 8 * (gr + 2)) : 0u;
+        gr += 2;
+        if (!__all_sync(0xffffffffu, mbar_wait(cfull + 8 * cs, cph))) {
+          ok = false;
+          break;
+        }
+        if (u >= nas && !__all_sync(0xffffffffu, mbar_wait(aempty + 8 * s, sph ^ 1u))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();  // the MMAs that read this stage's previous contents are complete
+        const uint32_t slot = cring + cs * CSLOT;
+        const uint32_t sw = lds32(slot + 2 * kI4Codes + tl * 32 + r0 * 4);
+        const uint32_t ss = shift ? prmt(sw, 0u, 0x3232u) : prmt(sw, 0u, 0x1010u);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[32];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const uint4 w4 = lds128(slot + h * kI4Codes + tl * 512 + r0 * 64 + t * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t wv = word(w4, j) >> shift;
+              const int c0 = 16 * (j >> 1) + 4 * t + 2 * (j & 1);
+              v[c0] = bf16x2_mul(bf16x2_sub(and_or(wv, 0x000F000Fu, 0x43004300u), zz), ss);
+              v[c0 + 1] = bf16x2_mul(bf16x2_sub(and_or(wv >> 8, 0x000F000Fu, 0x43004300u), zz), ss);
+            }
+          }
+          tmem_st32(trow + (uint32_t)(s * 64 + h * 32), v);
+        }
+        tmem_wait_st();
+        tc_fence_before();  // the stores are ordered before the arrival below
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(afull + 8 * s);
+          mbar_arrive(cempty + 8 * cs);  // after the loaded codes and scales were used
+        }
+        advance();
+      }
+    } else if constexpr (WT == kINT4) {
       // ---------------- INT4: warp gw of a group owns 16-row tiles 2 gw, 2 gw + 1 ----------------
       // Group 0 dequantises the first 64-k half of every 128-k group, group 1
       // the second, so each iteration starts a new group: zero points are
@@ -933,7 +1006,7 @@ GemmPlan plan_dq_gemm_tc(int wtype, int64_t m, int64_t n, int64_t k, int num_sms
   {
     const char* atm_env = std::getenv("DQD_GEMM_TC_ATM");
     const int cap = atm_env ? (atm_env[0] == '0' ? 0 : 128) : 64;
-    p.tc_atm = (wtype == kFP8 && best_n <= cap) ? 1 : 0;
+    p.tc_atm = (wtype != kBF16 && best_n <= cap) ? 1 : 0;
   }
   const int64_t per_units = (units + best_sp - 1) / best_sp;
   p.splits = (int)((units + per_units - 1) / per_units);
@@ -982,7 +1055,7 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
     }
   }
   if (e != cudaSuccess) return e;
-  const bool atm = p.tc_atm != 0 && l.wtype == kFP8 && p.ra <= 128;
+  const bool atm = p.tc_atm != 0 && l.wtype != kBF16 && p.ra <= 128;
   {  // the two MMA issuers need even rings (see Rings)
     const Rings R = rings(l.wtype, (int)p.ra, atm);
     if (((R.nas | R.nbs) & 1) || R.nas < 2 || R.nbs < 2 || (l.wtype != kBF16 && R.ncs < 2))
@@ -997,7 +1070,8 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
   if (dev < 0 || dev >= 64 || !configured[dev][fi].load(std::memory_order_relaxed)) {
     void* fn = nullptr;
     if (atm)
-      fn = rope ? tc_kernel<kFP8, true, true>() : tc_kernel<kFP8, false, true>();
+      fn = wi == 1 ? (rope ? tc_kernel<kFP8, true, true>() : tc_kernel<kFP8, false, true>())
+                   : (rope ? tc_kernel<kINT4, true, true>() : tc_kernel<kINT4, false, true>());
     else if (rope)
       fn = wi == 0 ? tc_kernel<kBF16, true, false>()
                    : (wi == 1 ? tc_kernel<kFP8, true, false>() : tc_kernel<kINT4, true, false>());
@@ -1024,7 +1098,8 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
   const size_t smem = (size_t)p.smem_bytes;
   if (rope) {
     const RopeEpi& r = *l.rope;
-    if (atm) return launch_tc<kFP8, true>(grid, smem, s, tmx, tmw, tms, a, r);
+    if (atm) return wi == 1 ? launch_tc<kFP8, true>(grid, smem, s, tmx, tmw, tms, a, r)
+                            : launch_tc<kINT4, true>(grid, smem, s, tmx, tmw, tms, a, r);
     switch (wi) {
       case 0: return launch_tc<kBF16, false>(grid, smem, s, tmx, tmw, tms, a, r);
       case 1: return launch_tc<kFP8, false>(grid, smem, s, tmx, tmw, tms, a, r);
@@ -1032,7 +1107,8 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
     }
   }
   const NoEpi none{};
-  if (atm) return launch_tc<kFP8, true>(grid, smem, s, tmx, tmw, tms, a, none);
+  if (atm) return wi == 1 ? launch_tc<kFP8, true>(grid, smem, s, tmx, tmw, tms, a, none)
+                          : launch_tc<kINT4, true>(grid, smem, s, tmx, tmw, tms, a, none);
   switch (wi) {
     case 0: return launch_tc<kBF16, false>(grid, smem, s, tmx, tmw, tms, a, none);
     case 1: return launch_tc<kFP8, false>(grid, smem, s, tmx, tmw, tms, a, none);

@@ -226,3 +226,59 @@ def test_fp8_a_in_tensor_memory(dev, dqd, monkeypatch, ntok, k, split):
     tol = 2.0 ** -7 * np.maximum(np.abs(f64(a)), np.abs(b)) + 1e-3 * np.sqrt(np.mean(b ** 2))
     assert np.all(np.abs(f64(a) - b) <= tol)
     assert dqd.device_errors() == 0
+
+
+@pytest.mark.parametrize("ntok", [16, 32, 48, 64, 96, 128])
+@pytest.mark.parametrize("k,split", [(128, 1), (1024, 1), (8192, 1), (8192, 3), (4224, 5)])
+def test_int4_a_in_tensor_memory(dev, dqd, monkeypatch, ntok, k, split):
+    """INT4 with the dequantised weights in tensor memory, one 128-k group per
+    stage, row-per-thread unpacking of the packed blocks: within tolerance of
+    the oracle, within one bf16 ulp plus fp32 reordering of the form with A in
+    shared memory, bit-identical on a rerun; ragged n (a partial row tile and
+    a CTA with fewer than eight tiles), one-group k, split k."""
+    monkeypatch.setenv("DQD_GEMM_TC", "1")
+    monkeypatch.setenv("DQD_GEMM_TC_N", str(ntok))
+    monkeypatch.setenv("DQD_GEMM_SPLITS", str(split))
+    monkeypatch.setenv("DQD_GEMM_TC_ATM", "1")
+    m, n = ntok - 3 if ntok > 16 else 11, 300
+    wq, w = _weight(dqd, dev, n, k, seed=ntok + k)
+    x = synth.normal_bf16(ntok + k + split, "x", (m, k))
+    xd = bf(x, dev)
+    a = dqd.dq_gemm(w, xd)
+    assert np.array_equal(bits(a), bits(dqd.dq_gemm(w, xd)))
+    assert_close(f64(a), oracle.dq_gemm(oracle.W_INT4_G128, wq.codes, wq.scales, wq.zeros, x),
+                 what=f"tc int4 tmem-A N={ntok} k={k}")
+    monkeypatch.setenv("DQD_GEMM_TC_ATM", "0")
+    b = f64(dqd.dq_gemm(w, xd))
+    tol = 2.0 ** -7 * np.maximum(np.abs(f64(a)), np.abs(b)) + 1e-3 * np.sqrt(np.mean(b ** 2))
+    assert np.all(np.abs(f64(a) - b) <= tol)
+    assert dqd.device_errors() == 0
+
+
+@pytest.mark.parametrize("wtype", ["int4", "fp8"])
+def test_one_hot_reads_back_tensor_memory_weights(dev, dqd, monkeypatch, wtype):
+    """One-hot tokens through the tensor-memory form (N = 64): y[t] is the
+    dequantised weight of column t, bit for bit, for every k position of two
+    groups (every nibble and column of the unpacking), over ragged n."""
+    monkeypatch.setenv("DQD_GEMM_TC", "1")
+    monkeypatch.setenv("DQD_GEMM_TC_N", "64")
+    monkeypatch.setenv("DQD_GEMM_SPLITS", "1")
+    n, k = 200, 256
+    if wtype == "int4":
+        wq, w = _weight(dqd, dev, n, k, seed=23)
+        deq = oracle.int4_dequant(wq.codes, wq.scales, wq.zeros)
+        scale = None
+    else:
+        w, (rc, rs, _) = _dense(dqd, dev, oracle.W_FP8_E4M3, n, k, seed=23)
+        deq, scale = None, rs
+    for start in range(0, k, 64):
+        x = np.zeros((64, k), np.uint16)
+        x[np.arange(64), start + np.arange(64)] = 0x3F80
+        y = dqd.dq_gemm(w, bf(x, dev))
+        if wtype == "int4":
+            assert np.array_equal(bits(y), deq[:, start:start + 64].T)
+        else:
+            # FP8: bf16(code value * row scale), the product of two exact factors rounded once
+            ref = oracle.dq_gemm(oracle.W_FP8_E4M3, rc, rs, None, x.view(np.uint16))
+            assert_close(f64(y), ref, what="fp8 one-hot")
+    assert dqd.device_errors() == 0
