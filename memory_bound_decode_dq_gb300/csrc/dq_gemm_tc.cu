@@ -922,22 +922,23 @@ cudaError_t launch_tc(dim3 grid, size_t smem, cudaStream_t s, const CUtensorMap&
 bool tc_supported(int wtype, int64_t m, int64_t n, int64_t k) {
   if (m > (int64_t)INT32_MAX || n <= 0 || (n + 127) / 128 > 65535 || k <= 0) return false;
   switch (wtype) {
-    // INT4 from m = 33. The tcgen05 kernel's INT4 time hardly depends on m
-    // (a per-slab cost caps it), while the warp-MMA kernel's grows with its
-    // m-tiles: with its 2-slot ring it is faster up to m = 32 on nearly every
-    // 8B and 70B projection (at m = 32, 70B down 78.6 vs 82.2 us, qkv 34.3 vs
-    // 38.9; the 70B gate+up, 149.0 vs 144.7, is the exception) and falls far
-    // behind from m = 40, where it needs eight m-tiles (gate+up 423 vs 142 us).
-    case kINT4: return m >= 33 && k % 128 == 0 && k / 128 <= 65535;
-    // FP8 from m = 24 and BF16 from m = 17, measured on the 8B and 70B
-    // projections against the warp-MMA kernel with four m-tiles (m = 17..32),
-    // 70B gate+up / down / qkv / o at m = 24, FP8: 130 / 79 / 38 / 27 us against
-    // 147 / 89 / 49 / 29; BF16 at m = 17: 144 / 79 / 39 / 27 against
-    // 157 / 95 / 44 / 32. Below those the warp-MMA kernels win or tie on nearly
-    // every shape (BF16 at m = 16: 4096 x 14336 down 22.6 vs 24.7 us); the
-    // 8B gate+up (28672 x 4096, 224 CTAs: a second wave half full) stays
-    // faster on them throughout (BF16 at m = 32: 46 vs 53 us).
-    case kFP8: return m >= 24 && k % 16 == 0;
+    // INT4 and FP8 from m = 17, where the warp-MMA kernels need a third
+    // m-tile and the tcgen05 kernel (A in tensor memory up to N = 64) runs at
+    // a nearly flat cost. Measured against the warp-MMA kernels at m = 20..32:
+    // FP8 faster on every 8B and 70B projection (70B gate+up 87.6 vs 139.4 us
+    // at m = 20); INT4 faster on the 70B layer as a whole (m = 24: qkv + o +
+    // gate+up + down 214 vs 242 us), within 10% behind on the 8B gate+up
+    // (28672 x 4096: 40.4 vs 36.6 us). At m = 12..16 FP8 wins on the 70B
+    // projections but loses on the 8B gate+up (38.9 vs 34.6 us), INT4 loses.
+    case kINT4: return m >= 17 && k % 128 == 0 && k / 128 <= 65535;
+    case kFP8: return m >= 17 && k % 16 == 0;
+    // BF16 from m = 17, measured on the 8B and 70B projections against the
+    // warp-MMA kernel with four m-tiles (m = 17..32): at m = 17, 70B
+    // gate+up / down / qkv / o 144 / 79 / 39 / 27 us against 157 / 95 / 44 / 32.
+    // Below that the warp-MMA kernels win or tie on nearly every shape (m = 16:
+    // 4096 x 14336 down 22.6 vs 24.7 us); the 8B gate+up (28672 x 4096, 224
+    // CTAs: a second wave half full) stays faster on them throughout (m = 32:
+    // 46 vs 53 us).
     case kBF16: return m >= 17 && k % 8 == 0;
     default: return false;
   }
@@ -985,7 +986,11 @@ GemmPlan plan_dq_gemm_tc(int wtype, int64_t m, int64_t n, int64_t k, int num_sms
       if (forced >= 1 && sp != std::min<int64_t>(forced, units)) continue;
       const int64_t per = (units + sp - 1) / sp * unit;  // slabs per split
       const double waves = (double)((ctas * sp + sms - 1) / sms);
-      const double slab = std::max(std::max(base + 2.0 * ntok, 700.0), ctas * sp >= sms ? wslab / 21.0 : 0.0);
+      // with A in tensor memory (FP8, INT4 at N <= 64) a slab measured about
+      // 480 (FP8) and 560 (INT4) cycles whatever N
+      const bool atm_n = wtype != kBF16 && ntok <= 64;
+      const double own = atm_n ? (wtype == kINT4 ? 560.0 : 480.0) : std::max(base + 2.0 * ntok, 700.0);
+      const double slab = std::max(own, ctas * sp >= sms ? wslab / 21.0 : 0.0);
       double cycles = waves * (per + 6.0) * slab;
       if (sp > 1) cycles += 8.0 * sp * m * n / 6e12 * 1.9e9;
       if (best < 0 || cycles < best * 0.97) {

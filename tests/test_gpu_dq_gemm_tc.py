@@ -1,5 +1,5 @@
-"""GPU parity of the tensor-core (tcgen05) dq_gemm path taken at wide m (INT4
-from 33 rows, FP8 from 24, BF16 from 17), against the float64 oracle and
+"""GPU parity of the tensor-core (tcgen05) dq_gemm path taken at wide m (from
+17 rows for every weight type), against the float64 oracle and
 against the warp-MMA kernels on the same inputs.
 
 Shapes span several 128-row weight tiles and 128-token chunks with ragged n
@@ -34,7 +34,7 @@ def _weight(dqd, dev, n, k, seed):
 
 SHAPES = [(128, 128, 128), (129, 1000, 256), (256, 2048, 1024), (300, 48, 4096), (1024, 130, 512),
           (500, 4112, 384), (200, 16, 128), (384, 6144, 4096), (33, 300, 1024), (40, 4096, 4096),
-          (64, 28672, 4096), (17, 300, 1024), (32, 4096, 4096)]   # the last two: the warp-MMA side of the boundary
+          (64, 28672, 4096), (17, 300, 1024), (32, 4096, 4096), (16, 300, 1024)]  # the last: the warp-MMA side of the boundary
 
 
 @pytest.mark.parametrize("m,n,k", SHAPES)
@@ -121,7 +121,7 @@ DENSE = [oracle.W_BF16, oracle.W_FP8_E4M3]
                                    (300, 64, 1024), (48, 10240, 8192), (1024, 300, 128)])
 def test_dense_against_oracle(dev, dqd, wtype, m, n, k):
     """Ragged k (a partial last slab), ragged n and m, one-slab k, big shapes
-    (FP8 takes this path from 24 rows, BF16 from 17)."""
+    (every weight type takes this path from 17 rows)."""
     w, host = _dense(dqd, dev, wtype, n, k, seed=m + n + k)
     x = synth.normal_bf16(m + 2 * k, "x", (m, k))
     y = dqd.dq_gemm(w, bf(x, dev))
