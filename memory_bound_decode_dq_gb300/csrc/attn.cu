@@ -35,6 +35,7 @@
 //    (o, m, l) that attn_merge_kernel combines per output row.
 #include "dqd_device.cuh"
 #include "dqd_internal.h"
+#include "tcgen05.cuh"
 
 #include <algorithm>
 #include <atomic>
@@ -636,6 +637,401 @@ __global__ void __launch_bounds__(128) attn_merge_wide_kernel(const Args a) {
   *reinterpret_cast<uint2*>(a.out + row * kD + lane * 4) = o;
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core (tcgen05) form for wide query tiles: 17..128 query rows per kv
+// head (verify widths), bf16 cache. One CTA per (sequence, kv head, chunk);
+// the context chunk is walked in tiles of 128 tokens (eight 16-token blocks):
+//  * warp 0: gathers each tile's K and V blocks through the block table by
+//    TMA into one of three stages: K and V as two 64-dim halves of 128 token
+//    rows each (16 KB per half, 128-byte swizzled, block i at rows
+//    16 i .. 16 i + 15);
+//  * warp 1, lane 0: S = Q K^T (M 128 query rows, N 128 tokens, K 128 dims;
+//    Q K-major, K K-major) into the S buffer of the tile's parity in tensor
+//    memory, then O += P V for the previous tile (M 128, N 128 dims, K 128
+//    tokens; P read from tensor memory, where it overwrote that tile's S; V
+//    MN-major: token rows with the dims contiguous, as the cache stores them)
+//    into the O accumulator of that parity;
+//  * warps 2-9: two softmax groups of four warps, for the even and the odd
+//    tiles, each with its own S buffer, O accumulator and running (m, l); one
+//    query row per thread (the tensor-memory lane the warp may reach): the
+//    online softmax in the log2 domain on its S row (masked keys -> -inf by
+//    select: past the context, past the causal limit of the row's verify
+//    position, or in an absent block), O rescaled in tensor memory when the
+//    row's reference maximum moves, P written as bf16 for the next MMA; V rows
+//    past the context are zeroed first so stale pool contents cannot leak.
+//    At the end the even group combines the two (m, l, O), as the merge of two
+//    chunks would.
+// The result is the normalised bf16 output (one chunk) or the same fp32
+// partial (o, m, l) as the mma.sync form, merged by the same kernels.
+namespace tca {
+constexpr int kTileBlk = 8;                 // 16-token blocks per tile
+constexpr int kTileTok = kTileBlk * kBlk;   // 128
+constexpr int kHalf = 128 * 128;            // one 64-dim half: 128 rows x 128 B
+constexpr int kQ = 0;                       // Q: two halves
+constexpr int kStage0 = 2 * kHalf;          // stages: K halves then V halves
+constexpr int kStageBytes = 4 * kHalf;
+constexpr int kStages = 3;
+constexpr int kBody = kStage0 + kStages * kStageBytes;  // 224 KB
+constexpr int kSmem = kBody;  // the dynamic region starts 1024-byte aligned (checked at run time)
+constexpr int kThreads = 320;
+constexpr int kSoft0 = 2;                   // first softmax warp
+// tensor-memory columns: S (then P) and O for the even and the odd tiles
+__host__ __device__ constexpr uint32_t s_col(int parity) { return parity ? 128u : 0u; }
+__host__ __device__ constexpr uint32_t o_col(int parity) { return parity ? 384u : 256u; }
+}  // namespace tca
+
+__device__ __forceinline__ void sts128z(uint32_t addr) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
+}
+__device__ __forceinline__ void softmax_barrier() {  // the eight softmax warps
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+// Ten warps: three share some SM sub-partitions, whose 16K registers then
+// allow about 168 per thread.
+__global__ void __launch_bounds__(tca::kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Args a) {
+  using namespace tca;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // kv_full[kStages], kv_empty[kStages], s_full[2], p_full[2], pv_done[2]
+  __shared__ __align__(8) uint64_t bars[2 * kStages + 6];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ float xm[2][128];  // the odd group's final (m, l) per row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  grid_dependency_wait();  // q, the tables and the cache may come from the previous kernel
+  allow_dependent_launch();
+  if (smem_addr(smem_raw) & 1023u) {  // the layout needs a 1024-byte aligned region
+    if (threadIdx.x == 0) atomicOr(&g_attn_error, kErrBadInput);
+    return;
+  }
+  const int ctx = seq_ctx(a, b);
+  if (chunk == 0 && g == 0 && threadIdx.x == 0) {
+    const int raw = a.ctx[b];
+    if (raw < a.W || raw != ctx) atomicOr(&g_attn_error, kErrBadInput);
+  }
+  const int nblk_seq = (ctx + kBlk - 1) / kBlk;
+  const int blk0 = chunk * a.chunk_blocks;
+  if (blk0 >= nblk_seq) {  // whole CTA: nothing of this sequence here
+    if (a.nchunks == 1 && nblk_seq == 0) {
+      for (int i = threadIdx.x; i < a.QR * kD / 2; i += tca::kThreads) {
+        const int r = i / (kD / 2);
+        const int64_t orow = ((int64_t)b * a.W + r / a.G) * a.Hq + g * a.G + r % a.G;
+        reinterpret_cast<uint32_t*>(a.out + orow * kD)[i % (kD / 2)] = 0u;
+      }
+    }
+    return;
+  }
+  const int blk_end = min(blk0 + a.chunk_blocks, nblk_seq);
+  const int ntiles = (blk_end - blk0 + kTileBlk - 1) / kTileBlk;
+  const uint32_t base = smem_addr(smem_raw);
+  const uint32_t kv_full = smem_addr(&bars[0]), kv_empty = kv_full + 8 * kStages, s_full = kv_full + 16 * kStages,
+                 p_full = s_full + 16, pv_done = s_full + 32;
+  auto stage = [&](int st) { return base + kStage0 + st * kStageBytes; };
+  bool ok = true;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(kv_full + 8 * i, 1);
+      mbar_init(kv_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + 8 * i, 1);
+      mbar_init(p_full + 8 * i, 4);  // the four warps of a softmax group
+      mbar_init(pv_done + 8 * i, 1);
+    }
+    fence_mbar_init();
+  }
+  // Q: the QR rows of this kv head (row r: position r / G, head g G + r % G),
+  // zero rows up to 128, K-major and 128-byte swizzled in two 64-dim halves;
+  // thread (r, hh) of the softmax warps copies half hh of row r.
+  if (warp >= kSoft0) {
+    const int tq = threadIdx.x - kSoft0 * 32;
+    const int r = tq & 127, hh = tq >> 7;
+    const bool live = r < a.QR;
+    const uint4* src = live ? reinterpret_cast<const uint4*>(
+                                  a.q + (((int64_t)b * a.W + r / a.G) * a.Hq + g * a.G + r % a.G) * kD) + 8 * hh
+                            : nullptr;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t dst = base + kQ + hh * kHalf + r * 128 + ((((uint32_t)c) ^ (uint32_t)(r & 7)) << 4);
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) tmem_alloc(smem_addr(&tmem_base_sh), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  int issued = 0;  // tiles whose copies the gather warp issued
+  if (warp == 0) {
+    // ---------------- K/V gather ----------------
+    // Lane i (< 8) issues the four copies of the tile's block i, so that a
+    // tile's 32 copies go out eight at a time; lane l reads the block-table
+    // entry of block 32 q + l of the chunk for groups of four tiles.
+    const int64_t tab_row = (int64_t)b * a.max_blocks;
+    const int nblk = blk_end - blk0;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmk) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmv) : "memory");
+    int tab = 0;
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int st = j % kStages;
+      if (j >= kStages && !__all_sync(0xffffffffu, mbar_wait(kv_empty + 8 * st, ((j - kStages) / kStages) & 1))) {
+        ok = false;
+        break;
+      }
+      if ((j & 3) == 0) {  // the table entries of tiles j .. j + 3
+        const int bi = j * kTileBlk + lane;
+        const int32_t v = bi < nblk ? a.table[tab_row + blk0 + bi] : 0;
+        tab = v < 0 ? 0 : (v >= a.num_blocks ? (int)(a.num_blocks - 1) : v);
+        if (tab != v) atomicOr(&g_attn_error, kErrBadInput);  // clamped: reads stay inside the pool
+      }
+      const int nb = min(kTileBlk, nblk - j * kTileBlk);
+      const uint32_t fb = kv_full + 8 * st, dst = stage(st);
+      if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)nb * 4u * 2048u);
+      __syncwarp();
+      const int phys = __shfl_sync(0xffffffffu, tab, (j & 3) * kTileBlk + (lane & 7));
+      if (lane < nb) {
+        const uint32_t d = dst + lane * 2048;
+        tma_load_4d(d, &tmk, fb, 0, 0, g, phys);
+        tma_load_4d(d + kHalf, &tmk, fb, 64, 0, g, phys);
+        tma_load_4d(d + 2 * kHalf, &tmv, fb, 0, 0, g, phys);
+        tma_load_4d(d + 3 * kHalf, &tmv, fb, 64, 0, g, phys);
+      }
+      issued = j + 1;
+    }
+    if (!ok && lane == 0) atomicOr(&g_attn_error, kErrWaitTimeout);
+  } else if (warp == 1) {
+    // ---------------- MMA issue ----------------
+    // The tensor pipe runs one thread's MMAs in order: S of tile j + 2
+    // overwrites the buffer that P of tile j occupied only after P V of tile j
+    // has read it.
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16(128, kTileTok), id_pv = idesc_bf16_bmn(128, kD);
+      auto issue_pv = [&](int j) {  // O[j & 1] += P V of tile j
+        const int pg = j & 1;
+        if (!mbar_wait(p_full + 8 * pg, (j >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t v0 = stage(j % kStages) + 2 * kHalf;
+#pragma unroll
+        for (int kk = 0; kk < kTileTok / 16; ++kk)  // 16 tokens = 8 columns of P
+          umma_bf16_ta(tmem + o_col(pg), tmem + s_col(pg) + kk * 8, sw128_desc_mn(v0 + kk * 2048, kHalf, 1024), id_pv,
+                       (j >= 2 || kk > 0) ? 1u : 0u);
+        umma_commit(kv_empty + 8 * (j % kStages));  // the stage is free once these MMAs have read V
+        umma_commit(pv_done + 8 * pg);
+        return true;
+      };
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int ks = j % kStages, sg = j & 1;
+        if (!mbar_wait(kv_full + 8 * ks, (j / kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k0 = stage(ks);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          umma_bf16(tmem + s_col(sg), sw128_desc(base + kQ + (kk >> 2) * kHalf + (kk & 3) * 32),
+                    sw128_desc(k0 + (kk >> 2) * kHalf + (kk & 3) * 32), id_s, kk > 0 ? 1u : 0u);
+        umma_commit(s_full + 8 * sg);
+        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+      }
+      if (ok && !issue_pv(ntiles - 1)) ok = false;
+      if (!ok) atomicOr(&g_attn_error, kErrWaitTimeout);
+    }
+  } else {
+    // ---------------- softmax: group grp takes tiles grp, grp + 2, ... ----------------
+    const int grp = (warp - kSoft0) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // query row = tensor-memory lane
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tS = trow + s_col(grp), tO = trow + o_col(grp);
+    const bool live = r < a.QR;
+    // key j is visible to row r iff j < ctx and j <= ctx - W + r / G
+    const int lim = live ? min(ctx - 1, ctx - a.W + r / a.G) : -1;
+    float m = kNegInf, l = 0.f;
+    int last = -1;  // this group's last tile
+    for (int j = grp; j < ntiles; j += 2) {
+      const int tok0 = (blk0 + j * kTileBlk) * kBlk;  // first token of the tile
+      const int tok_end = min(blk_end * kBlk, ctx);   // tokens past this are absent or past the context
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * grp, (j >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[kTileTok];
+      {
+        uint32_t u0[32], u1[32], u2[32], u3[32];  // four loads in flight, one wait
+        tmem_ld32_nowait(tS, u0);
+        tmem_ld32_nowait(tS + 32, u1);
+        tmem_ld32_nowait(tS + 64, u2);
+        tmem_ld32_nowait(tS + 96, u3);
+        tmem_wait_ld();
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          sv[t] = __uint_as_float(u0[t]);
+          sv[32 + t] = __uint_as_float(u1[t]);
+          sv[64 + t] = __uint_as_float(u2[t]);
+          sv[96 + t] = __uint_as_float(u3[t]);
+        }
+      }
+      float mx[8];  // eight independent partial maxima (short dependency chains)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = kNegInf;
+      const int vl = min(lim, tok_end - 1) - tok0;  // columns 0 .. vl are visible to this row
+#pragma unroll
+      for (int t = 0; t < kTileTok; ++t) {
+        sv[t] = t <= vl ? sv[t] * a.scale_log2 : kNegInf;
+        mx[t & 7] = fmaxf(mx[t & 7], sv[t]);
+      }
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // The row's reference maximum moves only when the tile's maximum exceeds
+      // it by more than 8 (log2 units): P stays below 2^8, and O and l are
+      // rescaled on few tiles.
+      const float mn = (mt > m + 8.f || m == kNegInf) ? fmaxf(m, mt) : m;
+      const float mb = mn == kNegInf ? 0.f : mn;  // a row with no visible key so far keeps p = 0
+      const float alpha = mn == m ? 1.f : ex2(m - mb);  // m = -inf: 0
+      // P over the S it was computed from, one 64-token half at a time: 128
+      // tokens as bf16, two per column (the S row is already in registers)
+      float pa[8];  // eight partial sums
+#pragma unroll
+      for (int u = 0; u < 8; ++u) pa[u] = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pw[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = ex2(sv[64 * h + 2 * c] - mb), p1 = ex2(sv[64 * h + 2 * c + 1] - mb);
+          pa[c & 7] += p0 + p1;
+          pw[c] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + 32 * h, pw);
+      }
+      const float ps = ((pa[0] + pa[1]) + (pa[2] + pa[3])) + ((pa[4] + pa[5]) + (pa[6] + pa[7]));
+      l = l * alpha + ps;
+      // V rows past the context (or of absent blocks) are zeroed before the
+      // MMA reads them: 0 * NaN would otherwise leak stale pool contents
+      if (tok0 + kTileTok > tok_end) {
+        if (!__all_sync(0xffffffffu, mbar_wait(kv_full + 8 * (j % kStages), (j / kStages) & 1))) {
+          ok = false;
+          break;
+        }
+        const int t = r;  // this thread's token row of the tile
+        if (tok0 + t >= tok_end) {
+          const uint32_t v0 = stage(j % kStages) + 2 * kHalf + t * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            sts128z(v0 + c * 16);
+            sts128z(v0 + kHalf + c * 16);
+          }
+        }
+      }
+      if (j >= 2) {
+        // O holds this group's earlier tiles once the previous P V is
+        // complete; it is rescaled only when some row of the warp moved its
+        // reference maximum
+        if (!__all_sync(0xffffffffu, mbar_wait(pv_done + 8 * grp, ((j - 2) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t u[32];
+            tmem_ld32(tO + c * 32, u);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) u[t] = __float_as_uint(__uint_as_float(u[t]) * alpha);
+            tmem_st32(tO + c * 32, u);
+          }
+        }
+      }
+      tmem_wait_st();  // P (and a rescaled O) in place
+      fence_proxy_async_smem();  // zeroed V rows, if any
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full + 8 * grp);
+      m = mn;
+      last = j;
+    }
+    // ---------------- epilogue ----------------
+    // each group waits for its last P V, the odd group hands over its (m, l),
+    // and the even group combines both O accumulators row by row
+    bool good = ok && (last < 0 || __all_sync(0xffffffffu, mbar_wait(pv_done + 8 * grp, (last >> 1) & 1)));
+    if (!good && lane == 0) atomicOr(&g_attn_error, kErrWaitTimeout);
+    if (grp == 1) {
+      xm[0][r] = last < 0 ? kNegInf : m;
+      xm[1][r] = last < 0 ? 0.f : l;
+    }
+    tc_fence_before();
+    softmax_barrier();
+    tc_fence_after();
+    if (grp == 0) {
+      const float m1 = xm[0][r], l1 = xm[1][r];
+      const float ms = fmaxf(m, m1);
+      const float mbs = ms == kNegInf ? 0.f : ms;
+      const float w0 = ex2(m - mbs), w1 = ex2(m1 - mbs);  // -inf: 0
+      const bool use1 = __any_sync(0xffffffffu, m1 != kNegInf);  // the odd accumulator holds data
+      const float lt = l * w0 + l1 * w1;
+      const int64_t orow = live ? ((int64_t)b * a.W + r / a.G) * a.Hq + g * a.G + r % a.G : 0;
+      const float inv = (lt > 0.f ? 1.f / lt : 0.f) * a.v_scale;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32], u1[32];
+        tmem_ld32(trow + o_col(0) + c * 32, u);  // warp-collective: every lane takes part
+        if (use1) {
+          tmem_ld32(trow + o_col(1) + c * 32, u1);
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            u[t] = __float_as_uint(__uint_as_float(u[t]) * w0 + (m1 != kNegInf ? __uint_as_float(u1[t]) * w1 : 0.f));
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) u[t] = __float_as_uint(__uint_as_float(u[t]) * w0);
+        }
+        if (good && live) {
+          if (a.nchunks == 1) {
+            uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kD + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pack_bf16x2(__uint_as_float(u[8 * q]) * inv, __uint_as_float(u[8 * q + 1]) * inv),
+                                  pack_bf16x2(__uint_as_float(u[8 * q + 2]) * inv, __uint_as_float(u[8 * q + 3]) * inv),
+                                  pack_bf16x2(__uint_as_float(u[8 * q + 4]) * inv, __uint_as_float(u[8 * q + 5]) * inv),
+                                  pack_bf16x2(__uint_as_float(u[8 * q + 6]) * inv, __uint_as_float(u[8 * q + 7]) * inv));
+          } else {
+            float4* po = reinterpret_cast<float4*>(a.part_o + (orow * a.nchunks + chunk) * kD + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              po[q] = make_float4(__uint_as_float(u[4 * q]) * a.v_scale, __uint_as_float(u[4 * q + 1]) * a.v_scale,
+                                  __uint_as_float(u[4 * q + 2]) * a.v_scale, __uint_as_float(u[4 * q + 3]) * a.v_scale);
+          }
+        }
+      }
+      if (good && live && a.nchunks > 1) {
+        a.part_ml[(orow * a.nchunks + chunk) * 2] = ms;
+        a.part_ml[(orow * a.nchunks + chunk) * 2 + 1] = lt;
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    // every issued copy has landed before the CTA exits (immediate unless a
+    // wait gave up): the last tile issued into each stage, bounded
+    for (int st = 0; st < kStages; ++st) {
+      const int jl = issued - 1 - (((issued - 1 - st) % kStages + kStages) % kStages);
+      if (jl >= 0) (void)mbar_wait(kv_full + 8 * st, (jl / kStages) & 1);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // A 4-D tensor map over a KV pool [num_blocks][hkv][16][128] whose box is 16
 // tokens of one (block, kv head), 128 bytes wide (64 bf16 head dims or 128
 // FP8 codes), 128-byte swizzled.
@@ -840,6 +1236,45 @@ AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms, 
   p.nchunks = (maxblk + cb - 1) / cb;
   p.smem_bytes = kv_fp8 ? smem_of<true>(p.qt) : smem_of<false>(p.qt);
   p.kv_fp8 = kv_fp8 ? 1 : 0;
+  // Wide query tiles over a bf16 cache (17..128 rows per kv head: verify
+  // widths) take the tensor-core form: one CTA per SM, chunks of whole
+  // 128-token tiles; the chunk count minimises waves x (chunk + a fixed cost
+  // per CTA), with a quarter of a chunk more when the partials need merging.
+  // The fixed cost (Q load, the first tile's copy latency, epilogue) is about
+  // 96 blocks' worth: measured at batch 64, width 16, 144 blocks per
+  // sequence, one chunk 140 us, two 173 us, three 207 us. Test hook:
+  // DQD_ATTN_TC=0 keeps the mma.sync form.
+  {
+    const char* tc_env = std::getenv("DQD_ATTN_TC");
+    p.tc = (!kv_fp8 && qr > 16 && qr <= 128 && !(tc_env && tc_env[0] == '0')) ? 1 : 0;
+  }
+  if (p.tc) {
+    const int64_t titems = (int64_t)b * hkv, tslots = std::max(num_sms, 1);
+    auto round8 = [](int64_t c) { return (c + 7) / 8 * 8; };
+    double best = -1.0;
+    int64_t best_c = round8(maxblk);
+    for (int64_t n = 1; n <= std::min<int64_t>(64, (maxblk + 7) / 8); ++n) {
+      const int64_t c = round8((maxblk + n - 1) / n);
+      const int64_t n_eff = (maxblk + c - 1) / c;
+      const int64_t waves = (titems * n_eff + tslots - 1) / tslots;
+      const double cost = (double)waves * (double)(c + 96) + (n_eff > 1 ? 0.25 * (double)c : 0.0);
+      if (best < 0 || cost < best) {
+        best = cost;
+        best_c = c;
+      }
+    }
+    int64_t c = best_c;
+    if (const char* env = std::getenv("DQD_ATTN_CHUNK_BLOCKS")) {
+      const long v = std::strtol(env, nullptr, 10);
+      if (v >= 1) c = v;
+    }
+    c = std::min<int64_t>(c, maxblk);
+    p.chunk_blocks = (int)c;
+    p.nchunks = (int)((maxblk + c - 1) / c);
+    p.qt = 4;
+    p.qgroups = 1;
+    p.smem_bytes = tca::kSmem;
+  }
   const size_t rows = (size_t)b * w * hq;
   p.ws_bytes = p.nchunks > 1 ? kCounterBytes + rows * p.nchunks * (kD + 2) * sizeof(float) : 0;
   return p;
@@ -887,7 +1322,18 @@ cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) 
   cudaError_t e = kv_tensor_map(l.k_pool, f8, l.hkv, l.num_blocks, &tmk);
   if (e == cudaSuccess) e = kv_tensor_map(l.v_pool, f8, l.hkv, l.num_blocks, &tmv);
   if (e != cudaSuccess) return e;
-  if (f8) {
+  if (p.tc) {
+    static std::atomic<int> configured[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tca::kSmem);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_relaxed);
+    }
+    e = launch_pdl(attn_tc_kernel, dim3(p.nchunks, a.Hkv, a.B), dim3(tca::kThreads), (size_t)tca::kSmem, s, tmk, tmv,
+                   a);
+  } else if (f8) {
     switch (p.qt) {
       case 1: e = launch_split<1, true>(a, p, tmk, tmv, s); break;
       case 2: e = launch_split<2, true>(a, p, tmk, tmv, s); break;

@@ -161,6 +161,7 @@ struct AttnPlan {
   int nchunks;
   int smem_bytes;
   int kv_fp8;        // 1: FP8-E4M3 cache codes, 0: bf16 cache
+  int tc;            // 1: tensor-core (tcgen05) form for wide query tiles
   size_t ws_bytes;   // 0 if nchunks == 1
 };
 

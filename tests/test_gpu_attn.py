@@ -219,3 +219,33 @@ def test_rejects_bad_arguments(dev, dqd):
 def test_no_device_error_flags_after_the_suite(dev, dqd):
     """No bounded wait on an asynchronous copy gave up during this module."""
     assert dqd.device_errors() == 0
+
+
+TC_CASES = [
+    # B, W, Hq, Hkv, contexts: 17..128 query rows per kv head over a bf16 cache
+    (2, 6, 32, 8, (6, 700)),          # 24 rows, one context shorter than a tile
+    (2, 16, 32, 8, (16, 513)),        # 64 rows
+    (1, 16, 64, 8, (900,)),           # 128 rows
+    (3, 5, 16, 4, (5, 130, 2049)),    # 20 rows, ragged tiles
+    (2, 9, 32, 4, (300, 4100)),       # 72 rows
+]
+
+
+@pytest.mark.parametrize("B,W,hq,hkv,ctx", TC_CASES)
+@pytest.mark.parametrize("cb", [None, 1, 3, 8, 13])
+def test_tensor_core_form(dev, dqd, monkeypatch, B, W, hq, hkv, ctx, cb):
+    """The tcgen05 form (S and O in tensor memory, V as an MN-major operand)
+    against the oracle, and against the mma.sync form within tolerance, for
+    every chunking: chunks of whole tiles, of partial tiles, and of 1 block;
+    bit-identical on a rerun."""
+    if cb is not None:
+        monkeypatch.setenv("DQD_ATTN_CHUNK_BLOCKS", str(cb))
+    kv = synth.paged_kv(B * 7 + W, "kv", ctx, hkv, spare_blocks=3)
+    q = synth.normal_bf16(B + W + hq, "q", (B, W, hq, 128))
+    a = run(dqd, dev, q, kv, hkv)
+    assert np.array_equal(bits(a), bits(run(dqd, dev, q, kv, hkv)))
+    r = ref(q, kv, hkv)
+    assert_close(f64(a), r, what=f"tc attn B={B} W={W} {hq}/{hkv} ctx={ctx} cb={cb}")
+    monkeypatch.setenv("DQD_ATTN_TC", "0")
+    assert_close(f64(run(dqd, dev, q, kv, hkv)), r, what="mma.sync form")
+    assert dqd.device_errors() == 0
