@@ -162,7 +162,9 @@ struct AttnPlan {
   int smem_bytes;
   int kv_fp8;        // 1: FP8-E4M3 cache codes, 0: bf16 cache
   int tc;            // 1: tensor-core (tcgen05) form for wide query tiles
-  size_t ws_bytes;   // 0 if nchunks == 1
+  int tail_items;    // tensor-core form: items of the last partial wave, split ...
+  int tail_pieces;   // ... into this many pieces (0: none)
+  size_t ws_bytes;   // 0 if nchunks == 1 and no tail
 };
 
 AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms, bool kv_fp8);

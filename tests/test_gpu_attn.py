@@ -249,3 +249,28 @@ def test_tensor_core_form(dev, dqd, monkeypatch, B, W, hq, hkv, ctx, cb):
     monkeypatch.setenv("DQD_ATTN_TC", "0")
     assert_close(f64(run(dqd, dev, q, kv, hkv)), r, what="mma.sync form")
     assert dqd.device_errors() == 0
+
+
+@pytest.mark.parametrize("B,W,hq,hkv", [(20, 16, 32, 8), (24, 6, 32, 8), (21, 9, 32, 4)])
+def test_tensor_core_balanced_tail(dev, dqd, monkeypatch, B, W, hq, hkv):
+    """More work items than SMs: the items of the last partial wave are split
+    into pieces of whole tiles (some empty, for short contexts) and merged by
+    the tail merge. Within tolerance of the same items run whole (each piece
+    rounds P to bf16 against its own reference maximum) and of the oracle
+    (queries halved: with full ones, random contexts put rare elements of
+    either attention form just past the 1% bound, an effect of the bf16 P that
+    both forms share), bit-identical on a rerun."""
+    rng = np.random.default_rng(B * 100 + W)
+    # contexts of 256 .. 1499 tokens: with fewer keys per row the bf16 rounding
+    # of P (either form) moves the output by a larger share of its rms (151
+    # tokens: twice the rms error, the worst element at 1.0-1.15 of the bound);
+    # items under 1024 tokens still leave pieces empty when split eight ways
+    ctx = tuple(int(c) for c in rng.integers(256, 1500, size=B))
+    kv = synth.paged_kv(B + W, "kv", ctx, hkv, spare_blocks=2)
+    q = synth.normal_bf16(B * W, "q", (B, W, hq, 128), std=0.5)
+    a = run(dqd, dev, q, kv, hkv)
+    assert np.array_equal(bits(a), bits(run(dqd, dev, q, kv, hkv)))
+    assert_close(f64(a), ref(q, kv, hkv), what=f"tc balanced tail B={B} W={W} {hq}/{hkv}")
+    monkeypatch.setenv("DQD_ATTN_TAIL", "0")
+    assert_close(f64(a), f64(run(dqd, dev, q, kv, hkv)), what="whole items")
+    assert dqd.device_errors() == 0
