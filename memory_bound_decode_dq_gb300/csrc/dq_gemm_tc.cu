@@ -151,6 +151,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 5-D tiled TMA load (the INT4 code blocks, reordered on the way in).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1, int c2,
+                                            int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
 __device__ __forceinline__ void sts128(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -355,11 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(cring + cs * CSLOT, &tmw, fb, j * kSlabK, (int)row0);
         } else if constexpr (ATM) {
           // a whole group (slabs j, j + 1; j even): both halves of the eight
-          // tiles' blocks, then their scales
+          // tiles' blocks in one 5-D box that puts 16-byte chunk t of row r0 at
+          // t * 128 + r0 * 16 (see the tensor map), then their scales
           const uint32_t dst = cring + cs * CSLOT;
           mbar_arrive_expect_tx(fb, CSLOT);
-          tma_load_2d(dst, &tmw, fb, j * 128, (int)tile0);
-          tma_load_2d(dst + kI4Codes, &tmw, fb, (j + 1) * 128, (int)tile0);
+          tma_load_5d(dst, &tmw, fb, 0, 0, 0, j, (int)tile0);
           tma_load_2d(dst + 2 * kI4Codes, &tms, fb, (j >> 1) * 8, (int)tile0);
         } else {
           const uint32_t dst = cring + cs * CSLOT;
@@ -427,6 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // puts (k, k + 1) in nibbles 0 and 4 and (k + 2, k + 3) in nibbles 2
       // and 6: two bf16x2 of 128 + q each with the 0x4300 magic, then the
       // exact subtraction of 128 + z and one rounded multiply by the scale.
+      // The code slot holds tile tl's half h with its 16-byte chunk t of row
+      // pair r0 at tl * 1024 + h * 512 + t * 128 + r0 * 16 (the TMA box
+      // reorders rows and chunks), so the eight rows of a quarter-warp read
+      // eight consecutive chunks: no bank conflicts.
       const int quarter = warp & 3;
       const int tl = quarter * 2 + (lane >> 4);  // row tile within the CTA
       const int r0 = lane & 7;
@@ -458,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
-            const uint4 w4 = lds128(slot + h * kI4Codes + tl * 512 + r0 * 64 + t * 16);
+            const uint4 w4 = lds128(slot + tl * 1024 + h * 512 + t * 128 + r0 * 16);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint32_t wv = word(w4, j) >> shift;
@@ -961,7 +975,16 @@ cudaError_t launch_dq_gemm_tc(const GemmLaunch& l, const GemmPlan& p, cudaStream
     e = tensor_map(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, l.data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
     const int64_t G = l.k / 128;
-    {  // packed codes as 32-bit words: [tile][G * 256]
+    if (p.tc_atm && p.ra <= 128) {
+      // packed codes as 32-bit words, five dimensions: 4 words of a 16-byte
+      // chunk, row pair r0 (8, 64 bytes apart), chunk t (4, 16 bytes apart),
+      // half-group (2 G, 512 bytes apart), tile (ntiles, G KB apart); the box
+      // {4, 8, 4, 2, 8} lands as [tile][half][t][r0][16 bytes]
+      const uint64_t dims[5] = {4, 8, 4, (uint64_t)G * 2, (uint64_t)ntiles};
+      const uint64_t strides[4] = {64, 16, 512, (uint64_t)G * 1024};
+      const uint32_t box[5] = {4, 8, 4, 2, 8};
+      e = tensor_map(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, l.data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {  // packed codes as 32-bit words: [tile][G * 256]
       const uint64_t dims[2] = {(uint64_t)G * 256, (uint64_t)ntiles};
       const uint64_t strides[1] = {(uint64_t)G * 1024};
       const uint32_t box[2] = {128, 8};
