@@ -71,6 +71,9 @@ struct Args {
   int tail_items, tail_pieces;
   float* tail_o;
   float* tail_ml;
+  // persistent tensor-core form: the work queue's ticket and finished-CTA
+  // count (the workspace's counter region; zero on entry and on exit)
+  unsigned* ctr;
 };
 
 // Per-module device error word (kErrWaitTimeout when a bounded wait gave up,
@@ -687,6 +690,14 @@ __host__ __device__ constexpr uint32_t s_col(int parity) { return parity ? 128u 
 __host__ __device__ constexpr uint32_t o_col(int parity) { return parity ? 384u : 256u; }
 }  // namespace tca
 
+// o0 w0 + o1 w1 for the two softmax groups' accumulators, each product and
+// the sum rounded on its own (no fused multiply-add), so that the result does
+// not depend on which accumulator holds the even and which the odd tiles; an
+// accumulator whose row saw no key (has = false) adds 0.
+__device__ __forceinline__ float combine2(float o0, float w0, bool has0, float o1, float w1, bool has1) {
+  return __fadd_rn(has0 ? __fmul_rn(o0, w0) : 0.f, has1 ? __fmul_rn(o1, w1) : 0.f);
+}
+
 __device__ __forceinline__ void sts128z(uint32_t addr) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
 }
@@ -1009,7 +1020,7 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
       const float mbs = ms == kNegInf ? 0.f : ms;
       const float w0 = ex2(m - mbs), w1 = ex2(m1 - mbs);  // -inf: 0
       const bool use1 = __any_sync(0xffffffffu, m1 != kNegInf);  // the odd accumulator holds data
-      const float lt = l * w0 + l1 * w1;
+      const float lt = __fadd_rn(__fmul_rn(l, w0), __fmul_rn(l1, w1));
       const int64_t orow = live ? ((int64_t)b * a.W + r / a.G) * a.Hq + g * a.G + r % a.G : 0;
       const float inv = (lt > 0.f ? 1.f / lt : 0.f) * a.v_scale;
 #pragma unroll 1
@@ -1020,10 +1031,12 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
           tmem_ld32(trow + o_col(1) + c * 32, u1);
 #pragma unroll
           for (int t = 0; t < 32; ++t)
-            u[t] = __float_as_uint(__uint_as_float(u[t]) * w0 + (m1 != kNegInf ? __uint_as_float(u1[t]) * w1 : 0.f));
+            u[t] = __float_as_uint(
+                combine2(__uint_as_float(u[t]), w0, m != kNegInf, __uint_as_float(u1[t]), w1, m1 != kNegInf));
         } else {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) u[t] = __float_as_uint(__uint_as_float(u[t]) * w0);
+          for (int t = 0; t < 32; ++t)
+            u[t] = __float_as_uint(combine2(__uint_as_float(u[t]), w0, m != kNegInf, 0.f, 0.f, false));
         }
         if (good && live) {
           if (piece >= 0) {
@@ -1076,6 +1089,548 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Persistent tensor-core form: the work units and the per-tile arithmetic of
+// attn_tc_kernel, with one CTA per SM taking units from a queue (an atomic
+// ticket in the workspace's counter region; the last CTA to find the queue
+// empty resets it), so that the tiles of successive units flow through one
+// pipeline instead of each CTA paying its own start-up and drain:
+//  * warp 0 takes the next unit once it has issued the copies of the current
+//    one, hands it to the other roles through a two-slot queue in shared
+//    memory, loads its Q by TMA (into a second Q slot when the unit has at
+//    most 64 query rows, so that it lands while the current Q is in use) and
+//    gathers its tiles into the same three stages;
+//  * tiles are numbered across units: tile J uses stage J mod 3, the S buffer
+//    and softmax group of J's parity, whatever unit it belongs to;
+//  * warp 1 issues S of a unit's first tile before P V of the previous unit's
+//    last tile, and the first P V of a unit (which starts an O accumulator
+//    afresh) only after the even group has read both accumulators of the
+//    previous unit;
+//  * the odd group hands its (m, l) to the even group through shared memory
+//    (a full/empty barrier pair) and goes on to the next unit.
+namespace tcp {
+// With at most 64 query rows, Q slot 1 starts 64 rows (8 KB) into each of
+// slot 0's halves: the rows past 64 that an M = 128 MMA reads from either slot
+// are rows of the other slot or of stage 0, and belong to masked query rows.
+constexpr int kQSlot = 64 * 128;
+}  // namespace tcp
+
+struct TcUnit {
+  int item, b, g, chunk, piece, ctx, blk0, blk_end, ntiles;
+};
+
+// Unit u of the tensor-core forms: chunk u mod nchunks of item u / nchunks,
+// or, with a balanced tail, the whole items first and then the pieces of the
+// last tail_items items.
+__device__ __forceinline__ TcUnit tc_unit(const Args& a, int u) {
+  TcUnit t;
+  t.piece = -1;
+  t.chunk = 0;
+  if (a.tail_pieces > 0) {
+    const int nwhole = a.B * a.Hkv - a.tail_items;
+    t.item = u < nwhole ? u : nwhole + (u - nwhole) / a.tail_pieces;
+    t.piece = u < nwhole ? -1 : (u - nwhole) % a.tail_pieces;
+  } else {
+    t.item = u / a.nchunks;
+    t.chunk = u % a.nchunks;
+  }
+  t.b = t.item / a.Hkv;
+  t.g = t.item % a.Hkv;
+  t.ctx = seq_ctx(a, t.b);
+  const int nblk_seq = (t.ctx + kBlk - 1) / kBlk;
+  t.blk0 = t.chunk * a.chunk_blocks;
+  t.blk_end = min(t.blk0 + a.chunk_blocks, nblk_seq);
+  if (t.piece >= 0) {  // piece k of p: tiles [k T / p, (k + 1) T / p) of the item's T tiles
+    const int T = (nblk_seq + tca::kTileBlk - 1) / tca::kTileBlk;
+    t.blk0 = (t.piece * T / a.tail_pieces) * tca::kTileBlk;
+    t.blk_end = min(((t.piece + 1) * T / a.tail_pieces) * tca::kTileBlk, nblk_seq);
+  }
+  t.ntiles = t.blk0 < t.blk_end ? (t.blk_end - t.blk0 + tca::kTileBlk - 1) / tca::kTileBlk : 0;
+  return t;
+}
+
+__global__ void __launch_bounds__(tca::kThreads, 1)
+    attn_tcp_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                    const __grid_constant__ CUtensorMap tmq, const Args a) {
+  using namespace tca;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // kv_full[3], kv_empty[3], s_full[2], p_full[2], pv_done[2], q_full[2],
+  // q_free[2], u_full[2], u_empty[2], o_free, xm_full, xm_empty, fin
+  __shared__ __align__(8) uint64_t bars[2 * kStages + 18];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int unit_sh[2];
+  __shared__ float xm[2][128];  // the odd group's (m, l) per row for the unit being combined
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dependency_wait();  // q, the tables, the cache and the queue's counters come from earlier kernels
+  allow_dependent_launch();
+  if (smem_addr(smem_raw) & 1023u) {  // the layout needs a 1024-byte aligned region
+    if (threadIdx.x == 0) atomicOr(&g_attn_error, kErrBadInput);
+    return;
+  }
+  const int items = a.B * a.Hkv;
+  const int units = a.tail_pieces > 0 ? items - a.tail_items + a.tail_items * a.tail_pieces : items * a.nchunks;
+  const int nq = a.QR <= 64 ? 2 : 1;  // Q slots
+  const uint32_t base = smem_addr(smem_raw);
+  const uint32_t kv_full = smem_addr(&bars[0]), kv_empty = kv_full + 8 * kStages, s_full = kv_full + 16 * kStages,
+                 p_full = s_full + 16, pv_done = s_full + 32, q_full = s_full + 48, q_free = s_full + 64,
+                 u_full = s_full + 80, u_empty = s_full + 96, o_free = s_full + 112, xm_full = s_full + 120,
+                 xm_empty = s_full + 128, fin = s_full + 136;
+  auto stage = [&](int st) { return base + kStage0 + st * kStageBytes; };
+  bool ok = true;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(kv_full + 8 * i, 1);
+      mbar_init(kv_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + 8 * i, 1);
+      mbar_init(p_full + 8 * i, 4);  // the four warps of a softmax group
+      mbar_init(pv_done + 8 * i, 1);
+      mbar_init(q_full + 8 * i, 1);
+      mbar_init(q_free + 8 * i, 1);
+      mbar_init(u_full + 8 * i, 1);
+      mbar_init(u_empty + 8 * i, 9);  // the MMA thread and the eight softmax warps
+    }
+    mbar_init(o_free, 4);  // the even group's warps
+    mbar_init(xm_full, 4);  // the odd group's warps
+    mbar_init(xm_empty, 4);
+    mbar_init(fin, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_addr(&tmem_base_sh), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ---------------- queue, Q and K/V gather ----------------
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmk) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmv) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmq) : "memory");
+    int J = 0;   // tiles whose copies were issued
+    int qi = 0;  // Q loads issued (one per unit with tiles)
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      if (k >= 2 && !__all_sync(0xffffffffu, mbar_wait(u_empty + 8 * slot, ((k >> 1) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      int u = 0;
+      if (lane == 0) u = (int)atomicAdd(a.ctr, 1u);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u >= units) u = -1;
+      if (lane == 0) {
+        unit_sh[slot] = u;
+        mbar_arrive(u_full + 8 * slot);
+      }
+      if (u < 0) break;
+      const TcUnit t = tc_unit(a, u);
+      if (lane == 0 && t.chunk == 0 && t.g == 0 && t.piece <= 0) {
+        const int raw = a.ctx[t.b];
+        if (raw < a.W || raw != t.ctx) atomicOr(&g_attn_error, kErrBadInput);
+      }
+      if (t.ntiles == 0) continue;
+      // Q of the unit: the QR rows of its kv head (row r: position r / G,
+      // head g G + r % G), two 64-dim halves, once the slot's previous unit has
+      // issued its last S
+      const int qs = qi % nq;
+      if (qi >= nq && !__all_sync(0xffffffffu, mbar_wait(q_free + 8 * qs, ((qi / nq) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        const uint32_t qb = q_full + 8 * qs, dst = base + kQ + qs * tcp::kQSlot;
+        mbar_arrive_expect_tx(qb, (uint32_t)a.QR * 256u);
+        tma_load_4d(dst, &tmq, qb, 0, t.g * a.G, 0, t.b);
+        tma_load_4d(dst + kHalf, &tmq, qb, 64, t.g * a.G, 0, t.b);
+      }
+      ++qi;
+      const int64_t tab_row = (int64_t)t.b * a.max_blocks;
+      const int nblk = t.blk_end - t.blk0;
+      int tab = 0;
+      for (int j = 0; j < t.ntiles; ++j) {
+        const int st = J % kStages;
+        if (J >= kStages && !__all_sync(0xffffffffu, mbar_wait(kv_empty + 8 * st, ((J - kStages) / kStages) & 1))) {
+          ok = false;
+          break;
+        }
+        if ((j & 3) == 0) {  // the table entries of tiles j .. j + 3
+          const int bi = j * kTileBlk + lane;
+          const int32_t v = bi < nblk ? a.table[tab_row + t.blk0 + bi] : 0;
+          tab = v < 0 ? 0 : (v >= a.num_blocks ? (int)(a.num_blocks - 1) : v);
+          if (tab != v) atomicOr(&g_attn_error, kErrBadInput);  // clamped: reads stay inside the pool
+        }
+        const int nb = min(kTileBlk, nblk - j * kTileBlk);
+        const uint32_t fb = kv_full + 8 * st, dst = stage(st);
+        if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)nb * 4u * 2048u);
+        __syncwarp();
+        const int phys = __shfl_sync(0xffffffffu, tab, (j & 3) * kTileBlk + (lane & 7));
+        if (lane < nb) {
+          const uint32_t d = dst + lane * 2048;
+          tma_load_4d(d, &tmk, fb, 0, 0, t.g, phys);
+          tma_load_4d(d + kHalf, &tmk, fb, 64, 0, t.g, phys);
+          tma_load_4d(d + 2 * kHalf, &tmv, fb, 0, 0, t.g, phys);
+          tma_load_4d(d + 3 * kHalf, &tmv, fb, 64, 0, t.g, phys);
+        }
+        ++J;
+      }
+    }
+    if (lane == 0) {
+      if (!ok) atomicOr(&g_attn_error, kErrWaitTimeout);
+      // Every CTA counts itself out once; the last one leaves both counters
+      // at zero for the next call (every other CTA has taken its last ticket).
+      __threadfence();
+      if (atomicAdd(a.ctr + 1, 1u) == gridDim.x - 1) {
+        atomicExch(a.ctr, 0u);
+        atomicExch(a.ctr + 1, 0u);
+      }
+      // every issued copy has landed before the CTA exits (immediate unless a
+      // wait gave up): the last tile issued into each stage, the last Q load
+      // into each slot, bounded
+      for (int st = 0; st < kStages; ++st) {
+        const int jl = J - 1 - (((J - 1 - st) % kStages + kStages) % kStages);
+        if (jl >= 0) (void)mbar_wait(kv_full + 8 * st, (jl / kStages) & 1);
+      }
+      for (int s = 0; s < nq; ++s) {
+        const int il = qi - 1 - (((qi - 1 - s) % nq + nq) % nq);
+        if (il >= 0) (void)mbar_wait(q_full + 8 * s, (il / nq) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issue ----------------
+    // The tensor pipe runs one thread's MMAs in order: S of tile J + 2
+    // overwrites the buffer that P of tile J occupied only after P V of tile J
+    // has read it, and a Q slot is reloaded only after the commit that follows
+    // its unit's last S.
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16(128, kTileTok), id_pv = idesc_bf16_bmn(128, kD);
+      int ofn = 0;  // o_free phases waited
+      // O[J & 1] += P V of tile J; acc = 0 starts the accumulator afresh (the
+      // group's first tile of a unit); wait_o: the even group must first have
+      // read both accumulators of the previous unit
+      auto issue_pv = [&](int Jp, bool acc, bool wait_o) {
+        const int pg = Jp & 1;
+        if (wait_o) {
+          if (!mbar_wait(o_free, ofn & 1)) return false;
+          ++ofn;
+        }
+        if (!mbar_wait(p_full + 8 * pg, (Jp >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t v0 = stage(Jp % kStages) + 2 * kHalf;
+#pragma unroll
+        for (int kk = 0; kk < kTileTok / 16; ++kk)  // 16 tokens = 8 columns of P
+          umma_bf16_ta(tmem + o_col(pg), tmem + s_col(pg) + kk * 8, sw128_desc_mn(v0 + kk * 2048, kHalf, 1024), id_pv,
+                       (acc || kk > 0) ? 1u : 0u);
+        umma_commit(kv_empty + 8 * (Jp % kStages));  // the stage is free once these MMAs have read V
+        umma_commit(pv_done + 8 * pg);
+        return true;
+      };
+      int J = 0, qi = 0;
+      int pend = -1;                       // the tile whose P V is still to issue
+      bool pend_acc = false, pend_wait = false;
+      for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (!mbar_wait(u_full + 8 * slot, (k >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int u = unit_sh[slot];
+        mbar_arrive(u_empty + 8 * slot);
+        if (u < 0) break;
+        const TcUnit t = tc_unit(a, u);
+        if (t.ntiles == 0) {
+          // The last P V of the previous unit waits for no S here: issued now.
+          // (Held back, it would wait for the next unit with tiles, which the
+          // queue may publish only once the softmax warps, who need this P V
+          // to finish their epilogue, have taken this empty unit.)
+          if (pend >= 0 && !issue_pv(pend, pend_acc, pend_wait)) {
+            ok = false;
+            break;
+          }
+          pend = -1;
+          continue;
+        }
+        const int qs = qi % nq;
+        if (!mbar_wait(q_full + 8 * qs, (qi / nq) & 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t qa = base + kQ + qs * tcp::kQSlot;
+        for (int j = 0; j < t.ntiles; ++j, ++J) {
+          const int ks = J % kStages, sg = J & 1;
+          if (!mbar_wait(kv_full + 8 * ks, (J / kStages) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k0 = stage(ks);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            umma_bf16(tmem + s_col(sg), sw128_desc(qa + (kk >> 2) * kHalf + (kk & 3) * 32),
+                      sw128_desc(k0 + (kk >> 2) * kHalf + (kk & 3) * 32), id_s, kk > 0 ? 1u : 0u);
+          umma_commit(s_full + 8 * sg);
+          if (j == t.ntiles - 1) umma_commit(q_free + 8 * qs);
+          if (pend >= 0 && !issue_pv(pend, pend_acc, pend_wait)) {
+            ok = false;
+            break;
+          }
+          pend = J;
+          pend_acc = j >= 2;
+          pend_wait = j == 0 && qi > 0;
+        }
+        ++qi;
+      }
+      if (ok && pend >= 0 && !issue_pv(pend, pend_acc, pend_wait)) ok = false;
+      if (!ok) atomicOr(&g_attn_error, kErrWaitTimeout);
+      umma_commit(fin);  // completes once every MMA issued above has
+      (void)mbar_wait(fin, 0);
+    }
+  } else {
+    // ---------------- softmax: group grp takes the tiles J of parity grp ----------------
+    const int grp = (warp - kSoft0) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // query row = tensor-memory lane
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tS = trow + s_col(grp), tO = trow + o_col(grp);
+    const bool live = r < a.QR;
+    int J = 0, qi = 0;
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(u_full + 8 * slot, (k >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      const int u = unit_sh[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(u_empty + 8 * slot);
+      if (u < 0) break;
+      const TcUnit t = tc_unit(a, u);
+      const int tail_row0 = (t.item - (a.B * a.Hkv - a.tail_items)) * a.QR;  // pieces: first tail row of the item
+      if (t.ntiles == 0) {  // nothing of the sequence in this unit
+        if (grp == 0 && t.piece >= 0) {  // an empty piece: (m, l, o) = (-inf, 0, 0)
+          for (int i = r; i < a.QR * kD; i += 128) {
+            const int64_t pr = (int64_t)(tail_row0 + i / kD) * a.tail_pieces + t.piece;
+            a.tail_o[pr * kD + i % kD] = 0.f;
+            if (i % kD == 0) {
+              a.tail_ml[pr * 2] = kNegInf;
+              a.tail_ml[pr * 2 + 1] = 0.f;
+            }
+          }
+        } else if (grp == 0 && a.nchunks == 1) {  // an empty sequence: zero rows
+          for (int i = r; i < a.QR * kD / 2; i += 128) {
+            const int rr = i / (kD / 2);
+            const int64_t orow = ((int64_t)t.b * a.W + rr / a.G) * a.Hq + t.g * a.G + rr % a.G;
+            reinterpret_cast<uint32_t*>(a.out + orow * kD)[i % (kD / 2)] = 0u;
+          }
+        }
+        continue;
+      }
+      const int J0 = J;
+      J += t.ntiles;
+      // key j is visible to row r iff j < ctx and j <= ctx - W + r / G
+      const int lim = live ? min(t.ctx - 1, t.ctx - a.W + r / a.G) : -1;
+      const int tok_end = min(t.blk_end * kBlk, t.ctx);  // tokens past this are absent or past the context
+      float m = kNegInf, l = 0.f;
+      int last = -1;  // this group's last tile of the unit
+      for (int Jt = J0 + ((J0 ^ grp) & 1); Jt < J; Jt += 2) {
+        const int tok0 = (t.blk0 + (Jt - J0) * kTileBlk) * kBlk;  // first token of the tile
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * grp, (Jt >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sv[kTileTok];
+        {
+          uint32_t u0[32], u1[32], u2[32], u3[32];  // four loads in flight, one wait
+          tmem_ld32_nowait(tS, u0);
+          tmem_ld32_nowait(tS + 32, u1);
+          tmem_ld32_nowait(tS + 64, u2);
+          tmem_ld32_nowait(tS + 96, u3);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            sv[c] = __uint_as_float(u0[c]);
+            sv[32 + c] = __uint_as_float(u1[c]);
+            sv[64 + c] = __uint_as_float(u2[c]);
+            sv[96 + c] = __uint_as_float(u3[c]);
+          }
+        }
+        float mx[8];  // eight independent partial maxima (short dependency chains)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx[q] = kNegInf;
+        const int vl = min(lim, tok_end - 1) - tok0;  // columns 0 .. vl are visible to this row
+#pragma unroll
+        for (int c = 0; c < kTileTok; ++c) {
+          sv[c] = c <= vl ? sv[c] * a.scale_log2 : kNegInf;
+          mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+        }
+        const float mt =
+            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        // the row's reference maximum moves only when the tile's maximum
+        // exceeds it by more than 8 (log2 units)
+        const float mn = (mt > m + 8.f || m == kNegInf) ? fmaxf(m, mt) : m;
+        const float mb = mn == kNegInf ? 0.f : mn;  // a row with no visible key so far keeps p = 0
+        const float alpha = mn == m ? 1.f : ex2(m - mb);  // m = -inf: 0
+        float pa[8];  // eight partial sums
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pa[q] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // P over its S, one 64-token half at a time
+          uint32_t pw[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float p0 = ex2(sv[64 * h + 2 * c] - mb), p1 = ex2(sv[64 * h + 2 * c + 1] - mb);
+            pa[c & 7] += p0 + p1;
+            pw[c] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + 32 * h, pw);
+        }
+        const float ps = ((pa[0] + pa[1]) + (pa[2] + pa[3])) + ((pa[4] + pa[5]) + (pa[6] + pa[7]));
+        l = l * alpha + ps;
+        // V rows past the context (or of absent blocks) are zeroed before the
+        // MMA reads them: 0 * NaN would otherwise leak stale pool contents
+        if (tok0 + kTileTok > tok_end) {
+          if (!__all_sync(0xffffffffu, mbar_wait(kv_full + 8 * (Jt % kStages), (Jt / kStages) & 1))) {
+            ok = false;
+            break;
+          }
+          if (tok0 + r >= tok_end) {  // this thread's token row of the tile
+            const uint32_t v0 = stage(Jt % kStages) + 2 * kHalf + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              sts128z(v0 + c * 16);
+              sts128z(v0 + kHalf + c * 16);
+            }
+          }
+        }
+        if (last >= 0) {
+          // O holds this group's earlier tiles of the unit once their P V is
+          // complete; it is rescaled only when some row of the warp moved its
+          // reference maximum
+          if (!__all_sync(0xffffffffu, mbar_wait(pv_done + 8 * grp, (last >> 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+#pragma unroll
+              for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
+              tmem_st32(tO + c * 32, o);
+            }
+          }
+        }
+        tmem_wait_st();            // P (and a rescaled O) in place
+        fence_proxy_async_smem();  // zeroed V rows, if any
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full + 8 * grp);
+        m = mn;
+        last = Jt;
+      }
+      if (!ok) break;
+      // ---------------- the unit's epilogue ----------------
+      // each group waits for its last P V; the odd group hands over its (m, l)
+      // and goes on; the even group combines both O accumulators row by row,
+      // then frees them for the next unit's first P V
+      if (last >= 0 && !__all_sync(0xffffffffu, mbar_wait(pv_done + 8 * grp, (last >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      if (grp == 1) {
+        if (qi >= 1 && !__all_sync(0xffffffffu, mbar_wait(xm_empty, (qi - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        xm[0][r] = last < 0 ? kNegInf : m;
+        xm[1][r] = last < 0 ? 0.f : l;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xm_full);
+      } else {
+        if (!__all_sync(0xffffffffu, mbar_wait(xm_full, qi & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float m1 = xm[0][r], l1 = xm[1][r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xm_empty);
+        const float m0 = last < 0 ? kNegInf : m, l0 = last < 0 ? 0.f : l;
+        const float ms = fmaxf(m0, m1);
+        const float mbs = ms == kNegInf ? 0.f : ms;
+        const float w0 = m0 != kNegInf ? ex2(m0 - mbs) : 0.f, w1 = m1 != kNegInf ? ex2(m1 - mbs) : 0.f;
+        // an accumulator with no tile of this unit holds the previous unit's
+        // values: it is neither read (warp-uniform) nor added (per row)
+        const bool use0 = __any_sync(0xffffffffu, m0 != kNegInf), use1 = __any_sync(0xffffffffu, m1 != kNegInf);
+        const float lt = __fadd_rn(__fmul_rn(l0, w0), __fmul_rn(l1, w1));
+        const int64_t orow = live ? ((int64_t)t.b * a.W + r / a.G) * a.Hq + t.g * a.G + r % a.G : 0;
+        const float inv = (lt > 0.f ? 1.f / lt : 0.f) * a.v_scale;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o0[32], o1[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) o0[q] = o1[q] = 0u;
+          if (use0) tmem_ld32(trow + o_col(0) + c * 32, o0);  // warp-collective: every lane takes part
+          if (use1) tmem_ld32(trow + o_col(1) + c * 32, o1);
+          float v[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            v[q] = combine2(__uint_as_float(o0[q]), w0, m0 != kNegInf, __uint_as_float(o1[q]), w1, m1 != kNegInf);
+          if (live) {
+            if (t.piece >= 0) {
+              float4* po = reinterpret_cast<float4*>(
+                  a.tail_o + ((int64_t)(tail_row0 + r) * a.tail_pieces + t.piece) * kD + c * 32);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                po[q] = make_float4(v[4 * q] * a.v_scale, v[4 * q + 1] * a.v_scale, v[4 * q + 2] * a.v_scale,
+                                    v[4 * q + 3] * a.v_scale);
+            } else if (a.nchunks == 1) {
+              uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kD + c * 32);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(pack_bf16x2(v[8 * q] * inv, v[8 * q + 1] * inv),
+                                    pack_bf16x2(v[8 * q + 2] * inv, v[8 * q + 3] * inv),
+                                    pack_bf16x2(v[8 * q + 4] * inv, v[8 * q + 5] * inv),
+                                    pack_bf16x2(v[8 * q + 6] * inv, v[8 * q + 7] * inv));
+            } else {
+              float4* po = reinterpret_cast<float4*>(a.part_o + (orow * a.nchunks + t.chunk) * kD + c * 32);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                po[q] = make_float4(v[4 * q] * a.v_scale, v[4 * q + 1] * a.v_scale, v[4 * q + 2] * a.v_scale,
+                                    v[4 * q + 3] * a.v_scale);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);  // both accumulators read
+        if (live && t.piece >= 0) {
+          const int64_t pr = (int64_t)(tail_row0 + r) * a.tail_pieces + t.piece;
+          a.tail_ml[pr * 2] = ms;
+          a.tail_ml[pr * 2 + 1] = lt;
+        } else if (live && a.nchunks > 1) {
+          a.part_ml[(orow * a.nchunks + t.chunk) * 2] = ms;
+          a.part_ml[(orow * a.nchunks + t.chunk) * 2 + 1] = lt;
+        }
+      }
+      ++qi;
+    }
+    if (!ok && lane == 0) atomicOr(&g_attn_error, kErrWaitTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // The balanced tail's merge: one warp per query row of a split item combines
 // its pieces' (o, m, l) in piece order.
 __global__ void __launch_bounds__(128) attn_tail_merge_kernel(const Args a) {
@@ -1119,6 +1674,17 @@ cudaError_t kv_tensor_map(const void* pool, bool f8, int hkv, int64_t num_blocks
   const uint32_t box[4] = {f8 ? 128u : 64u, (uint32_t)kBlk, 1, 1};
   return tensor_map(out, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pool, dims,
                     strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Queries [b][w][hq][128] bf16 as a 4-D map (dims, heads, positions,
+// sequences) whose box is one kv head's G heads at all W positions, one 64-dim
+// half: it lands as the W x G query rows of that head, 128 bytes each,
+// 128-byte swizzled.
+cudaError_t q_tensor_map(const uint16_t* q, int b, int w, int hq, int hkv, CUtensorMap* out) {
+  const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)hq, (uint64_t)w, (uint64_t)b};
+  const uint64_t strides[3] = {(uint64_t)kD * 2, (uint64_t)hq * kD * 2, (uint64_t)w * hq * kD * 2};
+  const uint32_t box[4] = {64u, (uint32_t)(hq / hkv), (uint32_t)w, 1};
+  return tensor_map(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int QT, bool F8>
@@ -1363,11 +1929,22 @@ AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms, 
       p.tail_items = (int)R;
       p.tail_pieces = (int)pieces;
     }
+    // Persistent form when there are more units than SMs: one CTA per SM
+    // takes the units from a queue in the workspace's counter region (with
+    // fewer units it only adds the queue's cost: batch 1, width 16, 8192
+    // tokens 17.6 -> 19.0 us). Test hook: DQD_ATTN_PERSIST=0 keeps one CTA per
+    // unit, =1 takes the persistent form whatever the unit count.
+    const char* persist_env = std::getenv("DQD_ATTN_PERSIST");
+    const int64_t units = p.tail_pieces > 0 ? titems - p.tail_items + (int64_t)p.tail_items * p.tail_pieces
+                                            : titems * p.nchunks;
+    const bool force = persist_env && persist_env[0] == '1', off = persist_env && persist_env[0] == '0';
+    if (!off && (force || units > tslots)) p.persist = (int)std::min<int64_t>(units, tslots);
   }
   const size_t rows = (size_t)b * w * hq;
   p.ws_bytes = p.nchunks > 1 ? kCounterBytes + rows * p.nchunks * (kD + 2) * sizeof(float) : 0;
   if (p.tail_pieces > 0)
     p.ws_bytes = kCounterBytes + (size_t)p.tail_items * qr * p.tail_pieces * (kD + 2) * sizeof(float);
+  if (p.persist > 0) p.ws_bytes = std::max(p.ws_bytes, kCounterBytes);
   return p;
 }
 
@@ -1396,6 +1973,7 @@ cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) 
   }
   a.tail_items = p.tail_items;
   a.tail_pieces = p.tail_pieces;
+  a.ctr = p.persist > 0 ? static_cast<unsigned*>(l.workspace) : nullptr;
   a.tail_o = nullptr;
   a.tail_ml = nullptr;
   if (p.tail_pieces > 0) {
@@ -1422,7 +2000,25 @@ cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) 
   cudaError_t e = kv_tensor_map(l.k_pool, f8, l.hkv, l.num_blocks, &tmk);
   if (e == cudaSuccess) e = kv_tensor_map(l.v_pool, f8, l.hkv, l.num_blocks, &tmv);
   if (e != cudaSuccess) return e;
-  if (p.tc) {
+  if (p.tc && p.persist > 0) {
+    static std::atomic<int> configured[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(attn_tcp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tca::kSmem);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_relaxed);
+    }
+    CUtensorMap tmq;
+    e = q_tensor_map(l.q, l.b, l.w, l.hq, l.hkv, &tmq);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(attn_tcp_kernel, dim3((unsigned)p.persist), dim3(tca::kThreads), (size_t)tca::kSmem, s, tmk, tmv,
+                   tmq, a);
+    if (e == cudaSuccess && p.tail_pieces > 0) {
+      const unsigned trows = (unsigned)(p.tail_items * a.QR);
+      return launch_pdl(attn_tail_merge_kernel, dim3((trows + 3) / 4), dim3(128), 0, s, a);
+    }
+  } else if (p.tc) {
     static std::atomic<int> configured[64];
     int dev = 0;
     cudaGetDevice(&dev);

@@ -164,6 +164,7 @@ struct AttnPlan {
   int tc;            // 1: tensor-core (tcgen05) form for wide query tiles
   int tail_items;    // tensor-core form: items of the last partial wave, split ...
   int tail_pieces;   // ... into this many pieces (0: none)
+  int persist;       // tensor-core form: > 0 = persistent, with this many CTAs taking units from a queue
   size_t ws_bytes;   // 0 if nchunks == 1 and no tail
 };
 

@@ -237,13 +237,18 @@ def test_tensor_core_form(dev, dqd, monkeypatch, B, W, hq, hkv, ctx, cb):
     """The tcgen05 form (S and O in tensor memory, V as an MN-major operand)
     against the oracle, and against the mma.sync form within tolerance, for
     every chunking: chunks of whole tiles, of partial tiles, and of 1 block;
-    bit-identical on a rerun."""
+    bit-identical on a rerun and with one CTA per work unit instead of the
+    persistent CTAs."""
     if cb is not None:
         monkeypatch.setenv("DQD_ATTN_CHUNK_BLOCKS", str(cb))
     kv = synth.paged_kv(B * 7 + W, "kv", ctx, hkv, spare_blocks=3)
     q = synth.normal_bf16(B + W + hq, "q", (B, W, hq, 128))
     a = run(dqd, dev, q, kv, hkv)
     assert np.array_equal(bits(a), bits(run(dqd, dev, q, kv, hkv)))
+    for persist in ("0", "1"):  # one CTA per unit; persistent CTAs taking units from the queue
+        monkeypatch.setenv("DQD_ATTN_PERSIST", persist)
+        assert np.array_equal(bits(a), bits(run(dqd, dev, q, kv, hkv))), f"DQD_ATTN_PERSIST={persist}"
+    monkeypatch.delenv("DQD_ATTN_PERSIST")
     r = ref(q, kv, hkv)
     assert_close(f64(a), r, what=f"tc attn B={B} W={W} {hq}/{hkv} ctx={ctx} cb={cb}")
     monkeypatch.setenv("DQD_ATTN_TC", "0")
@@ -270,7 +275,51 @@ def test_tensor_core_balanced_tail(dev, dqd, monkeypatch, B, W, hq, hkv):
     q = synth.normal_bf16(B * W, "q", (B, W, hq, 128), std=0.5)
     a = run(dqd, dev, q, kv, hkv)
     assert np.array_equal(bits(a), bits(run(dqd, dev, q, kv, hkv)))
+    monkeypatch.setenv("DQD_ATTN_PERSIST", "0")
+    assert np.array_equal(bits(a), bits(run(dqd, dev, q, kv, hkv))), "one CTA per unit"
+    monkeypatch.delenv("DQD_ATTN_PERSIST")
     assert_close(f64(a), ref(q, kv, hkv), what=f"tc balanced tail B={B} W={W} {hq}/{hkv}")
     monkeypatch.setenv("DQD_ATTN_TAIL", "0")
     assert_close(f64(a), f64(run(dqd, dev, q, kv, hkv)), what="whole items")
+    assert dqd.device_errors() == 0
+
+
+@pytest.mark.parametrize("B,W,hq,hkv,lo,hi,cb", [
+    (64, 16, 32, 8, 16, 700, None),   # 64 rows (two Q slots), 1-6 tiles per unit, odd and even counts
+    (40, 16, 64, 8, 16, 900, None),   # 128 rows (one Q slot)
+    (64, 6, 32, 8, 200, 2000, 8),     # 24 rows, 8-block chunks: many units per CTA, empty ones too
+    (20, 16, 64, 8, 256, 1500, None), # 128 rows, a balanced tail of eight pieces per item
+])
+def test_tensor_core_persistent_queue(dev, dqd, monkeypatch, B, W, hq, hkv, lo, hi, cb):
+    """The persistent tcgen05 form with many units per CTA, taken from the
+    queue in the workspace's counter region: the same bits as one CTA per unit
+    (the two softmax groups' accumulators are combined symmetrically, so the
+    schedule cannot change the result), the same bits on reruns over one
+    workspace, and the queue's counters back at zero after every call."""
+    if cb is not None:
+        monkeypatch.setenv("DQD_ATTN_CHUNK_BLOCKS", str(cb))
+    rng = np.random.default_rng(B * 1000 + W * 10 + hq)
+    ctx = tuple(int(c) for c in rng.integers(max(lo, W), hi + 1, size=B))
+    kv = synth.paged_kv(B * 3 + W, "kv", ctx, hkv, spare_blocks=2)
+    q = synth.normal_bf16(B * 5 + W, "q", (B, W, hq, 128), std=0.5)
+    maxc = max(ctx)
+    need = dqd.gqa_decode_attn_workspace_bytes(B, W, hq, hkv, 128, maxc)
+    assert need >= 65536, "the persistent form needs the counter region"
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    args = (bf(q, dev), bf(kv.k_pool, dev), bf(kv.v_pool, dev), i32(kv.block_table, dev),
+            i32(np.asarray(ctx, np.int32), dev), maxc)
+    outs = []
+    for _ in range(3):
+        outs.append(dqd.gqa_decode_attn(*args, ws=ws))
+        torch.cuda.synchronize()
+        assert int(torch.count_nonzero(ws[:8]).item()) == 0, "queue counters left nonzero"
+    for o in outs[1:]:
+        assert np.array_equal(bits(o), bits(outs[0])), "rerun differs"
+    monkeypatch.setenv("DQD_ATTN_PERSIST", "0")
+    assert np.array_equal(bits(outs[0]), bits(dqd.gqa_decode_attn(*args))), "one CTA per unit differs"
+    # parity is carried by the bit comparison above (the one-CTA-per-unit form
+    # meets the oracle at 1% in the tests before); against the oracle directly
+    # at 2%: with these many short contexts a rare element of either form sits
+    # just past 1%, the bf16 rounding of P (1.13x the 1% bound at 20 x 16 x 64)
+    assert_close(f64(outs[0]), ref(q, kv, hkv), tol=2e-2, what=f"persistent tc B={B} W={W} {hq}/{hkv}")
     assert dqd.device_errors() == 0
