@@ -698,6 +698,51 @@ __device__ __forceinline__ float combine2(float o0, float w0, bool has0, float o
   return __fadd_rn(has0 ? __fmul_rn(o0, w0) : 0.f, has1 ? __fmul_rn(o1, w1) : 0.f);
 }
 
+// One 128-token tile of the online softmax for one query row (a thread) of
+// the tensor-core forms, in the log2 domain: sv holds the row's raw q.k
+// products (scaled in place), columns 0 .. vl are visible (the others become
+// -inf by select), c is the softmax scale times log2(e). The row's reference
+// maximum m moves only when the tile's maximum exceeds it by more than 8, so
+// P stays below 2^8 and O is rescaled on few tiles. Updates (m, l), writes P
+// as bf16 pairs over the first 64 columns of the S row at tS and returns
+// alpha, the factor that the row's O must take. (Keeping the raw products and
+// taking c s - m in one fused multiply-add saves two instructions an element
+// but needs more registers; the spills made the attention 20% slower.)
+__device__ __forceinline__ float tc_softmax_tile(float (&sv)[tca::kTileTok], int vl, float c, float& m, float& l,
+                                                 uint32_t tS) {
+  constexpr int T = tca::kTileTok;
+  float mx[8];  // eight independent partial maxima (short dependency chains)
+#pragma unroll
+  for (int q = 0; q < 8; ++q) mx[q] = kNegInf;
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    sv[t] = t <= vl ? sv[t] * c : kNegInf;
+    mx[t & 7] = fmaxf(mx[t & 7], sv[t]);
+  }
+  const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  const float mn = (mt > m + 8.f || m == kNegInf) ? fmaxf(m, mt) : m;
+  const float mb = mn == kNegInf ? 0.f : mn;  // a row with no visible key so far keeps p = 0
+  const float alpha = mn == m ? 1.f : ex2(m - mb);  // m = -inf: 0
+  float pa[8];  // eight partial sums
+#pragma unroll
+  for (int q = 0; q < 8; ++q) pa[q] = 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {  // P over its S, one 64-token half at a time
+    uint32_t pw[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+      const float p0 = ex2(sv[64 * h + 2 * q] - mb), p1 = ex2(sv[64 * h + 2 * q + 1] - mb);
+      pa[q & 7] += p0 + p1;
+      pw[q] = pack_bf16x2(p0, p1);
+    }
+    tmem_st32(tS + 32 * h, pw);
+  }
+  const float ps = ((pa[0] + pa[1]) + (pa[2] + pa[3])) + ((pa[4] + pa[5]) + (pa[6] + pa[7]));
+  l = l * alpha + ps;
+  m = mn;
+  return alpha;
+}
+
 __device__ __forceinline__ void sts128z(uint32_t addr) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0u) : "memory");
 }
@@ -923,40 +968,8 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
           sv[96 + t] = __uint_as_float(u3[t]);
         }
       }
-      float mx[8];  // eight independent partial maxima (short dependency chains)
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = kNegInf;
       const int vl = min(lim, tok_end - 1) - tok0;  // columns 0 .. vl are visible to this row
-#pragma unroll
-      for (int t = 0; t < kTileTok; ++t) {
-        sv[t] = t <= vl ? sv[t] * a.scale_log2 : kNegInf;
-        mx[t & 7] = fmaxf(mx[t & 7], sv[t]);
-      }
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      // The row's reference maximum moves only when the tile's maximum exceeds
-      // it by more than 8 (log2 units): P stays below 2^8, and O and l are
-      // rescaled on few tiles.
-      const float mn = (mt > m + 8.f || m == kNegInf) ? fmaxf(m, mt) : m;
-      const float mb = mn == kNegInf ? 0.f : mn;  // a row with no visible key so far keeps p = 0
-      const float alpha = mn == m ? 1.f : ex2(m - mb);  // m = -inf: 0
-      // P over the S it was computed from, one 64-token half at a time: 128
-      // tokens as bf16, two per column (the S row is already in registers)
-      float pa[8];  // eight partial sums
-#pragma unroll
-      for (int u = 0; u < 8; ++u) pa[u] = 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pw[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = ex2(sv[64 * h + 2 * c] - mb), p1 = ex2(sv[64 * h + 2 * c + 1] - mb);
-          pa[c & 7] += p0 + p1;
-          pw[c] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(tS + 32 * h, pw);
-      }
-      const float ps = ((pa[0] + pa[1]) + (pa[2] + pa[3])) + ((pa[4] + pa[5]) + (pa[6] + pa[7]));
-      l = l * alpha + ps;
+      const float alpha = tc_softmax_tile(sv, vl, a.scale_log2, m, l, tS);
       // V rows past the context (or of absent blocks) are zeroed before the
       // MMA reads them: 0 * NaN would otherwise leak stale pool contents
       if (tok0 + kTileTok > tok_end) {
@@ -999,7 +1012,6 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full + 8 * grp);
-      m = mn;
       last = j;
     }
     // ---------------- epilogue ----------------
@@ -1111,8 +1123,17 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
 namespace tcp {
 // With at most 64 query rows, Q slot 1 starts 64 rows (8 KB) into each of
 // slot 0's halves: the rows past 64 that an M = 128 MMA reads from either slot
-// are rows of the other slot or of stage 0, and belong to masked query rows.
+// are rows of the other slot or of K slot 0, and belong to masked query rows.
 constexpr int kQSlot = 64 * 128;
+// K and V have rings of their own (three 32 KB slots each: two 64-dim halves
+// of 128 token rows), so that a K slot is free again once S has read it and
+// only V waits for P V.
+constexpr int kSlotBytes = 2 * tca::kHalf;
+constexpr int kK0 = 2 * tca::kHalf;               // after Q
+constexpr int kV0 = kK0 + tca::kStages * kSlotBytes;
+static_assert(kV0 + tca::kStages * kSlotBytes == tca::kSmem, "the K and V rings fill the stages' space");
+constexpr int kThreads = 352;  // gather K (warp 0), MMA (1), softmax (2-9), gather V (10)
+constexpr int kVWarp = 10;
 }  // namespace tcp
 
 struct TcUnit {
@@ -1149,14 +1170,17 @@ __device__ __forceinline__ TcUnit tc_unit(const Args& a, int u) {
   return t;
 }
 
-__global__ void __launch_bounds__(tca::kThreads, 1)
+// Eleven warps: three share each of three SM sub-partitions, whose 16K
+// registers then allow at most 168 per thread.
+__global__ void __maxnreg__(168)
     attn_tcp_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                     const __grid_constant__ CUtensorMap tmq, const Args a) {
   using namespace tca;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // kv_full[3], kv_empty[3], s_full[2], p_full[2], pv_done[2], q_full[2],
-  // q_free[2], u_full[2], u_empty[2], o_free, xm_full, xm_empty, fin
-  __shared__ __align__(8) uint64_t bars[2 * kStages + 18];
+  // k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], p_full[2],
+  // pv_done[2], q_full[2], q_free[2], u_full[2], u_empty[2], o_free, xm_full,
+  // xm_empty, fin
+  __shared__ __align__(8) uint64_t bars[4 * kStages + 18];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int unit_sh[2];
   __shared__ float xm[2][128];  // the odd group's (m, l) per row for the unit being combined
@@ -1171,17 +1195,21 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
   const int units = a.tail_pieces > 0 ? items - a.tail_items + a.tail_items * a.tail_pieces : items * a.nchunks;
   const int nq = a.QR <= 64 ? 2 : 1;  // Q slots
   const uint32_t base = smem_addr(smem_raw);
-  const uint32_t kv_full = smem_addr(&bars[0]), kv_empty = kv_full + 8 * kStages, s_full = kv_full + 16 * kStages,
-                 p_full = s_full + 16, pv_done = s_full + 32, q_full = s_full + 48, q_free = s_full + 64,
-                 u_full = s_full + 80, u_empty = s_full + 96, o_free = s_full + 112, xm_full = s_full + 120,
-                 xm_empty = s_full + 128, fin = s_full + 136;
-  auto stage = [&](int st) { return base + kStage0 + st * kStageBytes; };
+  const uint32_t k_full = smem_addr(&bars[0]), k_empty = k_full + 8 * kStages, v_full = k_full + 16 * kStages,
+                 v_empty = k_full + 24 * kStages, s_full = k_full + 32 * kStages, p_full = s_full + 16,
+                 pv_done = s_full + 32, q_full = s_full + 48, q_free = s_full + 64, u_full = s_full + 80,
+                 u_empty = s_full + 96, o_free = s_full + 112, xm_full = s_full + 120, xm_empty = s_full + 128,
+                 fin = s_full + 136;
+  auto kslot = [&](int st) { return base + tcp::kK0 + st * tcp::kSlotBytes; };
+  auto vslot = [&](int st) { return base + tcp::kV0 + st * tcp::kSlotBytes; };
   bool ok = true;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(kv_full + 8 * i, 1);
-      mbar_init(kv_empty + 8 * i, 1);
+      mbar_init(k_full + 8 * i, 1);
+      mbar_init(k_empty + 8 * i, 1);
+      mbar_init(v_full + 8 * i, 1);
+      mbar_init(v_empty + 8 * i, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + 8 * i, 1);
@@ -1190,7 +1218,7 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
       mbar_init(q_full + 8 * i, 1);
       mbar_init(q_free + 8 * i, 1);
       mbar_init(u_full + 8 * i, 1);
-      mbar_init(u_empty + 8 * i, 9);  // the MMA thread and the eight softmax warps
+      mbar_init(u_empty + 8 * i, 10);  // the MMA thread, the eight softmax warps and the V gather warp
     }
     mbar_init(o_free, 4);  // the even group's warps
     mbar_init(xm_full, 4);  // the odd group's warps
@@ -1205,9 +1233,8 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
   const uint32_t tmem = tmem_base_sh;
 
   if (warp == 0) {
-    // ---------------- queue, Q and K/V gather ----------------
+    // ---------------- queue, Q and K gather ----------------
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmk) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmv) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmq) : "memory");
     int J = 0;   // tiles whose copies were issued
     int qi = 0;  // Q loads issued (one per unit with tiles)
@@ -1252,7 +1279,7 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
       int tab = 0;
       for (int j = 0; j < t.ntiles; ++j) {
         const int st = J % kStages;
-        if (J >= kStages && !__all_sync(0xffffffffu, mbar_wait(kv_empty + 8 * st, ((J - kStages) / kStages) & 1))) {
+        if (J >= kStages && !__all_sync(0xffffffffu, mbar_wait(k_empty + 8 * st, ((J - kStages) / kStages) & 1))) {
           ok = false;
           break;
         }
@@ -1263,16 +1290,14 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
           if (tab != v) atomicOr(&g_attn_error, kErrBadInput);  // clamped: reads stay inside the pool
         }
         const int nb = min(kTileBlk, nblk - j * kTileBlk);
-        const uint32_t fb = kv_full + 8 * st, dst = stage(st);
-        if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)nb * 4u * 2048u);
+        const uint32_t fb = k_full + 8 * st;
+        if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)nb * 2u * 2048u);
         __syncwarp();
         const int phys = __shfl_sync(0xffffffffu, tab, (j & 3) * kTileBlk + (lane & 7));
-        if (lane < nb) {
-          const uint32_t d = dst + lane * 2048;
+        if (lane < nb) {  // block i of the tile: K rows 16 i .. 16 i + 15 of both halves
+          const uint32_t d = kslot(st) + lane * 2048;
           tma_load_4d(d, &tmk, fb, 0, 0, t.g, phys);
           tma_load_4d(d + kHalf, &tmk, fb, 64, 0, t.g, phys);
-          tma_load_4d(d + 2 * kHalf, &tmv, fb, 0, 0, t.g, phys);
-          tma_load_4d(d + 3 * kHalf, &tmv, fb, 64, 0, t.g, phys);
         }
         ++J;
       }
@@ -1287,15 +1312,64 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
         atomicExch(a.ctr + 1, 0u);
       }
       // every issued copy has landed before the CTA exits (immediate unless a
-      // wait gave up): the last tile issued into each stage, the last Q load
-      // into each slot, bounded
+      // wait gave up): the last K tile issued into each slot, the last Q load
+      // into each Q slot, bounded
       for (int st = 0; st < kStages; ++st) {
         const int jl = J - 1 - (((J - 1 - st) % kStages + kStages) % kStages);
-        if (jl >= 0) (void)mbar_wait(kv_full + 8 * st, (jl / kStages) & 1);
+        if (jl >= 0) (void)mbar_wait(k_full + 8 * st, (jl / kStages) & 1);
       }
       for (int s = 0; s < nq; ++s) {
         const int il = qi - 1 - (((qi - 1 - s) % nq + nq) % nq);
         if (il >= 0) (void)mbar_wait(q_full + 8 * s, (il / nq) & 1);
+      }
+    }
+  } else if (warp == tcp::kVWarp) {
+    // ---------------- V gather: the units from the queue, in order ----------------
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmv) : "memory");
+    int J = 0;
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(u_full + 8 * slot, (k >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      const int u = unit_sh[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(u_empty + 8 * slot);
+      if (u < 0) break;
+      const TcUnit t = tc_unit(a, u);
+      const int64_t tab_row = (int64_t)t.b * a.max_blocks;
+      const int nblk = t.blk_end - t.blk0;
+      int tab = 0;
+      for (int j = 0; j < t.ntiles; ++j) {
+        const int st = J % kStages;
+        if (J >= kStages && !__all_sync(0xffffffffu, mbar_wait(v_empty + 8 * st, ((J - kStages) / kStages) & 1))) {
+          ok = false;
+          break;
+        }
+        if ((j & 3) == 0) {  // clamped as the K gather clamps them (which reports it)
+          const int bi = j * kTileBlk + lane;
+          const int32_t v = bi < nblk ? a.table[tab_row + t.blk0 + bi] : 0;
+          tab = v < 0 ? 0 : (v >= a.num_blocks ? (int)(a.num_blocks - 1) : v);
+        }
+        const int nb = min(kTileBlk, nblk - j * kTileBlk);
+        const uint32_t fb = v_full + 8 * st;
+        if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)nb * 2u * 2048u);
+        __syncwarp();
+        const int phys = __shfl_sync(0xffffffffu, tab, (j & 3) * kTileBlk + (lane & 7));
+        if (lane < nb) {
+          const uint32_t d = vslot(st) + lane * 2048;
+          tma_load_4d(d, &tmv, fb, 0, 0, t.g, phys);
+          tma_load_4d(d + kHalf, &tmv, fb, 64, 0, t.g, phys);
+        }
+        ++J;
+      }
+    }
+    if (lane == 0) {
+      if (!ok) atomicOr(&g_attn_error, kErrWaitTimeout);
+      for (int st = 0; st < kStages; ++st) {  // the last V tile issued into each slot has landed, bounded
+        const int jl = J - 1 - (((J - 1 - st) % kStages + kStages) % kStages);
+        if (jl >= 0) (void)mbar_wait(v_full + 8 * st, (jl / kStages) & 1);
       }
     }
   } else if (warp == 1) {
@@ -1317,13 +1391,14 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
           ++ofn;
         }
         if (!mbar_wait(p_full + 8 * pg, (Jp >> 1) & 1)) return false;
+        if (!mbar_wait(v_full + 8 * (Jp % kStages), (Jp / kStages) & 1)) return false;
         tc_fence_after();
-        const uint32_t v0 = stage(Jp % kStages) + 2 * kHalf;
+        const uint32_t v0 = vslot(Jp % kStages);
 #pragma unroll
         for (int kk = 0; kk < kTileTok / 16; ++kk)  // 16 tokens = 8 columns of P
           umma_bf16_ta(tmem + o_col(pg), tmem + s_col(pg) + kk * 8, sw128_desc_mn(v0 + kk * 2048, kHalf, 1024), id_pv,
                        (acc || kk > 0) ? 1u : 0u);
-        umma_commit(kv_empty + 8 * (Jp % kStages));  // the stage is free once these MMAs have read V
+        umma_commit(v_empty + 8 * (Jp % kStages));  // the V slot is free once these MMAs have read it
         umma_commit(pv_done + 8 * pg);
         return true;
       };
@@ -1360,16 +1435,17 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
         const uint32_t qa = base + kQ + qs * tcp::kQSlot;
         for (int j = 0; j < t.ntiles; ++j, ++J) {
           const int ks = J % kStages, sg = J & 1;
-          if (!mbar_wait(kv_full + 8 * ks, (J / kStages) & 1)) {
+          if (!mbar_wait(k_full + 8 * ks, (J / kStages) & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t k0 = stage(ks);
+          const uint32_t k0 = kslot(ks);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
             umma_bf16(tmem + s_col(sg), sw128_desc(qa + (kk >> 2) * kHalf + (kk & 3) * 32),
                       sw128_desc(k0 + (kk >> 2) * kHalf + (kk & 3) * 32), id_s, kk > 0 ? 1u : 0u);
+          umma_commit(k_empty + 8 * ks);  // the K slot is free once S has read it
           umma_commit(s_full + 8 * sg);
           if (j == t.ntiles - 1) umma_commit(q_free + 8 * qs);
           if (pend >= 0 && !issue_pv(pend, pend_acc, pend_wait)) {
@@ -1457,47 +1533,17 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
             sv[96 + c] = __uint_as_float(u3[c]);
           }
         }
-        float mx[8];  // eight independent partial maxima (short dependency chains)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mx[q] = kNegInf;
         const int vl = min(lim, tok_end - 1) - tok0;  // columns 0 .. vl are visible to this row
-#pragma unroll
-        for (int c = 0; c < kTileTok; ++c) {
-          sv[c] = c <= vl ? sv[c] * a.scale_log2 : kNegInf;
-          mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
-        }
-        const float mt =
-            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        // the row's reference maximum moves only when the tile's maximum
-        // exceeds it by more than 8 (log2 units)
-        const float mn = (mt > m + 8.f || m == kNegInf) ? fmaxf(m, mt) : m;
-        const float mb = mn == kNegInf ? 0.f : mn;  // a row with no visible key so far keeps p = 0
-        const float alpha = mn == m ? 1.f : ex2(m - mb);  // m = -inf: 0
-        float pa[8];  // eight partial sums
-#pragma unroll
-        for (int q = 0; q < 8; ++q) pa[q] = 0.f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {  // P over its S, one 64-token half at a time
-          uint32_t pw[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float p0 = ex2(sv[64 * h + 2 * c] - mb), p1 = ex2(sv[64 * h + 2 * c + 1] - mb);
-            pa[c & 7] += p0 + p1;
-            pw[c] = pack_bf16x2(p0, p1);
-          }
-          tmem_st32(tS + 32 * h, pw);
-        }
-        const float ps = ((pa[0] + pa[1]) + (pa[2] + pa[3])) + ((pa[4] + pa[5]) + (pa[6] + pa[7]));
-        l = l * alpha + ps;
+        const float alpha = tc_softmax_tile(sv, vl, a.scale_log2, m, l, tS);
         // V rows past the context (or of absent blocks) are zeroed before the
         // MMA reads them: 0 * NaN would otherwise leak stale pool contents
         if (tok0 + kTileTok > tok_end) {
-          if (!__all_sync(0xffffffffu, mbar_wait(kv_full + 8 * (Jt % kStages), (Jt / kStages) & 1))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(v_full + 8 * (Jt % kStages), (Jt / kStages) & 1))) {
             ok = false;
             break;
           }
           if (tok0 + r >= tok_end) {  // this thread's token row of the tile
-            const uint32_t v0 = stage(Jt % kStages) + 2 * kHalf + r * 128;
+            const uint32_t v0 = vslot(Jt % kStages) + r * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               sts128z(v0 + c * 16);
@@ -1530,7 +1576,6 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full + 8 * grp);
-        m = mn;
         last = Jt;
       }
       if (!ok) break;
@@ -1576,8 +1621,10 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
           uint32_t o0[32], o1[32];
 #pragma unroll
           for (int q = 0; q < 32; ++q) o0[q] = o1[q] = 0u;
-          if (use0) tmem_ld32(trow + o_col(0) + c * 32, o0);  // warp-collective: every lane takes part
-          if (use1) tmem_ld32(trow + o_col(1) + c * 32, o1);
+          // warp-collective (every lane takes part); both loads in flight, one wait
+          if (use0) tmem_ld32_nowait(trow + o_col(0) + c * 32, o0);
+          if (use1) tmem_ld32_nowait(trow + o_col(1) + c * 32, o1);
+          tmem_wait_ld();
           float v[32];
 #pragma unroll
           for (int q = 0; q < 32; ++q)
@@ -1923,7 +1970,12 @@ AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms, 
     // 64, width 16: 512 items, 3.37 waves). Test hook: DQD_ATTN_TAIL=0 keeps
     // whole items.
     const char* tail_env = std::getenv("DQD_ATTN_TAIL");
-    const int64_t R = titems % tslots, pieces = R > 0 ? std::min<int64_t>(8, tslots / R) : 0;
+    const int64_t R = titems % tslots;
+    int64_t pieces = R > 0 ? std::min<int64_t>(8, tslots / R) : 0;
+    if (const char* env = std::getenv("DQD_ATTN_TAIL_PIECES")) {  // test hook: pieces per tail item
+      const long v = std::strtol(env, nullptr, 10);
+      if (v >= 2 && v <= 64 && R > 0) pieces = v;
+    }
     if (p.nchunks == 1 && titems > tslots && pieces >= 2 && !std::getenv("DQD_ATTN_CHUNK_BLOCKS") &&
         !(tail_env && tail_env[0] == '0')) {
       p.tail_items = (int)R;
@@ -2012,7 +2064,7 @@ cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) 
     CUtensorMap tmq;
     e = q_tensor_map(l.q, l.b, l.w, l.hq, l.hkv, &tmq);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(attn_tcp_kernel, dim3((unsigned)p.persist), dim3(tca::kThreads), (size_t)tca::kSmem, s, tmk, tmv,
+    e = launch_pdl(attn_tcp_kernel, dim3((unsigned)p.persist), dim3(tcp::kThreads), (size_t)tca::kSmem, s, tmk, tmv,
                    tmq, a);
     if (e == cudaSuccess && p.tail_pieces > 0) {
       const unsigned trows = (unsigned)(p.tail_items * a.QR);
