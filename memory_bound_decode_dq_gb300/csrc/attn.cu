@@ -71,9 +71,11 @@ struct Args {
   int tail_items, tail_pieces;
   float* tail_o;
   float* tail_ml;
+  uint8_t* tail_seq;  // [kLptMaxB] the longest-first order, written by CTA 0 for the tail merge
   // persistent tensor-core form: the work queue's ticket and finished-CTA
   // count (the workspace's counter region; zero on entry and on exit)
   unsigned* ctr;
+  int lpt;  // tensor-core forms: 1 = longest-first order of the sequences (B <= kLptMaxB)
 };
 
 // Per-module device error word (kErrWaitTimeout when a bounded wait gave up,
@@ -698,6 +700,97 @@ __device__ __forceinline__ float combine2(float o0, float w0, bool has0, float o
   return __fadd_rn(has0 ? __fmul_rn(o0, w0) : 0.f, has1 ? __fmul_rn(o1, w1) : 0.f);
 }
 
+// Work units of the tensor-core forms, in a longest-first order of the
+// sequences when there are at most kLptMaxB of them and the order matters (the
+// persistent form, whose CTAs take units in order; a balanced tail, whose
+// pieces split the last items): the units of the longest contexts go first
+// and the tail splits the shortest ones, so that no long unit starts last (a
+// CTA that did would finish long after the others). Every kernel that maps
+// units or tail rows to (sequence, kv head) then takes the same order, so the
+// two forms split the same items. Ties go by index: the order is
+// deterministic. Otherwise units follow the sequence index.
+constexpr int kLptMaxB = 256;
+
+// seq[p] = the sequence at position p of that order, for every p < B <=
+// kLptMaxB. Every thread of the CTA takes part (the caller synchronises
+// before reading): each lane loads its share of the context lengths once, and
+// warp w ranks sequences w, w + warps, ... by a count over all of them. Not
+// inlined: it runs once per CTA, and inlined its registers added spills to
+// the tensor-core kernels' tile loops.
+__device__ __noinline__ void lpt_order(const Args& a, uint8_t* seq) {
+  constexpr int K = kLptMaxB / 32;
+  if (!a.lpt) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  int c[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) c[k] = lane + 32 * k < a.B ? seq_ctx(a, lane + 32 * k) : -1;
+  for (int b = warp; b < a.B; b += nwarps) {
+    int cb = 0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {  // warp-uniform: b is the same in every lane
+      const int v = __shfl_sync(0xffffffffu, c[k], b & 31);
+      if ((b >> 5) == k) cb = v;
+    }
+    int n = 0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int i = lane + 32 * k;
+      n += (i < a.B && (c[k] > cb || (c[k] == cb && i < b))) ? 1 : 0;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+    if (lane == 0) seq[n] = (uint8_t)b;
+  }
+}
+
+struct TcUnit {
+  int item;  // position of the (sequence, kv head) item in the order
+  int b, g, chunk, piece, ctx, blk0, blk_end, ntiles;
+};
+
+// The item of unit u of the tensor-core forms: item u / nchunks (chunk u mod
+// nchunks) or, with a balanced tail, the whole items first and then the
+// pieces of the last tail_items items. Item i is kv head i mod Hkv of the
+// sequence at position i / Hkv of the order.
+__device__ __forceinline__ int tc_unit_item(const Args& a, int u) {
+  if (a.tail_pieces > 0) {
+    const int nwhole = a.B * a.Hkv - a.tail_items;
+    return u < nwhole ? u : nwhole + (u - nwhole) / a.tail_pieces;
+  }
+  return u / a.nchunks;
+}
+
+// The sequence at position pos of the order: seq from lpt_order, or pos
+// itself (seq null).
+__device__ __forceinline__ int tc_seq_at(const uint8_t* seq, int pos) { return seq ? (int)seq[pos] : pos; }
+
+// Unit u, whose item belongs to sequence b (tc_seq_at of the item's position).
+__device__ __forceinline__ TcUnit tc_unit(const Args& a, int u, int b) {
+  TcUnit t;
+  t.piece = -1;
+  t.chunk = 0;
+  t.item = tc_unit_item(a, u);
+  if (a.tail_pieces > 0) {
+    const int nwhole = a.B * a.Hkv - a.tail_items;
+    t.piece = u < nwhole ? -1 : (u - nwhole) % a.tail_pieces;
+  } else {
+    t.chunk = u % a.nchunks;
+  }
+  t.b = b;
+  t.g = t.item % a.Hkv;
+  t.ctx = seq_ctx(a, t.b);
+  const int nblk_seq = (t.ctx + kBlk - 1) / kBlk;
+  t.blk0 = t.chunk * a.chunk_blocks;
+  t.blk_end = min(t.blk0 + a.chunk_blocks, nblk_seq);
+  if (t.piece >= 0) {  // piece k of p: tiles [k T / p, (k + 1) T / p) of the item's T tiles
+    const int T = (nblk_seq + tca::kTileBlk - 1) / tca::kTileBlk;
+    t.blk0 = (t.piece * T / a.tail_pieces) * tca::kTileBlk;
+    t.blk_end = min(((t.piece + 1) * T / a.tail_pieces) * tca::kTileBlk, nblk_seq);
+  }
+  t.ntiles = t.blk0 < t.blk_end ? (t.blk_end - t.blk0 + tca::kTileBlk - 1) / tca::kTileBlk : 0;
+  return t;
+}
+
 // One 128-token tile of the online softmax for one query row (a thread) of
 // the tensor-core forms, in the log2 domain: sv holds the row's raw q.k
 // products (scaled in place), columns 0 .. vl are visible (the others become
@@ -760,10 +853,18 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
   __shared__ __align__(8) uint64_t bars[2 * kStages + 6];
   __shared__ uint32_t tmem_base_sh;
   __shared__ float xm[2][128];  // the odd group's final (m, l) per row
+  __shared__ uint8_t lpt_seq[kLptMaxB];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Work unit: a chunk of one (sequence, kv head) on a 3-D grid, or, with a
-  // balanced tail, a 1-D list: the whole items first, then the pieces of the
-  // last tail_items items (piece >= 0).
+  grid_dependency_wait();  // q, the tables and the cache may come from the previous kernel
+  allow_dependent_launch();
+  if (smem_addr(smem_raw) & 1023u) {  // the layout needs a 1024-byte aligned region
+    if (threadIdx.x == 0) atomicOr(&g_attn_error, kErrBadInput);
+    return;
+  }
+  // Work unit: a chunk of one (sequence position, kv head) on a 3-D grid, or,
+  // with a balanced tail, a 1-D list: the whole items first, then the pieces
+  // of the last tail_items items (piece >= 0), in the longest-first order of
+  // the persistent form (so that both forms split the same items)
   int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z, piece = -1, item = 0;
   if (a.tail_pieces > 0) {
     const int nwhole = a.B * a.Hkv - a.tail_items;
@@ -773,15 +874,16 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
     chunk = 0;
     b = item / a.Hkv;
     g = item % a.Hkv;
-  }
-  grid_dependency_wait();  // q, the tables and the cache may come from the previous kernel
-  allow_dependent_launch();
-  if (smem_addr(smem_raw) & 1023u) {  // the layout needs a 1024-byte aligned region
-    if (threadIdx.x == 0) atomicOr(&g_attn_error, kErrBadInput);
-    return;
+    if (a.lpt) {  // uniform across the grid
+      lpt_order(a, lpt_seq);
+      __syncthreads();
+      b = lpt_seq[b];
+      if (blockIdx.x == 0)  // for the tail merge
+        for (int p = threadIdx.x; p < a.B; p += blockDim.x) a.tail_seq[p] = lpt_seq[p];
+    }
   }
   const int ctx = seq_ctx(a, b);
-  if (chunk == 0 && g == 0 && threadIdx.x == 0) {
+  if (chunk == 0 && g == 0 && piece <= 0 && threadIdx.x == 0) {
     const int raw = a.ctx[b];
     if (raw < a.W || raw != ctx) atomicOr(&g_attn_error, kErrBadInput);
   }
@@ -1136,40 +1238,6 @@ constexpr int kThreads = 352;  // gather K (warp 0), MMA (1), softmax (2-9), gat
 constexpr int kVWarp = 10;
 }  // namespace tcp
 
-struct TcUnit {
-  int item, b, g, chunk, piece, ctx, blk0, blk_end, ntiles;
-};
-
-// Unit u of the tensor-core forms: chunk u mod nchunks of item u / nchunks,
-// or, with a balanced tail, the whole items first and then the pieces of the
-// last tail_items items.
-__device__ __forceinline__ TcUnit tc_unit(const Args& a, int u) {
-  TcUnit t;
-  t.piece = -1;
-  t.chunk = 0;
-  if (a.tail_pieces > 0) {
-    const int nwhole = a.B * a.Hkv - a.tail_items;
-    t.item = u < nwhole ? u : nwhole + (u - nwhole) / a.tail_pieces;
-    t.piece = u < nwhole ? -1 : (u - nwhole) % a.tail_pieces;
-  } else {
-    t.item = u / a.nchunks;
-    t.chunk = u % a.nchunks;
-  }
-  t.b = t.item / a.Hkv;
-  t.g = t.item % a.Hkv;
-  t.ctx = seq_ctx(a, t.b);
-  const int nblk_seq = (t.ctx + kBlk - 1) / kBlk;
-  t.blk0 = t.chunk * a.chunk_blocks;
-  t.blk_end = min(t.blk0 + a.chunk_blocks, nblk_seq);
-  if (t.piece >= 0) {  // piece k of p: tiles [k T / p, (k + 1) T / p) of the item's T tiles
-    const int T = (nblk_seq + tca::kTileBlk - 1) / tca::kTileBlk;
-    t.blk0 = (t.piece * T / a.tail_pieces) * tca::kTileBlk;
-    t.blk_end = min(((t.piece + 1) * T / a.tail_pieces) * tca::kTileBlk, nblk_seq);
-  }
-  t.ntiles = t.blk0 < t.blk_end ? (t.blk_end - t.blk0 + tca::kTileBlk - 1) / tca::kTileBlk : 0;
-  return t;
-}
-
 // Eleven warps: three share each of three SM sub-partitions, whose 16K
 // registers then allow at most 168 per thread.
 __global__ void __maxnreg__(168)
@@ -1182,8 +1250,9 @@ __global__ void __maxnreg__(168)
   // xm_empty, fin
   __shared__ __align__(8) uint64_t bars[4 * kStages + 18];
   __shared__ uint32_t tmem_base_sh;
-  __shared__ int unit_sh[2];
+  __shared__ int2 unit_sh[2];   // (unit, its sequence) handed from the queue to the other roles
   __shared__ float xm[2][128];  // the odd group's (m, l) per row for the unit being combined
+  __shared__ uint8_t lpt_seq[kLptMaxB];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dependency_wait();  // q, the tables, the cache and the queue's counters come from earlier kernels
   allow_dependent_launch();
@@ -1226,11 +1295,15 @@ __global__ void __maxnreg__(168)
     mbar_init(fin, 1);
     fence_mbar_init();
   }
+  lpt_order(a, lpt_seq);
+  const uint8_t* useq = a.lpt ? lpt_seq : nullptr;
   if (warp == 1) tmem_alloc(smem_addr(&tmem_base_sh), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  if (blockIdx.x == 0 && a.lpt && a.tail_pieces > 0)  // for the tail merge
+    for (int p = threadIdx.x; p < a.B; p += blockDim.x) a.tail_seq[p] = lpt_seq[p];
 
   if (warp == 0) {
     // ---------------- queue, Q and K gather ----------------
@@ -1248,12 +1321,13 @@ __global__ void __maxnreg__(168)
       if (lane == 0) u = (int)atomicAdd(a.ctr, 1u);
       u = __shfl_sync(0xffffffffu, u, 0);
       if (u >= units) u = -1;
+      const int ub = u < 0 ? 0 : tc_seq_at(useq, tc_unit_item(a, u) / a.Hkv);
       if (lane == 0) {
-        unit_sh[slot] = u;
+        unit_sh[slot] = make_int2(u, ub);
         mbar_arrive(u_full + 8 * slot);
       }
       if (u < 0) break;
-      const TcUnit t = tc_unit(a, u);
+      const TcUnit t = tc_unit(a, u, ub);
       if (lane == 0 && t.chunk == 0 && t.g == 0 && t.piece <= 0) {
         const int raw = a.ctx[t.b];
         if (raw < a.W || raw != t.ctx) atomicOr(&g_attn_error, kErrBadInput);
@@ -1333,11 +1407,12 @@ __global__ void __maxnreg__(168)
         ok = false;
         break;
       }
-      const int u = unit_sh[slot];
+      const int2 uv = unit_sh[slot];
+      const int u = uv.x;
       __syncwarp();
       if (lane == 0) mbar_arrive(u_empty + 8 * slot);
       if (u < 0) break;
-      const TcUnit t = tc_unit(a, u);
+      const TcUnit t = tc_unit(a, u, uv.y);
       const int64_t tab_row = (int64_t)t.b * a.max_blocks;
       const int nblk = t.blk_end - t.blk0;
       int tab = 0;
@@ -1411,10 +1486,11 @@ __global__ void __maxnreg__(168)
           ok = false;
           break;
         }
-        const int u = unit_sh[slot];
+        const int2 uv = unit_sh[slot];
+        const int u = uv.x;
         mbar_arrive(u_empty + 8 * slot);
         if (u < 0) break;
-        const TcUnit t = tc_unit(a, u);
+        const TcUnit t = tc_unit(a, u, uv.y);
         if (t.ntiles == 0) {
           // The last P V of the previous unit waits for no S here: issued now.
           // (Held back, it would wait for the next unit with tiles, which the
@@ -1478,11 +1554,12 @@ __global__ void __maxnreg__(168)
         ok = false;
         break;
       }
-      const int u = unit_sh[slot];
+      const int2 uv = unit_sh[slot];
+      const int u = uv.x;
       __syncwarp();
       if (lane == 0) mbar_arrive(u_empty + 8 * slot);
       if (u < 0) break;
-      const TcUnit t = tc_unit(a, u);
+      const TcUnit t = tc_unit(a, u, uv.y);
       const int tail_row0 = (t.item - (a.B * a.Hkv - a.tail_items)) * a.QR;  // pieces: first tail row of the item
       if (t.ntiles == 0) {  // nothing of the sequence in this unit
         if (grp == 0 && t.piece >= 0) {  // an empty piece: (m, l, o) = (-inf, 0, 0)
@@ -1681,12 +1758,13 @@ __global__ void __maxnreg__(168)
 // The balanced tail's merge: one warp per query row of a split item combines
 // its pieces' (o, m, l) in piece order.
 __global__ void __launch_bounds__(128) attn_tail_merge_kernel(const Args a) {
-  grid_dependency_wait();  // the partials come from the tensor-core kernel
+  grid_dependency_wait();  // the partials and the order come from the tensor-core kernel
   allow_dependent_launch();
   const int t = (int)blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= a.tail_items * a.QR) return;
   const int item = a.B * a.Hkv - a.tail_items + t / a.QR, r = t % a.QR;
-  const int b = item / a.Hkv, g = item % a.Hkv;
+  const int pos = item / a.Hkv, g = item % a.Hkv;
+  const int b = a.lpt ? (int)a.tail_seq[pos] : pos;  // the tail items are the last ones of its order
   const int P = a.tail_pieces;
   const float* ml = a.tail_ml + (int64_t)t * P * 2;
   float mstar = kNegInf;
@@ -1994,8 +2072,8 @@ AttnPlan plan_attn(int b, int w, int hq, int hkv, int max_context, int num_sms, 
   }
   const size_t rows = (size_t)b * w * hq;
   p.ws_bytes = p.nchunks > 1 ? kCounterBytes + rows * p.nchunks * (kD + 2) * sizeof(float) : 0;
-  if (p.tail_pieces > 0)
-    p.ws_bytes = kCounterBytes + (size_t)p.tail_items * qr * p.tail_pieces * (kD + 2) * sizeof(float);
+  if (p.tail_pieces > 0)  // partials, then the longest-first order of the sequences
+    p.ws_bytes = kCounterBytes + (size_t)p.tail_items * qr * p.tail_pieces * (kD + 2) * sizeof(float) + kLptMaxB;
   if (p.persist > 0) p.ws_bytes = std::max(p.ws_bytes, kCounterBytes);
   return p;
 }
@@ -2026,12 +2104,18 @@ cudaError_t launch_attn(const AttnLaunch& l, const AttnPlan& p, cudaStream_t s) 
   a.tail_items = p.tail_items;
   a.tail_pieces = p.tail_pieces;
   a.ctr = p.persist > 0 ? static_cast<unsigned*>(l.workspace) : nullptr;
+  {  // test hook: DQD_ATTN_ORDER=0 keeps the sequences in index order
+    const char* env = std::getenv("DQD_ATTN_ORDER");
+    a.lpt = p.tc && l.b <= kLptMaxB && !(env && env[0] == '0') ? 1 : 0;
+  }
   a.tail_o = nullptr;
   a.tail_ml = nullptr;
+  a.tail_seq = nullptr;
   if (p.tail_pieces > 0) {
     const size_t trows = (size_t)p.tail_items * (l.hq / l.hkv) * l.w;
     a.tail_o = reinterpret_cast<float*>(static_cast<uint8_t*>(l.workspace) + kCounterBytes);
     a.tail_ml = a.tail_o + trows * p.tail_pieces * kD;
+    a.tail_seq = reinterpret_cast<uint8_t*>(a.tail_ml + trows * p.tail_pieces * 2);
   }
   a.num_blocks = l.num_blocks;
   a.max_blocks = l.max_blocks;

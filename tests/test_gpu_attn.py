@@ -289,13 +289,15 @@ def test_tensor_core_balanced_tail(dev, dqd, monkeypatch, B, W, hq, hkv):
     (40, 16, 64, 8, 16, 900, None),   # 128 rows (one Q slot)
     (64, 6, 32, 8, 200, 2000, 8),     # 24 rows, 8-block chunks: many units per CTA, empty ones too
     (20, 16, 64, 8, 256, 1500, None), # 128 rows, a balanced tail of eight pieces per item
+    (300, 6, 32, 8, 64, 400, None),   # more sequences than the longest-first order covers: index order
 ])
 def test_tensor_core_persistent_queue(dev, dqd, monkeypatch, B, W, hq, hkv, lo, hi, cb):
     """The persistent tcgen05 form with many units per CTA, taken from the
-    queue in the workspace's counter region: the same bits as one CTA per unit
-    (the two softmax groups' accumulators are combined symmetrically, so the
-    schedule cannot change the result), the same bits on reruns over one
-    workspace, and the queue's counters back at zero after every call."""
+    queue in the workspace's counter region (longest contexts first, up to 256
+    sequences): the same bits as one CTA per unit (the two softmax groups'
+    accumulators are combined symmetrically, so the schedule cannot change the
+    result), the same bits on reruns over one workspace, and the queue's
+    counters back at zero after every call."""
     if cb is not None:
         monkeypatch.setenv("DQD_ATTN_CHUNK_BLOCKS", str(cb))
     rng = np.random.default_rng(B * 1000 + W * 10 + hq)
