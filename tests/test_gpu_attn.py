@@ -289,6 +289,7 @@ def test_tensor_core_balanced_tail(dev, dqd, monkeypatch, B, W, hq, hkv):
     (40, 16, 64, 8, 16, 900, None),   # 128 rows (one Q slot)
     (64, 6, 32, 8, 200, 2000, 8),     # 24 rows, 8-block chunks: many units per CTA, empty ones too
     (20, 16, 64, 8, 256, 1500, None), # 128 rows, a balanced tail of eight pieces per item
+    (256, 6, 32, 8, 64, 400, None),   # the most sequences the longest-first order covers
     (300, 6, 32, 8, 64, 400, None),   # more sequences than the longest-first order covers: index order
 ])
 def test_tensor_core_persistent_queue(dev, dqd, monkeypatch, B, W, hq, hkv, lo, hi, cb):
