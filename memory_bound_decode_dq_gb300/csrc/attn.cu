@@ -1210,12 +1210,13 @@ __global__ void __launch_bounds__(tca::kThreads, 1)
 // empty resets it), so that the tiles of successive units flow through one
 // pipeline instead of each CTA paying its own start-up and drain:
 //  * warp 0 takes the next unit once it has issued the copies of the current
-//    one, hands it to the other roles through a two-slot queue in shared
+//    one (units in the longest-first order of their sequences), hands it and
+//    its sequence to the other roles through a two-slot queue in shared
 //    memory, loads its Q by TMA (into a second Q slot when the unit has at
 //    most 64 query rows, so that it lands while the current Q is in use) and
-//    gathers its tiles into the same three stages;
-//  * tiles are numbered across units: tile J uses stage J mod 3, the S buffer
-//    and softmax group of J's parity, whatever unit it belongs to;
+//    gathers its K tiles; warp 10 gathers the V tiles of the same units;
+//  * tiles are numbered across units: tile J uses K and V slot J mod 3, the S
+//    buffer and softmax group of J's parity, whatever unit it belongs to;
 //  * warp 1 issues S of a unit's first tile before P V of the previous unit's
 //    last tile, and the first P V of a unit (which starts an O accumulator
 //    afresh) only after the even group has read both accumulators of the
