@@ -1766,6 +1766,10 @@ __global__ void __launch_bounds__(128) attn_tail_merge_kernel(const Args a) {
   const int item = a.B * a.Hkv - a.tail_items + t / a.QR, r = t % a.QR;
   const int pos = item / a.Hkv, g = item % a.Hkv;
   const int b = a.lpt ? (int)a.tail_seq[pos] : pos;  // the tail items are the last ones of its order
+  if (b >= a.B) {  // the order was not written (the tensor-core kernel bailed out): flag, write nothing
+    if (lane == 0) atomicOr(&g_attn_error, kErrBadInput);
+    return;
+  }
   const int P = a.tail_pieces;
   const float* ml = a.tail_ml + (int64_t)t * P * 2;
   float mstar = kNegInf;
