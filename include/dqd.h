@@ -273,6 +273,11 @@ DQD_API dqd_status dq_gemm(const dqd_weight* w, const uint16_t* x_bf16, int64_t 
  *  - a block-table entry outside [0, num_blocks) is clamped into range;
  *  - a context_lens[b] above max_context is taken as max_context;
  *  - a query row that sees no key (context_lens[b] < w) is written as zeros.
+ * Workspace (size from gqa_decode_attn_workspace_bytes for the same b, w, hq,
+ * hkv, d, max_context on the same device): the split-KV partials and, for
+ * 17-128 query rows per kv head, the pieces of a balanced last wave, the
+ * order of the sequences, and a work queue in the counter region when there
+ * are more work units than SMs; so it can be needed with a single split.
  * ---------------------------------------------------------------------- */
 DQD_API dqd_status gqa_decode_attn_workspace_bytes(int32_t b, int32_t w, int32_t hq,
                                            int32_t hkv, int32_t d,
